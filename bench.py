@@ -1,0 +1,331 @@
+"""Benchmark of the flat-shard optimizer step on the Llama-7B-shaped flat buffer.
+
+One step = the whole hot path over one batch of synthetic grads:
+  flatten/cast of the 291 bf16 per-tensor grads into the fp32 flat grad (K1)
+  -> deterministic grad norm + clip coefficient (K3, two launches)
+  -> fused AdamW on fp32 master/exp_avg/exp_avg_sq with the bf16 write-back (K4)
+  -> device->host read of the step's grad norm (the skip-policy decision).
+Inputs are resident in HBM (135 GB, far larger than the 129 MB L2, so no
+flush is needed between steps).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (plain single-threaded C) on a bounded
+sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "fused AdamW shard step: params/s and HBM GB/s as % of GB300 peak (Llama-7B flat)"
+UNIT = "params/s"
+ADAMW_BYTES_PER_PARAM = 30      # read g,p,m,v fp32; write p,m,v fp32 + bf16 copy
+FLATTEN_BYTES_PER_PARAM = 6     # read bf16 grad, write fp32 flat grad
+SQNORM_BYTES_PER_PARAM = 4      # read fp32 flat grad
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "adamw_llama7b_traffic.txt")
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def adamw_traffic_per_param():
+    """DRAM bytes per parameter of the AdamW kernel from the committed ncu summary, if current."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if line.startswith("dram_bytes_per_param:"):
+                    return float(line.split(":", 1)[1])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- oracle
+def oracle_step_rate(wl: W.Workload, sample_params: int, min_seconds: float, max_passes: int):
+    """Time the oracle's whole step (flatten/cast, sum of squares, clip, AdamW) on
+    the first `sample_params` params of the workload, single-threaded."""
+    import oracle
+    numels, tot = [], 0
+    for n in wl.numels:
+        take = min(n, sample_params - tot)
+        if take <= 0:
+            break
+        numels.append(take)
+        tot += take
+    g = torch.Generator().manual_seed(wl.seed)
+    grads = [(torch.randn(n, generator=g) * wl.grad_std).to(torch.bfloat16).view(torch.int16).numpy()
+             .view(np.uint16) for n in numels]
+    p = (torch.randn(tot, generator=g) * wl.init_std).numpy()
+    st = oracle.new_state(p)
+    flat = np.empty(tot, np.float32)
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.flatten(grads, numels, "bf16", 0, tot, 1.0, flat, accumulate=False)
+        sq = oracle.sqnorm(flat)
+        cr = oracle.clip(sq, 0.0, wl.max_norm)
+        st.t += 1
+        sc = oracle.adamw_scalars(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay, st.t)
+        oracle.adamw(st.p, st.m, st.v, flat, sc, cr.coef, st.lowp)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or passes >= max_passes:
+            break
+    return tot * passes / el, tot, passes, el
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    wl = W.llama7b()
+    sample = 1 << 24
+    # warm-up passes, then K timed passes, each one oracle step over the sample
+    oracle_step_rate(wl, sample, 0.0, max(args.warmup, 1))
+    rate, tot, passes, el = oracle_step_rate(wl, sample, 0.0, args.steps)
+    cores = 1
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / passes,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "llama7b_flat (oracle sample)", "params_per_step": tot, "world_size": 1, "rank": 0},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"first {tot} params of the Llama-7B flat list, whole step per pass"},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------------ GPU
+def run_gpu(args):
+    from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    base = W.llama7b()
+    # weak scaling: the flat parameter list is `world` copies of the Llama-7B
+    # list, so every rank's ZeRO shard is exactly one Llama-7B-shaped buffer
+    wl = base.with_(numels=base.numels * world, world_size=world, rank=rank)
+    s, e = zs.zero_shard_range(wl.total, world, rank)
+    n = e - s
+    shard_numels = list(base.numels)
+    torch.manual_seed(0)
+
+    # per-tensor bf16 grads of this rank's shard, one padded storage buffer
+    tg = W.tensor_grads(base.with_(seed=base.seed + rank), step=1, micro=0, device=dev)
+    master = W.master_init(wl, s, e, device=dev)
+    opt = FlatShardAdamW(shard_numels, lr=wl.lr, betas=wl.betas, eps=wl.eps, weight_decay=wl.weight_decay,
+                         max_norm=wl.max_norm, device=dev, master=master)
+    del master
+    grads = tg.tensors
+    d_table = opt._table(grads)
+    stream = torch.cuda.current_stream(dev)
+    grad_bytes = sum(t.numel() * t.element_size() for t in grads)
+
+    def one_step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        zs.zero_flatten_cast(d_table, len(grads), opt.total, torch.bfloat16, 0, n, 1.0, False, opt.grad, None,
+                             stream)
+        if ev is not None:
+            ev[1].record(stream)
+        zs.zero_grad_sqnorm(opt.grad, 0.0, opt.max_norm, opt.ws, opt.norm_buf, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        zs.zero_adamw_step(opt.master, opt.exp_avg, opt.exp_avg_sq, opt.grad, opt.lowp, opt.lr, opt.betas[0],
+                           opt.betas[1], opt.eps, opt.weight_decay, opt.t + 1, opt.norm_buf, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        r = opt.finish_step()  # device->host read of the step's result
+        if not r.finite:
+            raise RuntimeError("non-finite grad norm in the benchmark")
+        return r
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if pg is not None:
+            pg.barrier()
+
+    for _ in range(args.warmup):
+        one_step()
+    kernel_events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for k in range(args.steps):
+            one_step(kernel_events[k])
+        t_end.record(stream)
+        barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    k1 = [ev[0].elapsed_time(ev[1]) for ev in kernel_events]
+    k3 = [ev[1].elapsed_time(ev[2]) for ev in kernel_events]
+    k4 = [ev[2].elapsed_time(ev[3]) for ev in kernel_events]
+
+    # ---- end to end through the public API with host buffers
+    host = torch.empty(tg.storage.numel(), dtype=tg.storage.dtype, pin_memory=True)
+    host.copy_(tg.storage)
+    for _ in range(max(1, args.warmup // 2)):
+        tg.storage.copy_(host, non_blocking=True)
+        one_step()
+    barrier()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        tg.storage.copy_(host, non_blocking=True)
+        one_step()
+    e_end.record(stream)
+    barrier()
+    e2e_ms = e_start.elapsed_time(e_end)
+
+    if pg is not None:
+        t = torch.tensor([elapsed_ms, e2e_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed_ms, e2e_ms = t.tolist()
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return 0
+
+    peaks, peak_src = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    t_k4 = statistics.mean(k4) / 1e3
+    achieved = ADAMW_BYTES_PER_PARAM * n / t_k4 / 1e9
+    tpp = adamw_traffic_per_param()
+    value = n * world * args.steps / (elapsed_ms / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "llama7b_flat", "params_per_rank": n, "tensors": len(grads), "world_size": world,
+                   "grad_dtype": "bf16", "lowp_dtype": "bf16", "max_norm": wl.max_norm,
+                   "l2": "inputs larger than L2 (135 GB resident per GPU); no flush"},
+        "roofline": {"bound": "hbm", "kernel": "adamw_v8_kernel", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "peak_source": peak_src,
+                     "traffic": None if tpp is None else tpp * n,
+                     "algorithmic_bytes_per_launch": ADAMW_BYTES_PER_PARAM * n},
+        "kernels_ms": {"flatten": statistics.mean(k1), "grad_norm": statistics.mean(k3), "adamw": statistics.mean(k4)},
+        "kernels_gbs": {"flatten": FLATTEN_BYTES_PER_PARAM * n / (statistics.mean(k1) / 1e3) / 1e9,
+                        "grad_norm": SQNORM_BYTES_PER_PARAM * n / (statistics.mean(k3) / 1e3) / 1e9,
+                        "adamw": achieved},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+        "e2e": {"value": n * world * args.steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": grad_bytes,
+                "d2h_bytes_per_step": zs.NORM_RESULT_BYTES, "ms_per_step": e2e_ms / args.steps},
+    }
+    if not args.no_cpu_baseline and world == 1:
+        rate, tot, passes, el = oracle_step_rate(base, 1 << 25, 10.0, 50)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"first {tot} params of the Llama-7B flat list, {passes} whole-step "
+                                          f"passes in {el:.1f} s"}
+    print(json.dumps(line))
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,202 @@
+// api.cu -- the C-ABI entry points of libzeroshard (declared in
+// include/zero_shard.h): argument checking, per-step scalars, dispatch to the
+// kernel launchers, and the per-thread error message.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace zs {
+
+static thread_local char g_msg[512] = "";
+
+zero_status fail(zero_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+zero_status check_launch(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(ZERO_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+  return ZERO_OK;
+}
+
+namespace {
+struct GridEntry {
+  int device;
+  const void* kernel;
+  int threads;
+  size_t smem;
+  int blocks;
+};
+std::mutex g_grid_mu;
+std::vector<GridEntry> g_grid;
+}  // namespace
+
+int persistent_blocks(const void* kernel, int threads, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  {
+    std::lock_guard<std::mutex> lk(g_grid_mu);
+    for (const GridEntry& e : g_grid)
+      if (e.device == dev && e.kernel == kernel && e.threads == threads && e.smem == smem) return e.blocks;
+  }
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const int blocks = sms * per_sm;
+  std::lock_guard<std::mutex> lk(g_grid_mu);
+  g_grid.push_back({dev, kernel, threads, smem, blocks});
+  return blocks;
+}
+
+static bool valid_dtype(int d) { return d == ZERO_F32 || d == ZERO_BF16 || d == ZERO_F16; }
+
+}  // namespace zs
+
+using zs::fail;
+
+extern "C" {
+
+const char* zero_status_string(zero_status s) {
+  switch (s) {
+    case ZERO_OK: return "ZERO_OK";
+    case ZERO_EINVAL: return "ZERO_EINVAL: invalid argument";
+    case ZERO_ECUDA: return "ZERO_ECUDA: CUDA runtime error";
+  }
+  return "unknown zero_status";
+}
+
+const char* zero_last_error(void) { return zs::g_msg; }
+
+zero_status zero_shard_range(int64_t total, int32_t world_size, int32_t rank, int64_t* start, int64_t* end) {
+  if (start == nullptr || end == nullptr) return fail(ZERO_EINVAL, "zero_shard_range: NULL output");
+  if (total < 0) return fail(ZERO_EINVAL, "zero_shard_range: total %lld < 0", (long long)total);
+  if (world_size < 1) return fail(ZERO_EINVAL, "zero_shard_range: world_size %d < 1", world_size);
+  if (rank < 0 || rank >= world_size)
+    return fail(ZERO_EINVAL, "zero_shard_range: rank %d not in [0, %d)", rank, world_size);
+  // chunk = ceil(total / world) without overflow for totals near INT64_MAX
+  const int64_t chunk = total / world_size + (total % world_size != 0 ? 1 : 0);
+  const int64_t s = (chunk != 0 && rank > (total / chunk)) ? total : static_cast<int64_t>(rank) * chunk;
+  const int64_t lo = s < total ? s : total;
+  const int64_t hi = (chunk > total - lo) ? total : lo + chunk;
+  *start = lo;
+  *end = hi;
+  return ZERO_OK;
+}
+
+zero_status zero_tensor_table(const void* const* ptrs, const int64_t* numels, int32_t n_tensors,
+                              zero_tensor* table, int64_t* total) {
+  if (n_tensors < 0) return fail(ZERO_EINVAL, "zero_tensor_table: n_tensors %d < 0", n_tensors);
+  if (total == nullptr) return fail(ZERO_EINVAL, "zero_tensor_table: NULL total");
+  if (n_tensors > 0 && (numels == nullptr || table == nullptr))
+    return fail(ZERO_EINVAL, "zero_tensor_table: NULL numels or table");
+  int64_t acc = 0;
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    if (numels[i] < 0) return fail(ZERO_EINVAL, "zero_tensor_table: numel[%d] = %lld < 0", i, (long long)numels[i]);
+    if (numels[i] > INT64_MAX - acc) return fail(ZERO_EINVAL, "zero_tensor_table: total overflows int64");
+    acc += numels[i];
+  }
+  int64_t off = 0;
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    table[i].ptr = ptrs ? ptrs[i] : nullptr;
+    table[i].numel = numels[i];
+    table[i].flat_offset = off;
+    off += numels[i];
+  }
+  *total = acc;
+  return ZERO_OK;
+}
+
+zero_status zero_flatten_cast(const zero_tensor* d_table, int32_t n_tensors, int64_t total, zero_dtype src_dtype,
+                              int64_t shard_start, int64_t shard_end, float scale, int32_t accumulate,
+                              float* d_dst, int32_t* d_found_nonfinite, void* stream) {
+  if (n_tensors < 0) return fail(ZERO_EINVAL, "zero_flatten_cast: n_tensors %d < 0", n_tensors);
+  if (n_tensors > 0 && d_table == nullptr) return fail(ZERO_EINVAL, "zero_flatten_cast: NULL d_table");
+  if (total < 0 || (n_tensors == 0 && total != 0))
+    return fail(ZERO_EINVAL, "zero_flatten_cast: total %lld does not fit %d tensors", (long long)total, n_tensors);
+  if (shard_start < 0 || shard_start > shard_end || shard_end > total)
+    return fail(ZERO_EINVAL, "zero_flatten_cast: shard [%lld, %lld) outside [0, %lld]", (long long)shard_start,
+                (long long)shard_end, (long long)total);
+  if (!zs::valid_dtype(src_dtype)) return fail(ZERO_EINVAL, "zero_flatten_cast: bad src_dtype %d", (int)src_dtype);
+  if (accumulate != 0 && accumulate != 1) return fail(ZERO_EINVAL, "zero_flatten_cast: accumulate must be 0 or 1");
+  if (!std::isfinite(scale)) return fail(ZERO_EINVAL, "zero_flatten_cast: non-finite scale");
+  if (shard_end > shard_start && d_dst == nullptr) return fail(ZERO_EINVAL, "zero_flatten_cast: NULL d_dst");
+  if (shard_end == shard_start) return ZERO_OK;
+  return zs::launch_flatten(d_table, n_tensors, src_dtype, shard_start, shard_end, scale, accumulate, d_dst,
+                            d_found_nonfinite, zs::as_stream(stream));
+}
+
+zero_status zero_accum(float* d_acc, const void* d_src, zero_dtype src_dtype, int64_t n, float scale,
+                       int32_t accumulate, int32_t* d_found_nonfinite, void* stream) {
+  if (n < 0) return fail(ZERO_EINVAL, "zero_accum: n %lld < 0", (long long)n);
+  if (!zs::valid_dtype(src_dtype)) return fail(ZERO_EINVAL, "zero_accum: bad src_dtype %d", (int)src_dtype);
+  if (accumulate != 0 && accumulate != 1) return fail(ZERO_EINVAL, "zero_accum: accumulate must be 0 or 1");
+  if (!std::isfinite(scale)) return fail(ZERO_EINVAL, "zero_accum: non-finite scale");
+  if (n > 0 && (d_acc == nullptr || d_src == nullptr)) return fail(ZERO_EINVAL, "zero_accum: NULL buffer");
+  if (n == 0) return ZERO_OK;
+  return zs::launch_accum(d_acc, d_src, src_dtype, n, scale, accumulate, d_found_nonfinite, zs::as_stream(stream));
+}
+
+size_t zero_grad_sqnorm_workspace_bytes(int64_t n) {
+  if (n <= 0) return 0;
+  return static_cast<size_t>((n + zs::kSqTile - 1) / zs::kSqTile) * sizeof(double);
+}
+
+zero_status zero_grad_sqnorm(const float* d_grad, int64_t n, double extra_sqnorm, double max_norm, void* d_ws,
+                             size_t ws_bytes, zero_norm_result* d_out, void* stream) {
+  if (n < 0) return fail(ZERO_EINVAL, "zero_grad_sqnorm: n %lld < 0", (long long)n);
+  if (n > 0 && d_grad == nullptr) return fail(ZERO_EINVAL, "zero_grad_sqnorm: NULL d_grad");
+  if (d_out == nullptr) return fail(ZERO_EINVAL, "zero_grad_sqnorm: NULL d_out");
+  if (std::isnan(max_norm) || max_norm < 0.0) return fail(ZERO_EINVAL, "zero_grad_sqnorm: bad max_norm");
+  if (!std::isfinite(extra_sqnorm) || extra_sqnorm < 0.0)
+    return fail(ZERO_EINVAL, "zero_grad_sqnorm: bad extra_sqnorm");
+  const size_t need = zero_grad_sqnorm_workspace_bytes(n);
+  if (need > 0 && (d_ws == nullptr || ws_bytes < need))
+    return fail(ZERO_EINVAL, "zero_grad_sqnorm: workspace %zu bytes < %zu needed", d_ws ? ws_bytes : 0, need);
+  if (need > 0 && !zs::aligned(d_ws, 8)) return fail(ZERO_EINVAL, "zero_grad_sqnorm: workspace not 8-byte aligned");
+  return zs::launch_sqnorm(d_grad, n, extra_sqnorm, max_norm, static_cast<double*>(d_ws), d_out,
+                           zs::as_stream(stream));
+}
+
+zero_status zero_adamw_step(float* d_master, float* d_exp_avg, float* d_exp_avg_sq, const float* d_grad,
+                            void* d_param_lowp, zero_dtype lowp_dtype, int64_t n, const zero_adamw_hparams* hp,
+                            int64_t step, const zero_norm_result* d_clip, void* stream) {
+  if (n < 0) return fail(ZERO_EINVAL, "zero_adamw_step: n %lld < 0", (long long)n);
+  if (hp == nullptr) return fail(ZERO_EINVAL, "zero_adamw_step: NULL hparams");
+  if (step < 1) return fail(ZERO_EINVAL, "zero_adamw_step: step %lld < 1", (long long)step);
+  if (n > 0 && (d_master == nullptr || d_exp_avg == nullptr || d_exp_avg_sq == nullptr || d_grad == nullptr))
+    return fail(ZERO_EINVAL, "zero_adamw_step: NULL state or grad buffer");
+  if (d_param_lowp != nullptr && lowp_dtype != ZERO_BF16 && lowp_dtype != ZERO_F16)
+    return fail(ZERO_EINVAL, "zero_adamw_step: lowp_dtype must be BF16 or F16");
+  const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
+  if (!(std::isfinite(lr) && lr >= 0.0)) return fail(ZERO_EINVAL, "zero_adamw_step: bad lr");
+  if (!(b1 >= 0.0 && b1 < 1.0 && b2 >= 0.0 && b2 < 1.0)) return fail(ZERO_EINVAL, "zero_adamw_step: bad betas");
+  if (!(std::isfinite(eps) && eps > 0.0)) return fail(ZERO_EINVAL, "zero_adamw_step: bad eps");
+  if (!(std::isfinite(wd) && wd >= 0.0)) return fail(ZERO_EINVAL, "zero_adamw_step: bad weight_decay");
+  if (n == 0) return ZERO_OK;
+  // per-step scalars in binary64, each rounded to binary32 once
+  const double bc1 = 1.0 - std::pow(b1, static_cast<double>(step));
+  const double bc2 = 1.0 - std::pow(b2, static_cast<double>(step));
+  zs::AdamScalars s;
+  s.step_size = static_cast<float>(lr / bc1);
+  s.bc2_sqrt = static_cast<float>(std::sqrt(bc2));
+  s.decay = static_cast<float>(1.0 - lr * wd);
+  s.b1 = static_cast<float>(b1);
+  s.omb1 = static_cast<float>(1.0 - b1);
+  s.b2 = static_cast<float>(b2);
+  s.omb2 = static_cast<float>(1.0 - b2);
+  s.eps = static_cast<float>(eps);
+  return zs::launch_adamw(d_master, d_exp_avg, d_exp_avg_sq, d_grad, d_param_lowp, lowp_dtype, n, s, d_clip,
+                          zs::as_stream(stream));
+}
+
+}  // extern "C"

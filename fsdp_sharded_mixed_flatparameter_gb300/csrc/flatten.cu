@@ -1,0 +1,312 @@
+// flatten.cu -- gradient flatten/cast into the FlatParameter layout (K1) and
+// flat micro-batch accumulation (K2).
+//
+// K1 implements the ZeRO page's _flatten_gradients (grad.view(-1).float(),
+// zeros for a tensor without grad, concatenated in list order) restricted to
+// the rank's shard, scaled by 1/accum_steps (LLaMA-13B gradient-accumulation
+// page) or 1/world_size, optionally added to the fp32 accumulator.  The
+// tensors are given as a device table {ptr, numel, flat_offset} sorted by
+// flat offset, so thousands of tensors take one launch (the memory-ledger
+// page's point about FlatParameter: one big operation instead of hundreds of
+// small ones with microsecond launch costs each).
+//
+// Work split: the shard's destination range is cut into tiles of 8192
+// elements; a persistent grid gives each block a contiguous run of tiles, so
+// one binary search over the table per block finds the first tensor and the
+// block then walks forward.  A tile that lies inside one tensor whose source
+// address is co-aligned with the destination is copied directly with 16- or
+// 32-byte loads and 32-byte stores.  Any other tile (tensor boundaries inside
+// it, a NULL grad, source and destination misaligned relative to each other)
+// is staged: the block reads each source segment with loads aligned to the
+// SOURCE, writes the scaled binary32 values to shared memory, and then
+// writes the destination with loads/stores aligned to the DESTINATION.  The
+// staging buffer is padded by one word per 8 (index q -> q + q/8) so that
+// both phases are free of shared-memory bank conflicts.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace zs {
+
+constexpr int kFlThreads = 256;
+constexpr int kFlTile = 8192;
+constexpr int kFlStage = kFlTile + kFlTile / 8;
+
+__device__ __forceinline__ int stage_idx(int q) { return q + (q >> 3); }
+
+// last i with table[i].flat_offset <= k (the tensor that holds flat index k)
+__device__ __forceinline__ int find_tensor(const zero_tensor* __restrict__ table, int n, int64_t k) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(&table[mid].flat_offset) <= k)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int DT>
+struct SrcTraits {
+  static constexpr int esize = (DT == ZERO_F32) ? 4 : 2;
+};
+
+// 8 consecutive source elements starting at a 32-byte (f32) or 16-byte
+// (16-bit) aligned address, widened to binary32.
+template <int DT>
+__device__ __forceinline__ void load8_src(const void* p, float (&x)[8]) {
+  if (DT == ZERO_F32) {
+    ld8_ro(static_cast<const float*>(p), x);
+  } else {
+    const uint4 w = ld16_ro(p);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = half_bits_to_f32<DT>(ws[j] & 0xffffu);
+      x[2 * j + 1] = half_bits_to_f32<DT>(ws[j] >> 16);
+    }
+  }
+}
+
+// Write fl(scale * x) of source elements [j0, j0 + len) into stage[q0 ...).
+template <int DT>
+__device__ __forceinline__ void stage_segment(const void* __restrict__ src, int64_t j0, int len, int q0,
+                                              float scale, float* stage, bool& bad) {
+  if (src == nullptr) {
+    const float y = __fmul_rn(scale, 0.0f);
+    for (int e = threadIdx.x; e < len; e += kFlThreads) stage[stage_idx(q0 + e)] = y;
+    return;
+  }
+  constexpr int es = SrcTraits<DT>::esize;
+  constexpr int vb = (DT == ZERO_F32) ? 32 : 16;  // bytes of one 8-element source vector
+  const char* sp = static_cast<const char*>(src) + es * j0;
+  int h = static_cast<int>(((vb - reinterpret_cast<uintptr_t>(sp) % vb) % vb) / es);
+  if (h > len) h = len;
+  const int nv = (len - h) / 8;
+  const int body_end = h + 8 * nv;
+  for (int e = threadIdx.x; e < h; e += kFlThreads) {
+    const float y = __fmul_rn(scale, load_elem<DT>(src, j0 + e));
+    bad |= !finite_f(y);
+    stage[stage_idx(q0 + e)] = y;
+  }
+  for (int vi = threadIdx.x; vi < nv; vi += kFlThreads) {
+    float x[8];
+    load8_src<DT>(sp + es * (h + 8 * vi), x);
+    const int q = q0 + h + 8 * vi;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float y = __fmul_rn(scale, x[i]);
+      bad |= !finite_f(y);
+      stage[stage_idx(q + i)] = y;
+    }
+  }
+  for (int e = body_end + threadIdx.x; e < len; e += kFlThreads) {
+    const float y = __fmul_rn(scale, load_elem<DT>(src, j0 + e));
+    bad |= !finite_f(y);
+    stage[stage_idx(q0 + e)] = y;
+  }
+}
+
+template <int DT, bool ACC>
+__global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* __restrict__ table, int n_tensors,
+                                                             int64_t shard_start, int64_t len, int64_t ntiles,
+                                                             float* __restrict__ dst, bool dst_vec, float scale,
+                                                             int32_t* __restrict__ flag) {
+  __shared__ float stage[kFlStage];
+  constexpr int es = SrcTraits<DT>::esize;
+  constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
+  const int64_t t0 = ntiles * blockIdx.x / gridDim.x;
+  const int64_t t1 = ntiles * (blockIdx.x + 1) / gridDim.x;
+  bool bad = false;
+  int ti = (t0 < t1) ? find_tensor(table, n_tensors, shard_start + t0 * kFlTile) : 0;
+
+  for (int64_t tile = t0; tile < t1; ++tile) {
+    const int64_t lo = tile * kFlTile;
+    const int tlen = static_cast<int>((len - lo < kFlTile) ? (len - lo) : kFlTile);
+    const int64_t klo = shard_start + lo, khi = klo + tlen;
+    while (ti + 1 < n_tensors && __ldg(&table[ti + 1].flat_offset) <= klo) ++ti;
+    const void* tptr = table[ti].ptr;
+    const int64_t toff = __ldg(&table[ti].flat_offset), tnum = __ldg(&table[ti].numel);
+    const char* tsrc = static_cast<const char*>(tptr) + es * (klo - toff);
+
+    const bool direct = tlen == kFlTile && dst_vec && tptr != nullptr && toff <= klo && khi <= toff + tnum &&
+                        reinterpret_cast<uintptr_t>(tsrc) % vb == 0;
+    if (direct) {
+      // 1024 groups of 8; each thread takes 4, all loads first
+      float x[4][8];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) load8_src<DT>(tsrc + es * 8 * (threadIdx.x + r * kFlThreads), x[r]);
+      float a[4][8];
+      if (ACC) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) ld8_rw(dst + lo + 8 * (threadIdx.x + r * kFlThreads), a[r]);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float y = __fmul_rn(scale, x[r][i]);
+          bad |= !finite_f(y);
+          x[r][i] = ACC ? __fadd_rn(a[r][i], y) : y;
+        }
+        st8(dst + lo + 8 * (threadIdx.x + r * kFlThreads), x[r]);
+      }
+      continue;
+    }
+
+    // staged tile: walk the tensors that overlap [klo, khi)
+    int64_t k = klo;
+    int j = ti;
+    while (k < khi && j < n_tensors) {
+      const int64_t off = __ldg(&table[j].flat_offset), num = __ldg(&table[j].numel);
+      const int64_t seg_end = (off + num < khi) ? off + num : khi;
+      if (seg_end > k)
+        stage_segment<DT>(table[j].ptr, k - off, static_cast<int>(seg_end - k), static_cast<int>(k - klo), scale,
+                          stage, bad);
+      if (seg_end > k) k = seg_end;
+      ++j;
+    }
+    // a table that ends before `total` leaves the rest as zeros
+    for (int q = static_cast<int>(k - klo) + threadIdx.x; q < tlen; q += kFlThreads) stage[stage_idx(q)] = 0.0f;
+    __syncthreads();
+    const int ngroups = (tlen + 7) / 8;
+    for (int u = threadIdx.x; u < ngroups; u += kFlThreads) {
+      float y[8];
+      const int64_t d = lo + 8 * u;
+      if (dst_vec && 8 * u + 8 <= tlen) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = stage[stage_idx(8 * u + i)];
+        if (ACC) {
+          float a[8];
+          ld8_rw(dst + d, a);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) y[i] = __fadd_rn(a[i], y[i]);
+        }
+        st8(dst + d, y);
+      } else {
+        for (int i = 0; i < 8 && 8 * u + i < tlen; ++i) {
+          const float yi = stage[stage_idx(8 * u + i)];
+          dst[d + i] = ACC ? __fadd_rn(dst[d + i], yi) : yi;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
+}
+
+template <int DT, bool ACC>
+static zero_status launch_flatten_t(const zero_tensor* table, int32_t n_tensors, int64_t s, int64_t e, float scale,
+                                    float* dst, int32_t* flag, cudaStream_t st) {
+  const int64_t len = e - s;
+  const int64_t ntiles = (len + kFlTile - 1) / kFlTile;
+  const void* fn = reinterpret_cast<const void*>(&flatten_kernel<DT, ACC>);
+  int64_t blocks = persistent_blocks(fn, kFlThreads, 0);
+  if (ntiles < blocks) blocks = ntiles;
+  flatten_kernel<DT, ACC><<<static_cast<unsigned>(blocks), kFlThreads, 0, st>>>(
+      table, n_tensors, s, len, ntiles, dst, aligned(dst, 32), scale, flag);
+  return check_launch("flatten_kernel");
+}
+
+zero_status launch_flatten(const zero_tensor* table, int32_t n_tensors, int src_dtype, int64_t s, int64_t e,
+                           float scale, int accumulate, float* dst, int32_t* flag, cudaStream_t st) {
+  if (e <= s) return ZERO_OK;
+  switch (src_dtype * 2 + (accumulate ? 1 : 0)) {
+    case ZERO_F32 * 2: return launch_flatten_t<ZERO_F32, false>(table, n_tensors, s, e, scale, dst, flag, st);
+    case ZERO_F32 * 2 + 1: return launch_flatten_t<ZERO_F32, true>(table, n_tensors, s, e, scale, dst, flag, st);
+    case ZERO_BF16 * 2: return launch_flatten_t<ZERO_BF16, false>(table, n_tensors, s, e, scale, dst, flag, st);
+    case ZERO_BF16 * 2 + 1: return launch_flatten_t<ZERO_BF16, true>(table, n_tensors, s, e, scale, dst, flag, st);
+    case ZERO_F16 * 2: return launch_flatten_t<ZERO_F16, false>(table, n_tensors, s, e, scale, dst, flag, st);
+    default: return launch_flatten_t<ZERO_F16, true>(table, n_tensors, s, e, scale, dst, flag, st);
+  }
+}
+
+// ------------------------------------------------------------------- K2
+// acc[k] = (ACC ? acc[k] : 0-free) + fl(scale * x[k]); groups of 8 with one
+// 32-byte accumulator load/store and one 16/32-byte source load.
+template <int DT, bool ACC>
+__device__ __forceinline__ void accum_scalar(int64_t k, float* __restrict__ acc, const void* __restrict__ src,
+                                             float scale, bool& bad) {
+  const float y = __fmul_rn(scale, load_elem<DT>(src, k));
+  bad |= !finite_f(y);
+  acc[k] = ACC ? __fadd_rn(acc[k], y) : y;
+}
+
+template <int DT, bool ACC>
+__global__ void __launch_bounds__(256) accum_kernel(float* __restrict__ acc, const void* __restrict__ src,
+                                                    int64_t head, int64_t nvec, int64_t n, float scale,
+                                                    int32_t* __restrict__ flag) {
+  constexpr int es = SrcTraits<DT>::esize;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t body_end = head + 8 * nvec;
+  bool bad = false;
+  if (tid < head) accum_scalar<DT, ACC>(tid, acc, src, scale, bad);
+  if (tid < n - body_end) accum_scalar<DT, ACC>(body_end + tid, acc, src, scale, bad);
+  const char* s8 = static_cast<const char*>(src);
+  for (int64_t i = tid; i < nvec; i += stride) {
+    const int64_t k = head + 8 * i;
+    float x[8], a[8];
+    load8_src<DT>(s8 + es * k, x);
+    if (ACC) ld8_rw(acc + k, a);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float y = __fmul_rn(scale, x[j]);
+      bad |= !finite_f(y);
+      x[j] = ACC ? __fadd_rn(a[j], y) : y;
+    }
+    st8(acc + k, x);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
+}
+
+template <int DT, bool ACC>
+__global__ void __launch_bounds__(256) accum_scalar_kernel(float* __restrict__ acc, const void* __restrict__ src,
+                                                           int64_t n, float scale, int32_t* __restrict__ flag) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n; k += stride)
+    accum_scalar<DT, ACC>(k, acc, src, scale, bad);
+  if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
+}
+
+template <int DT, bool ACC>
+static zero_status launch_accum_t(float* acc, const void* src, int64_t n, float scale, int32_t* flag,
+                                  cudaStream_t st) {
+  constexpr int es = SrcTraits<DT>::esize;
+  constexpr uintptr_t vb = (DT == ZERO_F32) ? 32 : 16;
+  const uintptr_t aa = reinterpret_cast<uintptr_t>(acc) % 32;
+  int64_t head = (aa % 4 == 0) ? static_cast<int64_t>((32 - aa) % 32) / 4 : -1;
+  if (head > n) head = n;
+  const bool vec = head >= 0 && reinterpret_cast<uintptr_t>(src) % es == 0 &&
+                   (reinterpret_cast<uintptr_t>(src) + es * static_cast<uintptr_t>(head)) % vb == 0;
+  if (!vec) {
+    const void* fn = reinterpret_cast<const void*>(&accum_scalar_kernel<DT, ACC>);
+    int64_t want = (n + 255) / 256, blocks = persistent_blocks(fn, 256, 0);
+    if (want < blocks) blocks = want;
+    accum_scalar_kernel<DT, ACC><<<static_cast<unsigned>(blocks), 256, 0, st>>>(acc, src, n, scale, flag);
+    return check_launch("accum_scalar_kernel");
+  }
+  const int64_t nvec = (n - head) / 8;
+  const void* fn = reinterpret_cast<const void*>(&accum_kernel<DT, ACC>);
+  int64_t want = (nvec + 255) / 256, blocks = persistent_blocks(fn, 256, 0);
+  if (want < blocks) blocks = want;
+  if (blocks < 1) blocks = 1;
+  accum_kernel<DT, ACC><<<static_cast<unsigned>(blocks), 256, 0, st>>>(acc, src, head, nvec, n, scale, flag);
+  return check_launch("accum_kernel");
+}
+
+zero_status launch_accum(float* acc, const void* src, int src_dtype, int64_t n, float scale, int accumulate,
+                         int32_t* flag, cudaStream_t st) {
+  if (n <= 0) return ZERO_OK;
+  switch (src_dtype * 2 + (accumulate ? 1 : 0)) {
+    case ZERO_F32 * 2: return launch_accum_t<ZERO_F32, false>(acc, src, n, scale, flag, st);
+    case ZERO_F32 * 2 + 1: return launch_accum_t<ZERO_F32, true>(acc, src, n, scale, flag, st);
+    case ZERO_BF16 * 2: return launch_accum_t<ZERO_BF16, false>(acc, src, n, scale, flag, st);
+    case ZERO_BF16 * 2 + 1: return launch_accum_t<ZERO_BF16, true>(acc, src, n, scale, flag, st);
+    case ZERO_F16 * 2: return launch_accum_t<ZERO_F16, false>(acc, src, n, scale, flag, st);
+    default: return launch_accum_t<ZERO_F16, true>(acc, src, n, scale, flag, st);
+  }
+}
+
+}  // namespace zs

@@ -1,0 +1,40 @@
+// kernels.h -- launchers of the device kernels, called by the C-ABI entry
+// points in api.cu after argument checking.  Internal; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "zero_shard.h"
+
+namespace zs {
+
+// Per-step AdamW scalars, computed in binary64 on the host and rounded to
+// binary32 once (bias corrections of the ZeRO page's ZeRO1Optimizer.step).
+struct AdamScalars {
+  float step_size;  // lr / (1 - beta1^t)
+  float bc2_sqrt;   // sqrt(1 - beta2^t)
+  float decay;      // 1 - lr * weight_decay
+  float b1, omb1;   // beta1, 1 - beta1
+  float b2, omb2;   // beta2, 1 - beta2
+  float eps;
+};
+
+// Elements per binary64 partial of the grad-norm reduction.
+constexpr int64_t kSqTile = 32768;
+
+zero_status launch_adamw(float* p, float* m, float* v, const float* g, void* lowp, int lowp_dtype, int64_t n,
+                         const AdamScalars& s, const zero_norm_result* clip, cudaStream_t st);
+
+zero_status launch_flatten(const zero_tensor* table, int32_t n_tensors, int src_dtype, int64_t shard_start,
+                           int64_t shard_end, float scale, int accumulate, float* dst, int32_t* flag,
+                           cudaStream_t st);
+
+zero_status launch_accum(float* acc, const void* src, int src_dtype, int64_t n, float scale, int accumulate,
+                         int32_t* flag, cudaStream_t st);
+
+zero_status launch_sqnorm(const float* g, int64_t n, double extra_sqnorm, double max_norm, double* partials,
+                          zero_norm_result* out, cudaStream_t st);
+
+}  // namespace zs

@@ -1,0 +1,132 @@
+"""FlatShardAdamW: one data-parallel rank's optimizer step over its flat shard.
+
+Holds the rank's buffers (fp32 flat grad, fp32 master / exp_avg /
+exp_avg_sq, the low-precision parameter copy, the grad-norm workspace and
+result) and sequences the library calls of one training step the way the
+pages' loops do: per micro-batch flatten/accumulate (loss / accum_steps),
+then clip_grad_norm_, then the AdamW step with the step counter t
+incremented before use, skipping the step when the grad norm is not finite
+(the ZeRO page, section "组合策略": "if not isfinite(grad_norm): skip").
+
+All arithmetic runs in libzeroshard's kernels; this class only allocates
+buffers with PyTorch and keeps the host-side step counter.
+
+Grad range: for ZeRO-2/3 and FSDP the rank holds grads of its own shard
+only (``grad_range="shard"``, norm over the shard plus ``extra_sqnorm`` from
+the other ranks).  For ZeRO-1 every rank holds the whole averaged flat grad
+(the ZeRO page's ZeRO1Optimizer.step all-reduces it), so the grad buffer
+covers the whole flat parameter (``grad_range="full"``), the norm is global,
+and the update uses the rank's slice.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, Optional, Sequence, Tuple
+
+import torch
+
+from . import zero_shard as zs
+
+
+class FlatShardAdamW:
+    def __init__(self, numels: Sequence[int], *, world_size: int = 1, rank: int = 0, lr: float = 1e-4,
+                 betas: Tuple[float, float] = (0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0,
+                 max_norm: float = math.inf, lowp_dtype: Optional[torch.dtype] = torch.bfloat16,
+                 grad_range: str = "shard", device="cuda", master: Optional[torch.Tensor] = None,
+                 lowp_out: Optional[torch.Tensor] = None):
+        if grad_range not in ("shard", "full"):
+            raise ValueError("grad_range must be 'shard' or 'full'")
+        self.device = torch.device(device)
+        self.numels = [int(n) for n in numels]
+        self.total = int(sum(self.numels))
+        self.world_size, self.rank = world_size, rank
+        self.start, self.end = zs.zero_shard_range(self.total, world_size, rank)
+        self.n = self.end - self.start
+        self.glo, self.ghi = (0, self.total) if grad_range == "full" else (self.start, self.end)
+        self.lr, self.betas, self.eps, self.weight_decay, self.max_norm = lr, tuple(betas), eps, weight_decay, max_norm
+        dev = self.device
+        self.grad = torch.empty(self.ghi - self.glo, dtype=torch.float32, device=dev)
+        if master is None:
+            master = torch.zeros(self.n, dtype=torch.float32, device=dev)
+        if master.numel() != self.n or master.dtype != torch.float32:
+            raise ValueError("master must be fp32 with the shard's size")
+        self.master = master.to(dev).contiguous()
+        self.exp_avg = torch.zeros(self.n, dtype=torch.float32, device=dev)
+        self.exp_avg_sq = torch.zeros(self.n, dtype=torch.float32, device=dev)
+        if lowp_out is not None:
+            self.lowp = lowp_out  # e.g. the rank's slice of the full low-precision FlatParameter
+        elif lowp_dtype is not None:
+            self.lowp = torch.empty(self.n, dtype=lowp_dtype, device=dev)
+        else:
+            self.lowp = None
+        self.ws = torch.empty(max(zs.zero_grad_sqnorm_workspace_bytes(self.grad.numel()), 8), dtype=torch.uint8,
+                              device=dev)
+        self.norm_buf = zs.new_norm_result(dev)
+        self.found_nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.t = 0
+        self._tables: Dict[tuple, Tuple[torch.Tensor, int]] = {}
+
+    # ---------------------------------------------------------------- grads
+    def _table(self, grads: Sequence[Optional[torch.Tensor]]) -> torch.Tensor:
+        key = tuple(0 if g is None else g.data_ptr() for g in grads)
+        hit = self._tables.get(key)
+        if hit is None:
+            if len(grads) != len(self.numels):
+                raise ValueError("one grad (or None) per parameter tensor is required")
+            for i, (g, n) in enumerate(zip(grads, self.numels)):
+                if g is not None and g.numel() != n:
+                    raise ValueError(f"grad {i} has {g.numel()} elements, expected {n}")
+            table, total = zs.zero_tensor_table(grads, self.numels)
+            assert total == self.total
+            hit = (zs.device_table(table, len(grads), self.device), total)
+            if len(self._tables) > 64:
+                self._tables.clear()
+            self._tables[key] = hit
+        return hit[0]
+
+    def flatten(self, grads: Sequence[Optional[torch.Tensor]], *, accumulate: bool, scale: float = 1.0,
+                stream=None) -> None:
+        """Flatten/cast per-tensor grads into the rank's flat fp32 grad (K1)."""
+        dts = {g.dtype for g in grads if g is not None}
+        if len(dts) > 1:
+            raise ValueError("all grads must share one dtype")
+        dt = dts.pop() if dts else torch.float32
+        zs.zero_flatten_cast(self._table(grads), len(grads), self.total, dt, self.glo, self.ghi, scale, accumulate,
+                             self.grad, self.found_nonfinite, stream)
+
+    def accum(self, flat_src: torch.Tensor, *, accumulate: bool, scale: float = 1.0, stream=None) -> None:
+        """Accumulate a flat low-precision grad covering the grad range (K2)."""
+        zs.zero_accum(self.grad, flat_src, scale, accumulate, self.found_nonfinite, stream)
+
+    # ----------------------------------------------------------------- step
+    def shard_grad(self) -> torch.Tensor:
+        return self.grad[self.start - self.glo:self.end - self.glo]
+
+    def launch_step(self, extra_sqnorm: float = 0.0, stream=None) -> None:
+        """Enqueue grad norm (K3) and the AdamW step (K4) for t+1 without waiting.
+
+        When the norm turns out non-finite, K4 changes nothing on the device;
+        finish_step() then leaves t unchanged.
+        """
+        zs.zero_grad_sqnorm(self.grad, extra_sqnorm, self.max_norm, self.ws, self.norm_buf, stream)
+        zs.zero_adamw_step(self.master, self.exp_avg, self.exp_avg_sq, self.shard_grad(), self.lowp, self.lr,
+                           self.betas[0], self.betas[1], self.eps, self.weight_decay, self.t + 1, self.norm_buf,
+                           stream)
+
+    def finish_step(self) -> zs.NormResult:
+        """Read the step's grad norm (a device->host copy that waits for the step)."""
+        r = zs.decode_norm_result(self.norm_buf)
+        if r.finite:
+            self.t += 1
+        return r
+
+    def step(self, extra_sqnorm: float = 0.0, stream=None) -> zs.NormResult:
+        self.launch_step(extra_sqnorm, stream)
+        return self.finish_step()
+
+    def resident_bytes(self) -> int:
+        """Device bytes this rank holds for the step (grad + state + low-precision copy)."""
+        b = 4 * (self.grad.numel() + 3 * self.n)
+        if self.lowp is not None:
+            b += self.lowp.numel() * self.lowp.element_size()
+        return b

@@ -1,0 +1,227 @@
+"""ctypes binding of libzeroshard with the C ABI's names.
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Tensors are PyTorch tensors (device memory and streams come from
+PyTorch); they are checked to be contiguous CUDA tensors of the right dtype
+before their addresses are handed to the library, so that a host pointer can
+never reach a kernel.  There is no CPU fallback: without the built library
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, NamedTuple, Optional, Sequence, Tuple
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+ZERO_OK, ZERO_EINVAL, ZERO_ECUDA = 0, 1, 2
+ZERO_F32, ZERO_BF16, ZERO_F16 = 0, 1, 2
+
+_DT = {torch.float32: ZERO_F32, torch.bfloat16: ZERO_BF16, torch.float16: ZERO_F16}
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+class zero_tensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("numel", ctypes.c_int64), ("flat_offset", ctypes.c_int64)]
+
+
+class zero_norm_result(ctypes.Structure):
+    _fields_ = [("sqnorm", ctypes.c_double), ("norm", ctypes.c_double), ("clip_coef", ctypes.c_float),
+                ("finite", ctypes.c_int32)]
+
+
+class zero_adamw_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double)]
+
+
+NORM_RESULT_BYTES = ctypes.sizeof(zero_norm_result)
+TENSOR_ENTRY_BYTES = ctypes.sizeof(zero_tensor)
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load the in-tree libzeroshard.so (built by __graft_entry__.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libzeroshard is not built ({path} missing): run __graft_entry__.build()")
+    L = ctypes.CDLL(path)
+    i32, i64, f32, f64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double, ctypes.c_void_p
+    L.zero_shard_range.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    L.zero_tensor_table.argtypes = [vp, vp, i32, vp, ctypes.POINTER(i64)]
+    L.zero_flatten_cast.argtypes = [vp, i32, i64, ctypes.c_int, i64, i64, f32, i32, vp, vp, vp]
+    L.zero_accum.argtypes = [vp, vp, ctypes.c_int, i64, f32, i32, vp, vp]
+    L.zero_grad_sqnorm_workspace_bytes.argtypes = [i64]
+    L.zero_grad_sqnorm_workspace_bytes.restype = ctypes.c_size_t
+    L.zero_grad_sqnorm.argtypes = [vp, i64, f64, f64, vp, ctypes.c_size_t, vp, vp]
+    L.zero_adamw_step.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, i64, ctypes.POINTER(zero_adamw_hparams), i64,
+                                  vp, vp]
+    L.zero_status_string.argtypes = [ctypes.c_int]
+    L.zero_status_string.restype = ctypes.c_char_p
+    L.zero_last_error.argtypes = []
+    L.zero_last_error.restype = ctypes.c_char_p
+    for nm in ("zero_shard_range", "zero_tensor_table", "zero_flatten_cast", "zero_accum", "zero_grad_sqnorm",
+               "zero_adamw_step"):
+        getattr(L, nm).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(st: int) -> None:
+    if st != ZERO_OK:
+        L = lib()
+        raise ZeroError(st, f"{L.zero_status_string(st).decode()}: {L.zero_last_error().decode()}")
+
+
+def _dev(t: Optional[torch.Tensor], name: str, dtype=None, allow_none: bool = False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+# ------------------------------------------------------------------ host only
+def zero_shard_range(total: int, world_size: int, rank: int) -> Tuple[int, int]:
+    s, e = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().zero_shard_range(total, world_size, rank, ctypes.byref(s), ctypes.byref(e)))
+    return s.value, e.value
+
+
+def zero_tensor_table(grads: Sequence[Optional[torch.Tensor]] = None, numels: Sequence[int] = None):
+    """Host FlatParameter table for `grads` (None = no grad) or bare `numels`.
+
+    Returns (table, total) where table is a ctypes array of zero_tensor.
+    """
+    if numels is None:
+        numels = [0 if g is None else g.numel() for g in grads]
+    n = len(numels)
+    nm = np.ascontiguousarray(np.asarray(numels, dtype=np.int64))
+    ptrs = None
+    if grads is not None:
+        for i, g in enumerate(grads):
+            if g is not None:
+                _dev(g, f"grads[{i}]")
+        ptrs = (ctypes.c_void_p * n)(*[None if g is None else g.data_ptr() for g in grads])
+    table = (zero_tensor * max(n, 1))()
+    total = ctypes.c_int64()
+    _check(lib().zero_tensor_table(ptrs, ctypes.c_void_p(nm.ctypes.data), n, table, ctypes.byref(total)))
+    return table, total.value
+
+
+def device_table(table, n_tensors: int, device) -> torch.Tensor:
+    """Copy a host table (from zero_tensor_table) into device memory (uint8 bytes)."""
+    raw = bytes(memoryview(table))[: n_tensors * TENSOR_ENTRY_BYTES]
+    host = torch.frombuffer(bytearray(raw), dtype=torch.uint8) if raw else torch.empty(0, dtype=torch.uint8)
+    return host.to(device)
+
+
+def zero_grad_sqnorm_workspace_bytes(n: int) -> int:
+    return int(lib().zero_grad_sqnorm_workspace_bytes(n))
+
+
+# --------------------------------------------------------------------- device
+def zero_flatten_cast(d_table: torch.Tensor, n_tensors: int, total: int, src_dtype: torch.dtype, shard_start: int,
+                      shard_end: int, scale: float, accumulate: bool, dst: torch.Tensor,
+                      found_nonfinite: Optional[torch.Tensor] = None, stream=None) -> None:
+    if shard_end > shard_start and dst.numel() < shard_end - shard_start:
+        raise ValueError("dst is smaller than the shard")
+    tab = _dev(d_table, "d_table", torch.uint8, allow_none=n_tensors == 0)
+    if n_tensors > 0 and d_table.numel() < n_tensors * TENSOR_ENTRY_BYTES:
+        raise ValueError("d_table holds fewer entries than n_tensors")
+    _check(lib().zero_flatten_cast(tab, n_tensors, total, _DT[src_dtype], shard_start, shard_end, scale,
+                                   int(bool(accumulate)), _dev(dst, "dst", torch.float32),
+                                   _dev(found_nonfinite, "found_nonfinite", torch.int32, allow_none=True),
+                                   _stream(stream)))
+
+
+def zero_accum(acc: torch.Tensor, src: torch.Tensor, scale: float, accumulate: bool,
+               found_nonfinite: Optional[torch.Tensor] = None, stream=None) -> None:
+    if src.numel() != acc.numel():
+        raise ValueError("acc and src differ in size")
+    _check(lib().zero_accum(_dev(acc, "acc", torch.float32), _dev(src, "src"), _DT[src.dtype], acc.numel(), scale,
+                            int(bool(accumulate)),
+                            _dev(found_nonfinite, "found_nonfinite", torch.int32, allow_none=True), _stream(stream)))
+
+
+def zero_grad_sqnorm(grad: torch.Tensor, extra_sqnorm: float, max_norm: float, ws: torch.Tensor,
+                     out: torch.Tensor, stream=None) -> None:
+    if out.numel() * out.element_size() < NORM_RESULT_BYTES:
+        raise ValueError("out is smaller than zero_norm_result")
+    _check(lib().zero_grad_sqnorm(_dev(grad, "grad", torch.float32), grad.numel(), extra_sqnorm, max_norm,
+                                  _dev(ws, "ws", allow_none=True), 0 if ws is None else ws.numel() * ws.element_size(),
+                                  _dev(out, "out"), _stream(stream)))
+
+
+def zero_adamw_step(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg_sq: torch.Tensor, grad: torch.Tensor,
+                    param_lowp: Optional[torch.Tensor], lr: float, beta1: float, beta2: float, eps: float,
+                    weight_decay: float, step: int, clip: Optional[torch.Tensor] = None, stream=None) -> None:
+    n = master.numel()
+    for t, nm in ((exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq"), (grad, "grad")):
+        if t.numel() != n:
+            raise ValueError(f"{nm} differs in size from master")
+    lowp_dt = ZERO_BF16
+    if param_lowp is not None:
+        if param_lowp.numel() != n:
+            raise ValueError("param_lowp differs in size from master")
+        if param_lowp.dtype not in (torch.bfloat16, torch.float16):
+            raise ValueError("param_lowp must be bf16 or f16")
+        lowp_dt = _DT[param_lowp.dtype]
+    if clip is not None and clip.numel() * clip.element_size() < NORM_RESULT_BYTES:
+        raise ValueError("clip is smaller than zero_norm_result")
+    hp = zero_adamw_hparams(lr, beta1, beta2, eps, weight_decay)
+    _check(lib().zero_adamw_step(_dev(master, "master", torch.float32), _dev(exp_avg, "exp_avg", torch.float32),
+                                 _dev(exp_avg_sq, "exp_avg_sq", torch.float32), _dev(grad, "grad", torch.float32),
+                                 _dev(param_lowp, "param_lowp", allow_none=True), lowp_dt, n, ctypes.byref(hp), step,
+                                 _dev(clip, "clip", allow_none=True), _stream(stream)))
+
+
+# ------------------------------------------------------------ norm result I/O
+class NormResult(NamedTuple):
+    sqnorm: float
+    norm: float
+    clip_coef: float
+    finite: bool
+
+
+def new_norm_result(device) -> torch.Tensor:
+    """Device buffer for one zero_norm_result (8-byte aligned by the allocator)."""
+    return torch.zeros(NORM_RESULT_BYTES, dtype=torch.uint8, device=device)
+
+
+def decode_norm_result(buf: torch.Tensor) -> NormResult:
+    """Read a zero_norm_result (device or host bytes) into Python values."""
+    raw = bytes(buf.detach().cpu().numpy().tobytes()[:NORM_RESULT_BYTES])
+    r = zero_norm_result.from_buffer_copy(raw)
+    return NormResult(r.sqnorm, r.norm, r.clip_coef, bool(r.finite))

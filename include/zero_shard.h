@@ -1,0 +1,229 @@
+/*
+ * zero_shard.h -- C ABI of libzeroshard: one data-parallel rank's optimizer
+ * step over its flat 1-D shard (ZeRO-1/2/3, FSDP FlatParameter), on one GPU.
+ *
+ * The step has four parts, each one call below:
+ *   zero_flatten_cast  per-tensor grads -> the rank's flat fp32 grad shard
+ *                      (optionally accumulating micro-batches, scaled)
+ *   zero_accum         flat low-precision grads -> flat fp32 accumulator
+ *   zero_grad_sqnorm   global L2 grad norm and the clip coefficient
+ *   zero_adamw_step    fused bias-corrected AdamW on fp32 master / exp_avg /
+ *                      exp_avg_sq with a bf16 (or f16) parameter write-back
+ * plus the host-only helpers zero_shard_range and zero_tensor_table.
+ *
+ * Sources: the ZeRO page (ai6s.net, "cann-recipes-train" ZeRO-1/2/3 on
+ * Ascend), the memory-ledger / FlatParameter page (ybb.press,
+ * "大模型分布式训练并行与显存工程实战") and the LLaMA-13B gradient accumulation
+ * page (ai6s.net).  Each entry point names the passage that defines it.
+ *
+ * Conventions for every call:
+ *  - Memory.  The library allocates nothing (device or host) and keeps no
+ *    state between calls beyond a per-device cache of launch sizes.  The
+ *    caller owns every buffer.  Pointers prefixed d_ are device addresses;
+ *    everything else is host memory.
+ *  - Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Device work is enqueued asynchronously on it; no call
+ *    synchronises the host except where stated.
+ *  - Errors.  Arguments are checked on the host before anything is launched;
+ *    a bad argument returns ZERO_EINVAL and launches nothing.  A CUDA error
+ *    reported by the launch returns ZERO_ECUDA.  zero_last_error() gives a
+ *    readable message for the calling thread's last failure.
+ *  - n == 0 (or an empty shard) is a valid no-op that returns ZERO_OK.
+ *  - Alignment.  Any element-aligned address is accepted.  The fast paths
+ *    need 32-byte aligned fp32 buffers; other alignments take slower but
+ *    equally exact paths.
+ *  - Aliasing.  Outputs must not overlap inputs, except where a buffer is
+ *    updated in place by design (d_dst with accumulate, d_acc, the AdamW
+ *    state).
+ *  - Floating point.  Every result is reproducible bit for bit run to run;
+ *    no call uses atomics on floating-point data.
+ */
+#ifndef ZERO_SHARD_H_
+#define ZERO_SHARD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum zero_status {
+  ZERO_OK = 0,
+  ZERO_EINVAL = 1, /* invalid argument; nothing was launched */
+  ZERO_ECUDA = 2   /* the CUDA runtime reported an error */
+} zero_status;
+
+typedef enum zero_dtype {
+  ZERO_F32 = 0,
+  ZERO_BF16 = 1,
+  ZERO_F16 = 2
+} zero_dtype;
+
+/* One parameter's gradient in the FlatParameter layout.  ptr == NULL means
+ * the parameter has no grad; it reads as zeros (the ZeRO page's
+ * _flatten_gradients fills such a tensor with torch.zeros). */
+typedef struct zero_tensor {
+  const void* ptr;     /* device address of element 0, contiguous */
+  int64_t numel;       /* number of elements, >= 0 */
+  int64_t flat_offset; /* start of this tensor in the flat buffer */
+} zero_tensor;
+
+/* Result of zero_grad_sqnorm, written to device memory. */
+typedef struct zero_norm_result {
+  double sqnorm;    /* local sum of squares + extra_sqnorm */
+  double norm;      /* sqrt(sqnorm), binary64 */
+  float clip_coef;  /* min(1, max_norm / (norm + 1e-6)) in binary32 */
+  int32_t finite;   /* 1 if norm is finite; 0 means: skip this step */
+} zero_norm_result;
+
+/* AdamW hyper-parameters, binary64 as the user gives them. */
+typedef struct zero_adamw_hparams {
+  double lr;
+  double beta1;
+  double beta2;
+  double eps;
+  double weight_decay; /* 0: plain Adam as in the ZeRO page's step() */
+} zero_adamw_hparams;
+
+/* zero_shard_range -- host only.
+ * The ZeRO page, section "ZeRO-1: 切分 Optimizer States",
+ * ZeRO1Optimizer.__init__: chunk = ceil(total / world_size),
+ * start = rank * chunk, end = min(start + chunk, total).  Where
+ * rank * chunk > total (few elements, many ranks) the shard is the empty
+ * range [total, total).  The flat buffer is never padded: the last shards
+ * may be short or empty.
+ * Errors: ZERO_EINVAL if start/end is NULL, total < 0, world_size < 1 or
+ * rank is not in [0, world_size). */
+zero_status zero_shard_range(int64_t total, int32_t world_size, int32_t rank, int64_t* start,
+                             int64_t* end);
+
+/* zero_tensor_table -- host only.
+ * The FlatParameter layout (memory-ledger page, section "FSDP 的关键抽象：
+ * FlatParameter"; the ZeRO page's _flatten_gradients / _apply_update): the
+ * parameters are concatenated in list order, so tensor i starts at the sum
+ * of the sizes of tensors 0..i-1.  Fills table[i] = {ptrs[i], numels[i],
+ * offset_i} for i < n_tensors and *total = sum of numels.  ptrs may be NULL
+ * (then every table[i].ptr is NULL) and any ptrs[i] may be NULL.  The
+ * caller copies the table to device memory for zero_flatten_cast.
+ * Errors: ZERO_EINVAL if table/total/numels is NULL with n_tensors > 0,
+ * n_tensors < 0, a numel < 0, or the total overflows int64. */
+zero_status zero_tensor_table(const void* const* ptrs, const int64_t* numels, int32_t n_tensors,
+                              zero_tensor* table, int64_t* total);
+
+/* zero_flatten_cast -- device.
+ * The ZeRO page's _flatten_gradients (each grad viewed 1-D, cast to fp32,
+ * concatenated), sliced to the rank's shard (ZeRO1Optimizer.step:
+ * flat_grad[start:end]), scaled, and optionally accumulated over
+ * micro-batches (the page's GradientAccumulator adds fp32 grads; the
+ * gradient-accumulation page divides the loss by accum_steps).  For every
+ * flat index k in [shard_start, shard_end), with x the grad element at k
+ * (0 when its tensor has no grad):
+ *   accumulate == 0:  d_dst[k - shard_start] = fl(scale * x)
+ *   accumulate == 1:  d_dst[k - shard_start] = fl(d_dst[...] + fl(scale * x))
+ * d_table: device array of n_tensors entries as built by zero_tensor_table
+ *   (sorted by flat_offset, contiguous, ending at `total`).
+ * src_dtype: dtype of every grad in the table (F32, BF16 or F16).
+ * d_dst: fp32, shard_end - shard_start elements.
+ * d_found_nonfinite: NULL, or a device int32 set to 1 when any
+ *   fl(scale * x) is inf or NaN (never cleared by the call: zero it first).
+ * Errors: ZERO_EINVAL for n_tensors < 0, d_table NULL with n_tensors > 0,
+ * shard bounds outside 0 <= shard_start <= shard_end <= total, d_dst NULL
+ * on a non-empty shard, a bad dtype, accumulate not 0/1, or a non-finite
+ * scale.  The table's contents cannot be checked on the host: a table that
+ * does not match `total` or points at too-small buffers is the caller's
+ * error and reads out of bounds. */
+zero_status zero_flatten_cast(const zero_tensor* d_table, int32_t n_tensors, int64_t total,
+                              zero_dtype src_dtype, int64_t shard_start, int64_t shard_end,
+                              float scale, int32_t accumulate, float* d_dst,
+                              int32_t* d_found_nonfinite, void* stream);
+
+/* zero_accum -- device.
+ * Flat micro-batch accumulation and averaging (the ZeRO page's
+ * GradientAccumulator.backward; flat_grad /= world_size; the gradient-
+ * accumulation page's loss / accum_steps): for k in [0, n)
+ *   accumulate == 0:  d_acc[k] = fl(scale * x[k])
+ *   accumulate == 1:  d_acc[k] = fl(d_acc[k] + fl(scale * x[k]))
+ * with x = d_src in src_dtype cast exactly to fp32.  This is the ZeRO-2/3
+ * case, where the rank receives its shard's grads already flat.
+ * d_found_nonfinite as for zero_flatten_cast.
+ * Errors: ZERO_EINVAL for n < 0, NULL buffers with n > 0, a bad dtype,
+ * accumulate not 0/1, or a non-finite scale. */
+zero_status zero_accum(float* d_acc, const void* d_src, zero_dtype src_dtype, int64_t n, float scale,
+                       int32_t accumulate, int32_t* d_found_nonfinite, void* stream);
+
+/* zero_grad_sqnorm_workspace_bytes -- host only.
+ * Device scratch that zero_grad_sqnorm needs for n elements: one binary64
+ * partial per fixed tile of the grad buffer (8 bytes per 32768 elements).
+ * Returns 0 for n <= 0. */
+size_t zero_grad_sqnorm_workspace_bytes(int64_t n);
+
+/* zero_grad_sqnorm -- device.
+ * clip_grad_norm_(params, max_norm) as the ZeRO page's training loop
+ * (section "组合策略") and the gradient-accumulation page call it after
+ * accumulation and before the step, made deterministic:
+ *   sqnorm = sum_k d_grad[k]^2 + extra_sqnorm
+ *   norm   = sqrt(sqnorm)                                     (binary64)
+ *   clip_coef = max_norm / (norm + 1e-6) if that is < 1, else 1 (binary32)
+ *   finite = isfinite(norm)   -- the page skips the step when it is not
+ * The squares are summed in fixed tiles of 32768 elements (binary32 pairwise
+ * within a thread, compensated across rounds, binary64 across threads and
+ * tiles), so the result does not depend on the GPU or the launch size.
+ * extra_sqnorm is the other ranks' share of a global norm (0 for a norm over
+ * this buffer alone).  max_norm = +inf turns clipping off (coefficient 1).
+ * d_ws: device scratch of at least zero_grad_sqnorm_workspace_bytes(n)
+ *   bytes, 8-byte aligned; overwritten.
+ * d_out: device zero_norm_result, written by the call.
+ * Errors: ZERO_EINVAL for n < 0, d_grad NULL with n > 0, d_out NULL, d_ws
+ * NULL or smaller than required, a negative or NaN max_norm, or a
+ * negative or non-finite extra_sqnorm. */
+zero_status zero_grad_sqnorm(const float* d_grad, int64_t n, double extra_sqnorm, double max_norm,
+                             void* d_ws, size_t ws_bytes, zero_norm_result* d_out, void* stream);
+
+/* zero_adamw_step -- device.
+ * The ZeRO page's ZeRO1Optimizer.step Adam update (bias_correction1/2 with
+ * the step counter incremented before use; denom = sqrt(exp_avg_sq) /
+ * sqrt(bias_correction2) + eps; update = exp_avg / denom * (-lr /
+ * bias_correction1)), with AdamW's decoupled weight decay (the memory-ledger
+ * page names "bf16 + AdamW" as the default) applied to the old master value,
+ * the clip coefficient of zero_grad_sqnorm applied to the grad, and the
+ * low-precision parameter copy written in the same pass (memory-ledger page:
+ * 16 bytes/param = bf16 param + bf16 grad + 12 bytes fp32 state).  Per
+ * element, each operation rounded to nearest even in binary32:
+ *   g = grad * coef
+ *   p = p * (1 - lr*wd)
+ *   m = fma(1-beta1, g, m*beta1)
+ *   v = fma((1-beta2)*g, g, v*beta2)
+ *   d = sqrt(v) / sqrt(1-beta2^t) + eps
+ *   p = p - (lr / (1-beta1^t)) * (m / d)
+ *   lowp = round_to_nearest_even(p)
+ * where the per-step scalars are computed in binary64 on the host and
+ * rounded to binary32 once.  d_master, d_exp_avg, d_exp_avg_sq (fp32, n,
+ * updated in place), d_grad (fp32, n).  d_param_lowp: NULL or n elements of
+ * lowp_dtype (BF16, or F16 for the ZeRO-3 page's fp16 local chunk); the
+ * rank's slice of the full low-precision FlatParameter may start at any
+ * element.  step: t >= 1, already incremented (the page's step_count).
+ * d_clip: NULL (coefficient 1, no skip guard), or the device result of
+ * zero_grad_sqnorm; when its `finite` is 0 the call changes nothing (the
+ * device-side half of the page's skip-on-overflow policy; the caller should
+ * then not advance t).
+ * Errors: ZERO_EINVAL for n < 0, NULL state/grad buffers with n > 0, hp
+ * NULL, step < 1, a bad lowp_dtype (F32 is not a low-precision copy), or
+ * hyper-parameters outside lr >= 0, 0 <= beta < 1, eps > 0, wd >= 0 (all
+ * finite). */
+zero_status zero_adamw_step(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
+                            const float* d_grad, void* d_param_lowp, zero_dtype lowp_dtype,
+                            int64_t n, const zero_adamw_hparams* hp, int64_t step,
+                            const zero_norm_result* d_clip, void* stream);
+
+/* Static text for a status code. */
+const char* zero_status_string(zero_status status);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* zero_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_SHARD_H_ */

@@ -1,0 +1,157 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol the
+header declares, its host-only calls agree with the oracle bit for bit, and
+invalid arguments are rejected on the host before anything is launched."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from fsdp_sharded_mixed_flatparameter_gb300 import build, zero_shard
+    build.build()
+    return zero_shard.lib()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(zero_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_header_declares_the_boundary():
+    want = {"zero_shard_range", "zero_tensor_table", "zero_flatten_cast", "zero_accum",
+            "zero_grad_sqnorm_workspace_bytes", "zero_grad_sqnorm", "zero_adamw_step", "zero_status_string",
+            "zero_last_error"}
+    assert want <= declared_symbols()
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in sorted(declared_symbols()):
+        assert hasattr(L, name), name
+
+
+def test_shard_range_matches_oracle(L):
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    for total in list(range(0, 70)) + [1261891, 124439808, 6738415616, 13015864320, 2**62]:
+        for world in (1, 2, 3, 4, 7, 8, 17, 64):
+            for rank in {0, 1 % world, world // 2, world - 1}:
+                assert zs.zero_shard_range(total, world, rank) == oracle.shard_range(total, world, rank), \
+                    (total, world, rank)
+
+
+def test_shard_range_rejects(L):
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    for args in [(-1, 2, 0), (10, 0, 0), (10, 2, 2), (10, 2, -1)]:
+        with pytest.raises(zs.ZeroError) as ei:
+            zs.zero_shard_range(*args)
+        assert ei.value.status == zs.ZERO_EINVAL
+    s = ctypes.c_int64()
+    assert L.zero_shard_range(10, 2, 0, ctypes.byref(s), None) == 1
+    assert b"NULL" in L.zero_last_error()
+
+
+def test_tensor_table_matches_oracle_offsets(L):
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    for numels in (W.small_ragged().numels, W.gpt2_zero1().numels, W.llama7b().numels, (0, 0, 5, 0), ()):
+        table, total = zs.zero_tensor_table(numels=numels)
+        off = oracle.flat_offsets(numels)
+        assert total == off[-1]
+        got = [table[i].flat_offset for i in range(len(numels))]
+        assert got == list(off[:-1])
+        assert all(table[i].ptr is None for i in range(len(numels)))
+
+
+def test_tensor_table_rejects(L):
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    with pytest.raises(zs.ZeroError):
+        zs.zero_tensor_table(numels=[3, -1])
+    with pytest.raises(zs.ZeroError):
+        zs.zero_tensor_table(numels=[2**62, 2**62, 2**62])
+
+
+def test_workspace_bytes(L):
+    assert L.zero_grad_sqnorm_workspace_bytes(0) == 0
+    assert L.zero_grad_sqnorm_workspace_bytes(-5) == 0
+    assert L.zero_grad_sqnorm_workspace_bytes(1) == 8
+    assert L.zero_grad_sqnorm_workspace_bytes(32768) == 8
+    assert L.zero_grad_sqnorm_workspace_bytes(32769) == 16
+    assert L.zero_grad_sqnorm_workspace_bytes(6738415616) == 8 * 205641
+
+
+def test_invalid_arguments_return_einval_before_any_launch(L):
+    """Every check below happens on the host; no CUDA call is made (there is no GPU here)."""
+    from fsdp_sharded_mixed_flatparameter_gb300.zero_shard import zero_adamw_hparams
+    FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: each call fails validation first
+    hp = zero_adamw_hparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    cases = [
+        L.zero_flatten_cast(None, 2, 10, 1, 0, 5, 1.0, 0, FAKE, None, None),          # NULL table
+        L.zero_flatten_cast(FAKE, -1, 10, 1, 0, 5, 1.0, 0, FAKE, None, None),         # n_tensors < 0
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 6, 5, 1.0, 0, FAKE, None, None),          # start > end
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 11, 1.0, 0, FAKE, None, None),         # end > total
+        L.zero_flatten_cast(FAKE, 2, 10, 7, 0, 5, 1.0, 0, FAKE, None, None),          # bad dtype
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, 2, FAKE, None, None),          # accumulate 2
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, math.nan, 0, FAKE, None, None),     # NaN scale
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, 0, None, None, None),          # NULL dst
+        L.zero_flatten_cast(FAKE, 0, 10, 1, 0, 5, 1.0, 0, FAKE, None, None),          # total without tensors
+        L.zero_accum(None, FAKE, 1, 10, 1.0, 0, None, None),
+        L.zero_accum(FAKE, FAKE, 1, -1, 1.0, 0, None, None),
+        L.zero_accum(FAKE, FAKE, 9, 10, 1.0, 0, None, None),
+        L.zero_accum(FAKE, FAKE, 1, 10, math.inf, 0, None, None),
+        L.zero_grad_sqnorm(None, 10, 0.0, 1.0, FAKE, 8, FAKE, None),                  # NULL grad
+        L.zero_grad_sqnorm(FAKE, 10, 0.0, 1.0, FAKE, 8, None, None),                  # NULL out
+        L.zero_grad_sqnorm(FAKE, 40000, 0.0, 1.0, FAKE, 8, FAKE, None),               # workspace too small
+        L.zero_grad_sqnorm(FAKE, 10, 0.0, 1.0, None, 8, FAKE, None),                  # NULL workspace
+        L.zero_grad_sqnorm(FAKE, 10, 0.0, 1.0, ctypes.c_void_p(0x1004), 8, FAKE, None),  # misaligned ws
+        L.zero_grad_sqnorm(FAKE, 10, -1.0, 1.0, FAKE, 8, FAKE, None),                 # negative extra
+        L.zero_grad_sqnorm(FAKE, 10, 0.0, math.nan, FAKE, 8, FAKE, None),             # NaN max_norm
+        L.zero_grad_sqnorm(FAKE, 10, 0.0, -1.0, FAKE, 8, FAKE, None),                 # negative max_norm
+        L.zero_adamw_step(FAKE, FAKE, FAKE, FAKE, None, 1, 10, ctypes.byref(hp), 0, None, None),   # step 0
+        L.zero_adamw_step(FAKE, FAKE, FAKE, FAKE, None, 1, 10, None, 1, None, None),               # NULL hp
+        L.zero_adamw_step(FAKE, None, FAKE, FAKE, None, 1, 10, ctypes.byref(hp), 1, None, None),   # NULL m
+        L.zero_adamw_step(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 10, ctypes.byref(hp), 1, None, None),   # F32 lowp
+        L.zero_adamw_step(FAKE, FAKE, FAKE, FAKE, None, 1, -3, ctypes.byref(hp), 1, None, None),   # n < 0
+    ]
+    for i, bad in enumerate([zero_adamw_hparams(-1, .9, .999, 1e-8, 0), zero_adamw_hparams(1e-3, 1.0, .999, 1e-8, 0),
+                             zero_adamw_hparams(1e-3, .9, .999, 0.0, 0), zero_adamw_hparams(1e-3, .9, .999, 1e-8, -1),
+                             zero_adamw_hparams(math.nan, .9, .999, 1e-8, 0)]):
+        cases.append(L.zero_adamw_step(FAKE, FAKE, FAKE, FAKE, None, 1, 10, ctypes.byref(bad), 1, None, None))
+    assert cases == [1] * len(cases), [i for i, c in enumerate(cases) if c != 1]
+    assert len(L.zero_last_error()) > 0
+
+
+def test_empty_calls_are_noops_without_a_gpu(L):
+    from fsdp_sharded_mixed_flatparameter_gb300.zero_shard import zero_adamw_hparams
+    hp = zero_adamw_hparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    assert L.zero_flatten_cast(None, 0, 0, 1, 0, 0, 1.0, 0, None, None, None) == 0
+    assert L.zero_accum(None, None, 1, 0, 1.0, 0, None, None) == 0
+    assert L.zero_adamw_step(None, None, None, None, None, 1, 0, ctypes.byref(hp), 1, None, None) == 0
+
+
+def test_status_strings(L):
+    assert L.zero_status_string(0) == b"ZERO_OK"
+    assert b"EINVAL" in L.zero_status_string(1)
+    assert b"ECUDA" in L.zero_status_string(2)
+
+
+def test_binding_refuses_host_tensors(L):
+    import torch
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    cpu = torch.zeros(16)
+    with pytest.raises(ValueError):
+        zs.zero_adamw_step(cpu, cpu, cpu, cpu, None, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1)
+    with pytest.raises(ValueError):
+        zs.zero_accum(cpu, cpu, 1.0, False)

@@ -1,0 +1,110 @@
+"""The five workload configurations end to end on the GPU against the oracle.
+
+tiny, GPT-2 ZeRO-1 and the ragged stress run at full size with the whole
+shard compared after every step; Llama-7B and the Llama-13B ZeRO-3 shard run
+at full size with every grad in the norm and a seeded sample of shard
+positions compared, and their full step counts run on shape-preserving
+smaller lists with the whole shard compared.
+"""
+import math
+
+import pytest
+import torch
+
+import workloads as W
+from _configs import run_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from fsdp_sharded_mixed_flatparameter_gb300 import build, zero_shard
+    build.build()
+    zero_shard.lib()
+
+
+def _summary(rep):
+    exact = sum(s.exact for s in rep.steps)
+    worst = max(abs(s.gpu_norm - s.ref_norm) / s.ref_norm for s in rep.steps)
+    print(f"{rep.name}: n={rep.n} steps={len(rep.steps)} bit-exact steps={exact} worst norm rel err={worst:.2e}")
+
+
+def test_tiny_full():
+    rep = run_workload(W.tiny(), steps=3)
+    assert len(rep.steps) == 3 and all(s.gpu_coef == 1.0 for s in rep.steps)
+    _summary(rep)
+
+
+def test_tiny_short_tail_shard():
+    """tiny list, 8 ranks, rank 7: the short last shard [1,104,159, 1,261,891)."""
+    wl = W.tiny().with_(world_size=8, rank=7, max_norm=0.5)
+    rep = run_workload(wl, steps=3)
+    assert rep.n == 157732
+    _summary(rep)
+
+
+def test_gpt2_zero1_rank3_full():
+    rep = run_workload(W.gpt2_zero1(), steps=10)
+    assert all(s.ref_coef < 1.0 for s in rep.steps), "clipping expected to trigger"
+    _summary(rep)
+
+
+def test_ragged_rank2_full():
+    rep = run_workload(W.ragged(), steps=5)
+    assert all(s.ref_coef < 1.0 for s in rep.steps)
+    _summary(rep)
+
+
+def test_llama7b_full_size_sampled():
+    wl = W.llama7b()
+    rep = run_workload(wl, steps=2, sample=1_000_000)
+    assert rep.n == 6738415616
+    _summary(rep)
+
+
+def test_llama7b_shape_all_steps():
+    wl = W.small_llama(layers=4, hidden=512, mlp=1376, vocab=3200)
+    rep = run_workload(wl, steps=W.llama7b().steps)
+    _summary(rep)
+
+
+def test_llama13b_zero3_rank7_full_size_sampled():
+    wl = W.llama13b_zero3()
+    rep = run_workload(wl, steps=1, sample=1_000_000)
+    assert rep.n == 1626983040
+    assert rep.steps[0].ref_coef < 1.0
+    _summary(rep)
+
+
+def test_llama13b_zero3_shape_all_steps():
+    wl = W.llama13b_zero3().with_(numels=tuple(W.llama_numels(5, 640, 1728, 4000)), max_norm=0.1)
+    rep = run_workload(wl, steps=W.llama13b_zero3().steps)
+    assert all(s.ref_coef < 1.0 for s in rep.steps)
+    _summary(rep)
+
+
+def test_null_grads_and_fp16_writeback():
+    """Tensors without grad read as zeros; the ZeRO-3 fp16 local chunk as the low-precision copy."""
+    wl = W.small_ragged(n_tensors=400, null_grads=(0, 5, 399), lowp_dtype="f16", world_size=3, rank=1)
+    rep = run_workload(wl, steps=3)
+    _summary(rep)
+
+
+def test_nonfinite_grad_skips_step():
+    """An inf grad makes the norm non-finite: the step is skipped on both sides, t does not move."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
+    dev = torch.device("cuda:0")
+    opt = FlatShardAdamW([1000, 24], lr=1e-3, max_norm=1.0, device=dev,
+                         master=torch.linspace(-1, 1, 1024, device=dev))
+    g = [torch.full((1000,), 1e-3, device=dev, dtype=torch.bfloat16), torch.zeros(24, device=dev, dtype=torch.bfloat16)]
+    opt.flatten(g, accumulate=False)
+    assert opt.step().finite and opt.t == 1
+    snap = [x.clone() for x in (opt.master, opt.exp_avg, opt.exp_avg_sq, opt.lowp)]
+    g[1][3] = math.inf
+    opt.found_nonfinite.zero_()
+    opt.flatten(g, accumulate=False)
+    r = opt.step()
+    assert not r.finite and opt.t == 1 and opt.found_nonfinite.item() == 1
+    for a, b in zip(snap, (opt.master, opt.exp_avg, opt.exp_avg_sq, opt.lowp)):
+        assert torch.equal(a, b)

@@ -1,0 +1,312 @@
+"""GPU parity of each kernel against the CPU oracle, through the C ABI.
+
+Adversarial cases: empty, 1, 7, 8, 9 elements, sizes spanning several tiles
+with a ragged tail, every start alignment within a 32-byte line, source and
+destination misaligned relative to each other, tensors without grad,
+zero-size tensors, shard cuts inside tensors, non-finite values.  Every
+buffer sits inside a larger allocation whose guard bands are checked after
+the call.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from _helpers import (RTOL_NORM, assert_close_f32, assert_lowp_ulp, assert_lowp_ulp_f16, bits_equal_f32,
+                      norm_result_tensor, raw)
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+GUARD = 40
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from fsdp_sharded_mixed_flatparameter_gb300 import build, zero_shard
+    build.build()
+    zero_shard.lib()
+    torch.cuda.init()
+
+
+class Guarded:
+    """A device buffer at a chosen element offset inside a NaN-filled allocation."""
+
+    def __init__(self, n, dtype, offset, fill: torch.Tensor = None):
+        self.base = torch.empty(n + offset + GUARD, dtype=dtype, device=DEV)
+        self.base.view(torch.uint8).fill_(0xFF)  # NaN pattern for float types
+        self.offset, self.n = offset, n
+        self.t = self.base[offset:offset + n]
+        if fill is not None:
+            self.t.copy_(fill.to(DEV))
+        self.snap = self.base.clone()
+
+    def check_guards(self):
+        b, s = self.base.view(torch.uint8), self.snap.view(torch.uint8)
+        es = self.base.element_size()
+        lo, hi = self.offset * es, (self.offset + self.n) * es
+        assert torch.equal(b[:lo], s[:lo]) and torch.equal(b[hi:], s[hi:]), "write outside the buffer"
+
+
+def _rand(n, seed, std=1.0, dtype=torch.float32):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(n, generator=g) * std).to(dtype)
+
+
+# ----------------------------------------------------------------- K4 AdamW
+SIZES = [0, 1, 7, 8, 9, 31, 257, 4096 + 13, 100003]
+
+
+@pytest.mark.parametrize("n", SIZES)
+@pytest.mark.parametrize("lowp", [torch.bfloat16, torch.float16, None])
+def test_adamw_matches_oracle_bit_exact(n, lowp):
+    """Fused AdamW vs the oracle for 3 steps, each buffer at its own alignment.
+    The kernel follows the oracle's rounding sequence, so the fp32 state is
+    expected bit for bit; the bar (1e-6 relative, 1 ulp) is checked as well."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    rng = np.random.default_rng(n + 7)
+    for trial, (po, mo, vo, go, lo) in enumerate([(0, 0, 0, 0, 0), (3, 3, 3, 3, 5), (5, 5, 5, 5, 2),
+                                                    (1, 2, 3, 4, 1), (7, 7, 7, 7, 7)]):
+        p0 = _rand(n, 10 + trial, 0.02)
+        P = Guarded(n, torch.float32, po, p0)
+        M = Guarded(n, torch.float32, mo, torch.zeros(n))
+        V = Guarded(n, torch.float32, vo, torch.zeros(n))
+        L = Guarded(n, lowp, lo) if lowp is not None else None
+        st = oracle.new_state(p0.numpy())
+        lr, b1, b2, eps, wd = 3e-4, 0.9, 0.95, 1e-8, 0.1
+        for t in range(1, 4):
+            g = _rand(n, 100 * t + trial, 10.0 ** rng.uniform(-6, -1))
+            if n > 3:
+                g[1] = 0.0
+            G = Guarded(n, torch.float32, go, g)
+            coef = float(np.float32(rng.uniform(0.2, 1.0)))
+            clip = norm_result_tensor(DEV, norm=1.0 / coef, coef=coef)
+            zs.zero_adamw_step(P.t, M.t, V.t, G.t, None if L is None else L.t, lr, b1, b2, eps, wd, t, clip)
+            sc = oracle.adamw_scalars(lr, b1, b2, eps, wd, t)
+            oracle.adamw(st.p, st.m, st.v, g.numpy(), sc, np.float32(coef), st.lowp,
+                         "f16" if lowp == torch.float16 else "bf16")
+        torch.cuda.synchronize()
+        for B in (P, M, V) + ((L,) if L is not None else ()):
+            B.check_guards()
+        for name, B, ref in (("p", P, st.p), ("m", M, st.m), ("v", V, st.v)):
+            got = raw(B.t)
+            assert_close_f32(got, ref, name=f"{name} trial {trial}")
+            assert bits_equal_f32(got, ref), f"{name} not bit-exact, trial {trial}"
+        if L is not None:
+            (assert_lowp_ulp_f16 if lowp == torch.float16 else assert_lowp_ulp)(raw(L.t), st.lowp, name="lowp")
+            assert np.array_equal(raw(L.t), st.lowp), "low-precision copy not bit-exact"
+
+
+def test_adamw_skips_on_nonfinite_norm():
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    n = 5000
+    P = Guarded(n, torch.float32, 0, _rand(n, 1, 0.02))
+    M = Guarded(n, torch.float32, 0, _rand(n, 2, 1e-3))
+    V = Guarded(n, torch.float32, 0, _rand(n, 3, 1e-3) ** 2)
+    L = Guarded(n, torch.bfloat16, 0)
+    G = Guarded(n, torch.float32, 0, _rand(n, 4, 1e-3))
+    before = [B.base.clone() for B in (P, M, V, L)]
+    clip = norm_result_tensor(DEV, norm=math.inf, coef=0.0, finite=False)
+    zs.zero_adamw_step(P.t, M.t, V.t, G.t, L.t, 1e-3, 0.9, 0.999, 1e-8, 0.01, 5, clip)
+    torch.cuda.synchronize()
+    for b, B in zip(before, (P, M, V, L)):
+        assert torch.equal(b.view(torch.uint8), B.base.view(torch.uint8))
+
+
+def test_adamw_without_clip_and_special_values():
+    """No clip result (coefficient 1); inf/NaN/huge grads propagate as in the oracle."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    n = 1000
+    g = _rand(n, 9, 1e-2)
+    g[10], g[11], g[12], g[13] = math.inf, -math.inf, math.nan, 3e38
+    p0 = _rand(n, 8, 0.02)
+    p0[20] = 70000.0  # overflows f16 on the write-back
+    P, M, V = (Guarded(n, torch.float32, 0, x) for x in (p0, torch.zeros(n), torch.zeros(n)))
+    G = Guarded(n, torch.float32, 0, g)
+    L = Guarded(n, torch.float16, 0)
+    zs.zero_adamw_step(P.t, M.t, V.t, G.t, L.t, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, None)
+    st = oracle.new_state(p0.numpy())
+    oracle.adamw(st.p, st.m, st.v, g.numpy(), oracle.adamw_scalars(1e-3, 0.9, 0.999, 1e-8, 0.0, 1), 1.0, st.lowp,
+                 "f16")
+    torch.cuda.synchronize()
+    for B, ref in ((P, st.p), (M, st.m), (V, st.v)):
+        assert bits_equal_f32(raw(B.t), ref)
+    assert_lowp_ulp_f16(raw(L.t), st.lowp)
+
+
+# --------------------------------------------------------------- K3 sqnorm
+NORM_SIZES = [0, 1, 5, 32767, 32768, 32769, 3 * 32768 + 5, 1_000_003, 12_582_917]
+
+
+@pytest.mark.parametrize("n", NORM_SIZES)
+@pytest.mark.parametrize("offset", [0, 1])
+def test_grad_sqnorm_matches_oracle(n, offset):
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    g = _rand(n, n % 1000 + offset, 1e-3) * torch.exp(torch.linspace(-8, 8, n)) if n else torch.zeros(0)
+    G = Guarded(n, torch.float32, offset, g)
+    ws = torch.empty(max(zs.zero_grad_sqnorm_workspace_bytes(n), 8), dtype=torch.uint8, device=DEV)
+    out = zs.new_norm_result(DEV)
+    for max_norm, extra in ((1.0, 0.0), (0.5, 2.5), (math.inf, 0.0)):
+        zs.zero_grad_sqnorm(G.t, extra, max_norm, ws, out)
+        r1 = zs.decode_norm_result(out)
+        zs.zero_grad_sqnorm(G.t, extra, max_norm, ws, out)
+        r2 = zs.decode_norm_result(out)
+        assert r1 == r2, "not deterministic"
+        cr = oracle.clip(oracle.sqnorm(g.numpy()), extra, max_norm)
+        assert r1.finite and cr.finite
+        if cr.norm == 0.0:
+            assert r1.norm == 0.0
+        else:
+            assert abs(r1.norm - cr.norm) <= RTOL_NORM * cr.norm, (r1.norm, cr.norm)
+            assert abs(r1.norm - cr.norm) <= 5e-7 * cr.norm  # the kernel's own error budget
+        assert abs(r1.clip_coef - cr.coef) <= RTOL_NORM * cr.coef
+    G.check_guards()
+
+
+def test_grad_sqnorm_closed_form_and_launch_independence():
+    """All-equal c: sum of squares c^2 n exactly (c with few mantissa bits)."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    for n, c in ((32768 * 7 + 3, 0.75), (4_000_000, 3.0517578125e-05), (1, -1.5)):
+        G = Guarded(n, torch.float32, 0, torch.full((n,), c))
+        ws = torch.empty(zs.zero_grad_sqnorm_workspace_bytes(n), dtype=torch.uint8, device=DEV)
+        out = zs.new_norm_result(DEV)
+        zs.zero_grad_sqnorm(G.t, 0.0, math.inf, ws, out)
+        r = zs.decode_norm_result(out)
+        assert r.sqnorm == n * c * c and r.clip_coef == 1.0
+
+
+def test_grad_sqnorm_nonfinite_and_empty():
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    n = 100000
+    for bad in (math.inf, -math.inf, math.nan):
+        g = _rand(n, 3, 1e-3)
+        g[77777] = bad
+        G = Guarded(n, torch.float32, 0, g)
+        ws = torch.empty(zs.zero_grad_sqnorm_workspace_bytes(n), dtype=torch.uint8, device=DEV)
+        out = zs.new_norm_result(DEV)
+        zs.zero_grad_sqnorm(G.t, 0.0, 1.0, ws, out)
+        assert not zs.decode_norm_result(out).finite
+    out = zs.new_norm_result(DEV)
+    zs.zero_grad_sqnorm(torch.zeros(0, device=DEV), 4.0, 1.0, None, out)
+    r = zs.decode_norm_result(out)
+    assert r.finite and r.norm == 2.0 and r.clip_coef == np.float32(1.0 / (2.0 + 1e-6))
+
+
+# ---------------------------------------------------------------- K2 accum
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("n", [0, 1, 9, 1000, 262147])
+def test_accum_matches_oracle_bit_exact(dtype, n):
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    tdt = W.torch_dtype(dtype)
+    for ao, so in ((0, 0), (3, 3), (1, 6), (0, 5), (7, 0)):
+        A = Guarded(n, torch.float32, ao)
+        ref = np.zeros(n, np.float32)
+        flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+        for j, scale in enumerate((0.125, 0.125, 1.0 / 3.0)):
+            x = _rand(n, 50 * j + ao + so, 1e-3, tdt)
+            S = Guarded(n, tdt, so, x)
+            zs.zero_accum(A.t, S.t, scale, accumulate=j > 0, found_nonfinite=flag)
+            oracle.accum(ref, raw(x), dtype, scale, accumulate=j > 0)
+            S.check_guards()
+        torch.cuda.synchronize()
+        A.check_guards()
+        assert bits_equal_f32(raw(A.t), ref), (ao, so)
+        assert flag.item() == 0
+
+
+def test_accum_flags_nonfinite():
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    n = 10007
+    for where in (0, 5, 5000, n - 1):
+        x = _rand(n, 1, 1e-3, torch.float16)
+        x[where] = math.inf
+        acc = torch.zeros(n, device=DEV)
+        flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+        zs.zero_accum(acc, x.to(DEV), 0.125, False, flag)
+        assert flag.item() == 1
+    # a finite value that overflows once scaled is flagged too
+    x = torch.full((100,), 3e38)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    zs.zero_accum(torch.zeros(100, device=DEV), x.to(DEV), 4.0, False, flag)
+    assert flag.item() == 1
+
+
+# -------------------------------------------------------------- K1 flatten
+def _table_case(numels, dtype, null=(), seed=0, elem_offsets=None):
+    """Per-tensor device grads: each tensor at its own element offset in its own allocation."""
+    tdt = W.torch_dtype(dtype)
+    host, dev = [], []
+    g = torch.Generator().manual_seed(seed)
+    for i, n in enumerate(numels):
+        if i in null:
+            host.append(None)
+            dev.append(None)
+            continue
+        x = (torch.randn(n, generator=g) * 1e-2).to(tdt)
+        off = 0 if elem_offsets is None else elem_offsets[i % len(elem_offsets)]
+        base = torch.empty(n + off + 8, dtype=tdt, device=DEV)
+        v = base[off:off + n]
+        v.copy_(x.to(DEV))
+        host.append(x)
+        dev.append(v)
+    return host, dev
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_flatten_ragged_matches_oracle_bit_exact(dtype):
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    numels = list(W.ragged_numels(300, seed=5, max_log2=14))
+    numels[4] = 0
+    numels[17] = 0
+    numels[40] = 20000  # spans several 8192-element tiles
+    host, dev = _table_case(numels, dtype, null=(2, 9, 40), seed=3, elem_offsets=[0, 1, 3, 8, 5])
+    table, total = zs.zero_tensor_table(dev, numels)
+    d_table = zs.device_table(table, len(numels), DEV)
+    rawh = [raw(h) for h in host]
+    for world, rank in ((1, 0), (4, 2), (7, 6), (3, 1), (16, 15)):
+        s, e = oracle.shard_range(total, world, rank)
+        for dst_off in (0, 1, 4):
+            D = Guarded(e - s, torch.float32, dst_off)
+            ref = np.zeros(e - s, np.float32)
+            flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+            for j, scale in enumerate((0.125, 0.125, 1.0)):
+                zs.zero_flatten_cast(d_table, len(numels), total, W.torch_dtype(dtype), s, e, scale, j > 0, D.t,
+                                     flag)
+                oracle.flatten(rawh, numels, dtype, s, e, scale, ref, accumulate=j > 0)
+            torch.cuda.synchronize()
+            D.check_guards()
+            assert bits_equal_f32(raw(D.t), ref), (world, rank, dst_off)
+            assert flag.item() == 0
+
+
+def test_flatten_big_aligned_tensors_fast_path():
+    """Llama-shaped list (tensors aligned, tiles inside one tensor) vs torch.cat and the oracle."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    wl = W.small_llama(layers=2, hidden=256, mlp=688, vocab=1000)
+    tg = W.tensor_grads(wl, 1, 0, device=DEV)
+    table, total = zs.zero_tensor_table(tg.tensors, wl.numels)
+    d_table = zs.device_table(table, wl.n_tensors, DEV)
+    full = torch.cat([t.float() for t in tg.tensors])
+    for world, rank in ((1, 0), (8, 3), (5, 4)):
+        s, e = oracle.shard_range(total, world, rank)
+        dst = torch.empty(e - s, device=DEV)
+        zs.zero_flatten_cast(d_table, wl.n_tensors, total, torch.bfloat16, s, e, 1.0, False, dst)
+        assert torch.equal(dst.view(torch.int32), full[s:e].view(torch.int32))
+
+
+def test_flatten_flags_nonfinite():
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    numels = [100, 50000, 7]
+    host, dev = _table_case(numels, "bf16", seed=1)
+    dev[1][33333] = math.nan
+    table, total = zs.zero_tensor_table(dev, numels)
+    d_table = zs.device_table(table, 3, DEV)
+    dst = torch.empty(total, device=DEV)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    zs.zero_flatten_cast(d_table, 3, total, torch.bfloat16, 0, 100 + 33333, 1.0, False, dst, flag)
+    assert flag.item() == 0  # the NaN lies outside the range
+    zs.zero_flatten_cast(d_table, 3, total, torch.bfloat16, 0, total, 1.0, False, dst, flag)
+    assert flag.item() == 1
