@@ -5,19 +5,31 @@
 //
 //  1. sqnorm_tiles_kernel: the grad buffer is cut into fixed tiles of
 //     kSqTile = 32768 elements.  A block reduces one tile at a time: each of
-//     its 256 threads squares 128 elements (16 x 32-byte loads, two rounds of
-//     eight) and sums them by a fixed binary tree in binary32 (depth 7), the
-//     256 thread sums are added in binary64 by a fixed shuffle/shared-memory
-//     tree, and the tile's binary64 partial is stored.  A persistent grid
-//     strides over the tiles, so the partial of a tile does not depend on
-//     which block computed it or how many blocks ran.
+//     its 256 threads takes 128 elements (16 x 32-byte loads, two rounds of
+//     eight) and adds their squares into a double-float accumulator (an
+//     unevaluated sum hi + lo of two binary32 values): every square is split
+//     exactly into x*x = p + e with one fma, p is added to hi with an
+//     error-free TwoSum, and the two error terms go into lo.  The 256 thread
+//     sums are added in binary64 by a fixed shuffle/shared-memory tree and the
+//     tile's binary64 partial is stored.  A persistent grid strides over the
+//     tiles, so the partial of a tile does not depend on which block computed
+//     it or how many blocks ran.
 //  2. sqnorm_finalize_kernel: one block adds the partials in a fixed order
 //     (binary64), adds the other ranks' share, takes the square root and the
 //     clip coefficient, and writes the zero_norm_result.
 //
-// Accuracy: each square is one rounding, the tree adds at most 7 more per
-// path, so the relative error of the sum of squares is below ~8 * 2^-24
-// (< 5e-7; about 2.5e-7 on the norm), far inside the 1e-5 the step needs.
+// Accuracy: the double-float sum carries about 48 significant bits, so the
+// relative error of the sum of squares is ~1e-14 (binary64 beyond the
+// thread level), about as good as the compensated binary64 sum of the CPU
+// oracle.  That is what makes the binary32 clip coefficient -- and with it
+// the whole AdamW step -- agree bit for bit with the oracle in practice: a
+// coarser norm would move the coefficient by an ulp now and then, and where
+// p*(1-lr*wd) and the Adam update nearly cancel, that ulp is a large
+// relative error of the new parameter.  The extra arithmetic (~10 binary32
+// operations per element) hides under the 4 bytes/element memory stream.
+// Limits: squares outside the binary32 range (|g| >= 2^64 overflows to a
+// non-finite norm, |g| < 2^-75 underflows toward 0) are where the result can
+// differ from the binary64 oracle; gradients never come near either.
 // No atomics: the result is bit-identical from run to run and GPU to GPU.
 #include "common.cuh"
 #include "kernels.h"
@@ -28,17 +40,15 @@ constexpr int kSqThreads = 256;
 constexpr int kSqVecPerThread = 16;  // 16 x 8 = 128 elements per thread per tile
 static_assert(kSqThreads * kSqVecPerThread * 8 == kSqTile, "tile size");
 
-__device__ __forceinline__ float sum8_sq(const float (&x)[8]) {
-  float q[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(x[i], x[i]);
-  return __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
-                   __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
-}
-
-__device__ __forceinline__ float tree8(const float (&s)[8]) {
-  return __fadd_rn(__fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3])),
-                   __fadd_rn(__fadd_rn(s[4], s[5]), __fadd_rn(s[6], s[7])));
+// hi + lo += x*x, error-free except for the rounding of lo itself
+__device__ __forceinline__ void df_add_square(float& hi, float& lo, float x) {
+  const float p = __fmul_rn(x, x);
+  const float e = __fmaf_rn(x, x, -p);  // x*x == p + e exactly
+  const float s = __fadd_rn(hi, p);     // TwoSum(hi, p) = s + t exactly
+  const float bp = __fsub_rn(s, hi);
+  const float t = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
+  hi = s;
+  lo = __fadd_rn(lo, __fadd_rn(t, e));
 }
 
 // Block-wide binary64 sum in a fixed order; the result is valid in thread 0.
@@ -60,9 +70,10 @@ __device__ __forceinline__ double block_sum(double x, double* red) {
 
 // Element e of a tile belongs to thread t, vector slot r, lane i where
 // e = ((r * 256) + t) * 8 + i: each 32-byte load of a warp covers 1 KiB.
+// The thread adds its 128 squares in that (r, i) order.
 template <bool VEC>
-__device__ __forceinline__ float thread_tile_sum(const float* __restrict__ g, int64_t base, int64_t n) {
-  float rs[2];
+__device__ __forceinline__ double thread_tile_sum(const float* __restrict__ g, int64_t base, int64_t n) {
+  float hi = 0.0f, lo = 0.0f;
 #pragma unroll
   for (int round = 0; round < 2; ++round) {
     float x[8][8];
@@ -76,12 +87,13 @@ __device__ __forceinline__ float thread_tile_sum(const float* __restrict__ g, in
         for (int i = 0; i < 8; ++i) x[r][i] = (e + i < n) ? __ldg(g + e + i) : 0.0f;
       }
     }
-    float s[8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) s[r] = sum8_sq(x[r]);
-    rs[round] = tree8(s);
+    for (int r = 0; r < 8; ++r) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) df_add_square(hi, lo, x[r][i]);
+    }
   }
-  return __fadd_rn(rs[0], rs[1]);
+  return static_cast<double>(hi) + static_cast<double>(lo);
 }
 
 __global__ void __launch_bounds__(kSqThreads) sqnorm_tiles_kernel(const float* __restrict__ g, int64_t n,
@@ -90,12 +102,9 @@ __global__ void __launch_bounds__(kSqThreads) sqnorm_tiles_kernel(const float* _
   __shared__ double red[kSqThreads / 32];
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const int64_t base = tile * kSqTile;
-    float ts;
-    if (vec_ok && base + kSqTile <= n)
-      ts = thread_tile_sum<true>(g, base, n);
-    else
-      ts = thread_tile_sum<false>(g, base, n);
-    const double bs = block_sum<kSqThreads>(static_cast<double>(ts), red);
+    const double ts = (vec_ok && base + kSqTile <= n) ? thread_tile_sum<true>(g, base, n)
+                                                      : thread_tile_sum<false>(g, base, n);
+    const double bs = block_sum<kSqThreads>(ts, red);
     if (threadIdx.x == 0) partials[tile] = bs;
   }
 }

@@ -160,5 +160,9 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
         (assert_lowp_ulp_f16 if wl.lowp_dtype == "f16" else assert_lowp_ulp)(got["lowp"], st.lowp,
                                                                                 name=f"{wl.name} step {t} lowp")
         exact &= bool(np.array_equal(got["lowp"], st.lowp))
+        # both sides follow the same rounding sequence: with the same binary32
+        # clip coefficient the whole state must agree bit for bit
+        if res.clip_coef == cr.coef:
+            assert exact, f"{wl.name} step {t}: same coefficient but state not bit-exact"
         report.steps.append(StepReport(t, res.norm, cr.norm, res.clip_coef, cr.coef, exact))
     return report

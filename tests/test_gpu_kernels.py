@@ -161,7 +161,7 @@ def test_grad_sqnorm_matches_oracle(n, offset):
             assert r1.norm == 0.0
         else:
             assert abs(r1.norm - cr.norm) <= RTOL_NORM * cr.norm, (r1.norm, cr.norm)
-            assert abs(r1.norm - cr.norm) <= 5e-7 * cr.norm  # the kernel's own error budget
+            assert abs(r1.norm - cr.norm) <= 1e-12 * cr.norm  # the kernel's own error budget (double-float)
         assert abs(r1.clip_coef - cr.coef) <= RTOL_NORM * cr.coef
     G.check_guards()
 
