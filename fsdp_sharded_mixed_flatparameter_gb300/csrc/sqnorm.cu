@@ -31,6 +31,9 @@
 // non-finite norm, |g| < 2^-75 underflows toward 0) are where the result can
 // differ from the binary64 oracle; gradients never come near either.
 // No atomics: the result is bit-identical from run to run and GPU to GPU.
+#include <cmath>
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -148,4 +151,59 @@ zero_status launch_sqnorm(const float* g, int64_t n, double extra_sqnorm, double
   return check_launch("sqnorm_finalize_kernel");
 }
 
+// ---------------------------------------------------------------------------
+// zero_grad_sqnorm_noalloc: the same grad-norm computation for callers that
+// cannot allocate device memory.  The tile partials live in a fixed array in
+// this library's own device memory instead of a caller-provided workspace.
+// The array is a module global: every GPU that loads the library holds its
+// 4 MiB until the process exits.  In host code `g_noalloc_partials` is only a
+// host-side stand-in for the symbol, never a device address; the device
+// address is looked up once per device with cudaGetSymbolAddress.
+
+constexpr int64_t kNoAllocMaxTiles = int64_t(1) << 19;  // 4 MiB of binary64 partials
+
+static __device__ __align__(256) double g_noalloc_partials[kNoAllocMaxTiles];
+
+namespace {
+constexpr int kMaxDevices = 256;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+}  // namespace
+
 }  // namespace zs
+
+extern "C" zero_status zero_grad_sqnorm_noalloc(const float* d_grad, int64_t n, double extra_sqnorm,
+                                                double max_norm, zero_norm_result* d_out, void* stream) {
+  using zs::fail;
+  if (n < 0) return fail(ZERO_EINVAL, "zero_grad_sqnorm_noalloc: n %lld < 0", (long long)n);
+  if (n > zs::kNoAllocMaxTiles * zs::kSqTile)
+    return fail(ZERO_EINVAL,
+                "zero_grad_sqnorm_noalloc: n = %lld exceeds the built-in scratch limit of %lld elements "
+                "(%lld tiles of %lld); use zero_grad_sqnorm with a caller workspace",
+                (long long)n, (long long)(zs::kNoAllocMaxTiles * zs::kSqTile), (long long)zs::kNoAllocMaxTiles,
+                (long long)zs::kSqTile);
+  if (n > 0 && d_grad == nullptr) return fail(ZERO_EINVAL, "zero_grad_sqnorm_noalloc: NULL d_grad");
+  if (d_out == nullptr) return fail(ZERO_EINVAL, "zero_grad_sqnorm_noalloc: NULL d_out");
+  if (std::isnan(max_norm) || max_norm < 0.0) return fail(ZERO_EINVAL, "zero_grad_sqnorm_noalloc: bad max_norm");
+  if (!std::isfinite(extra_sqnorm) || extra_sqnorm < 0.0)
+    return fail(ZERO_EINVAL, "zero_grad_sqnorm_noalloc: bad extra_sqnorm");
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return fail(ZERO_ECUDA, "zero_grad_sqnorm_noalloc: cudaGetDevice: %s", cudaGetErrorString(ce));
+  if (dev < 0 || dev >= zs::kMaxDevices) return fail(ZERO_EINVAL, "zero_grad_sqnorm_noalloc: device %d", dev);
+  void* scratch = nullptr;
+  {
+    // once per device, with that device current: find the array's device address
+    std::lock_guard<std::mutex> lk(zs::g_noalloc_mu);
+    if (zs::g_noalloc_addr[dev] == nullptr) {
+      void* p = nullptr;
+      ce = cudaGetSymbolAddress(&p, zs::g_noalloc_partials);
+      if (ce != cudaSuccess || p == nullptr)
+        return fail(ZERO_ECUDA, "zero_grad_sqnorm_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(ce));
+      zs::g_noalloc_addr[dev] = p;
+    }
+    scratch = zs::g_noalloc_addr[dev];
+  }
+  return zs::launch_sqnorm(d_grad, n, extra_sqnorm, max_norm, static_cast<double*>(scratch), d_out,
+                           zs::as_stream(stream));
+}

@@ -71,6 +71,7 @@ def lib() -> ctypes.CDLL:
     L.zero_grad_sqnorm_workspace_bytes.argtypes = [i64]
     L.zero_grad_sqnorm_workspace_bytes.restype = ctypes.c_size_t
     L.zero_grad_sqnorm.argtypes = [vp, i64, f64, f64, vp, ctypes.c_size_t, vp, vp]
+    L.zero_grad_sqnorm_noalloc.argtypes = [vp, i64, f64, f64, vp, vp]
     L.zero_adamw_step.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, i64, ctypes.POINTER(zero_adamw_hparams), i64,
                                   vp, vp]
     L.zero_status_string.argtypes = [ctypes.c_int]
@@ -78,7 +79,7 @@ def lib() -> ctypes.CDLL:
     L.zero_last_error.argtypes = []
     L.zero_last_error.restype = ctypes.c_char_p
     for nm in ("zero_shard_range", "zero_tensor_table", "zero_flatten_cast", "zero_accum", "zero_grad_sqnorm",
-               "zero_adamw_step"):
+               "zero_grad_sqnorm_noalloc", "zero_adamw_step"):
         getattr(L, nm).restype = ctypes.c_int
     _lib = L
     return L
@@ -182,6 +183,15 @@ def zero_grad_sqnorm(grad: torch.Tensor, extra_sqnorm: float, max_norm: float, w
     _check(lib().zero_grad_sqnorm(_dev(grad, "grad", torch.float32), grad.numel(), extra_sqnorm, max_norm,
                                   _dev(ws, "ws", allow_none=True), 0 if ws is None else ws.numel() * ws.element_size(),
                                   _dev(out, "out"), _stream(stream)))
+
+
+def zero_grad_sqnorm_noalloc(grad: torch.Tensor, extra_sqnorm: float, max_norm: float, out: torch.Tensor,
+                             stream=None) -> None:
+    """zero_grad_sqnorm for callers that cannot allocate a workspace (library-owned scratch)."""
+    if out.numel() * out.element_size() < NORM_RESULT_BYTES:
+        raise ValueError("out is smaller than zero_norm_result")
+    _check(lib().zero_grad_sqnorm_noalloc(_dev(grad, "grad", torch.float32), grad.numel(), extra_sqnorm, max_norm,
+                                          _dev(out, "out"), _stream(stream)))
 
 
 def zero_adamw_step(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg_sq: torch.Tensor, grad: torch.Tensor,

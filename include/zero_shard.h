@@ -18,8 +18,9 @@
  *
  * Conventions for every call:
  *  - Memory.  The library allocates nothing (device or host) and keeps no
- *    state between calls beyond a per-device cache of launch sizes.  The
- *    caller owns every buffer.  Pointers prefixed d_ are device addresses;
+ *    state between calls beyond a per-device cache of launch sizes (and the
+ *    fixed scratch array of zero_grad_sqnorm_noalloc).  The caller owns
+ *    every buffer.  Pointers prefixed d_ are device addresses;
  *    everything else is host memory.
  *  - Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *    default stream).  Device work is enqueued asynchronously on it; no call
@@ -217,6 +218,31 @@ zero_status zero_adamw_step(float* d_master, float* d_exp_avg, float* d_exp_avg_
                             const float* d_grad, void* d_param_lowp, zero_dtype lowp_dtype,
                             int64_t n, const zero_adamw_hparams* hp, int64_t step,
                             const zero_norm_result* d_clip, void* stream);
+
+/* zero_grad_sqnorm_noalloc -- device.  No counterpart on the source pages:
+ * a convenience of this library.
+ * Computes exactly what zero_grad_sqnorm computes, for callers that cannot
+ * allocate device memory for its workspace: code that runs inside another
+ * framework's memory pool which owns all device memory, inside an allocator
+ * hook, or in a loop that must not pay the implicit device synchronisation
+ * that cudaMalloc/cudaFree can cause.  Instead of a caller workspace the
+ * tile partials go to a fixed array inside the library: 4 MiB of device
+ * memory on every GPU that loads the library, held until the process exits.
+ * The caller still passes d_grad and d_out; the call itself allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * Limit: n <= 2^19 tiles * 32768 = 17,179,869,184 elements; a larger n
+ * returns ZERO_EINVAL with a message that names the limit.
+ * Set-up: the first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture begins.
+ * Sharing: all calls on a device use the same array, which keeps the last
+ * call's partials.  Calls whose work overlaps on the GPU (for example on two
+ * streams at once) race on it; the caller must serialise them.  Nothing
+ * needs clearing between calls: each call writes every partial it reads.
+ * Errors: those of zero_grad_sqnorm without the workspace checks, the limit
+ * above, and ZERO_ECUDA if the address lookup fails. */
+zero_status zero_grad_sqnorm_noalloc(const float* d_grad, int64_t n, double extra_sqnorm,
+                                     double max_norm, zero_norm_result* d_out, void* stream);
 
 /* Static text for a status code. */
 const char* zero_status_string(zero_status status);
