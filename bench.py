@@ -50,16 +50,30 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
+def adamw_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("adamw.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "fsdp_sharded_mixed_flatparameter_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def adamw_traffic_per_param():
-    """DRAM bytes per parameter of the AdamW kernel from the committed ncu summary, if current."""
+    """DRAM bytes per parameter of the AdamW kernel from the committed ncu summary,
+    or None when the kernel sources have changed since those counters were taken."""
+    vals = {}
     try:
         with open(TRAFFIC_FILE) as f:
             for line in f:
-                if line.startswith("dram_bytes_per_param:"):
-                    return float(line.split(":", 1)[1])
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    vals[k.strip()] = v.strip()
     except OSError:
-        pass
-    return None
+        return None
+    if vals.get("adamw_source_sha256") != adamw_source_hash():
+        return None
+    return float(vals["dram_bytes_per_param"]) if "dram_bytes_per_param" in vals else None
 
 
 class ClockSampler:
@@ -191,6 +205,10 @@ def run_gpu(args):
         pg = dist
 
     base = W.llama7b()
+    if args.small:
+        # profiling case: same tensor shapes per layer, 1 layer, smaller vocab (268M params,
+        # ~5 GB on the device, still far larger than L2)
+        base = base.with_(name="llama7b_1layer_v8000", numels=tuple(W.llama_numels(1, 4096, 11008, 8000)))
     # weak scaling: the flat parameter list is `world` copies of the Llama-7B
     # list, so every rank's ZeRO shard is exactly one Llama-7B-shaped buffer
     wl = base.with_(numels=base.numels * world, world_size=world, rank=rank)
@@ -285,7 +303,7 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "llama7b_flat", "params_per_rank": n, "tensors": len(grads), "world_size": world,
+        "config": {"workload": base.name, "params_per_rank": n, "tensors": len(grads), "world_size": world,
                    "grad_dtype": "bf16", "lowp_dtype": "bf16", "max_norm": wl.max_norm,
                    "l2": "inputs larger than L2 (135 GB resident per GPU); no flush"},
         "roofline": {"bound": "hbm", "kernel": "adamw_v8_kernel", "achieved": achieved, "peak": hbm,
@@ -319,6 +337,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small", action="store_true",
+                    help="profiling case for ncu: a 1-layer Llama-7B-shaped list (268M params), not a bench line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         raise SystemExit("--warmup must be >= 3")
