@@ -9,11 +9,11 @@
 // step is an explicitly rounded binary32 intrinsic, so the compiler cannot
 // contract or reorder it and the result is the same on every run.
 //
-// Work split: a persistent grid (SM count x resident blocks) strides over
-// groups of 8 consecutive elements; each group is four 32-byte loads, three
-// 32-byte stores and one store of 8 packed 16-bit values.  Up to 7 leading
-// elements (to reach 32-byte alignment) and 7 trailing ones are done by
-// single threads of the same launch.
+// Work split: one pass, one thread per group of 8 consecutive elements
+// (256 groups per block, as many blocks as groups need); each group is four
+// 32-byte loads, three 32-byte stores and one store of 8 packed 16-bit
+// values.  Up to 7 leading elements (to reach 32-byte alignment) and 7
+// trailing ones are done by single threads of the same launch.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -117,13 +117,7 @@ template <int LOWP, int LW>
 static zero_status launch_v8(float* p, float* m, float* v, const float* g, void* lowp, int64_t head,
                              int64_t nvec, int64_t n, const AdamScalars& s, const zero_norm_result* clip,
                              cudaStream_t st) {
-  const void* fn = reinterpret_cast<const void*>(&adamw_v8_kernel<LOWP, LW>);
-  int64_t want = (nvec + 255) / 256;
-  int64_t blocks = persistent_blocks(fn, 256, 0);
-  if (want < blocks) blocks = want;
-  if (blocks < 1) blocks = 1;
-  adamw_v8_kernel<LOWP, LW><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, m, v, g, lowp, head, nvec, n, s,
-                                                                          clip);
+  adamw_v8_kernel<LOWP, LW><<<one_pass_blocks(nvec, 256), 256, 0, st>>>(p, m, v, g, lowp, head, nvec, n, s, clip);
   return check_launch("adamw_v8_kernel");
 }
 
@@ -135,10 +129,7 @@ static zero_status launch_lowp(float* p, float* m, float* v, const float* g, voi
                          reinterpret_cast<uintptr_t>(v) % 32 == a && reinterpret_cast<uintptr_t>(g) % 32 == a &&
                          (LOWP == 0 || reinterpret_cast<uintptr_t>(lowp) % 2 == 0);
   if (!coaligned) {
-    const void* fn = reinterpret_cast<const void*>(&adamw_scalar_kernel<LOWP>);
-    int64_t want = (n + 255) / 256, blocks = persistent_blocks(fn, 256, 0);
-    if (want < blocks) blocks = want;
-    adamw_scalar_kernel<LOWP><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, m, v, g, lowp, n, s, clip);
+    adamw_scalar_kernel<LOWP><<<one_pass_blocks(n, 256), 256, 0, st>>>(p, m, v, g, lowp, n, s, clip);
     return check_launch("adamw_scalar_kernel");
   }
   int64_t head = static_cast<int64_t>((32 - a) % 32) / 4;

@@ -4,8 +4,6 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
-#include <mutex>
-#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -26,36 +24,6 @@ zero_status check_launch(const char* what) {
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ZERO_ECUDA, "%s: %s", what, cudaGetErrorString(e));
   return ZERO_OK;
-}
-
-namespace {
-struct GridEntry {
-  int device;
-  const void* kernel;
-  int threads;
-  size_t smem;
-  int blocks;
-};
-std::mutex g_grid_mu;
-std::vector<GridEntry> g_grid;
-}  // namespace
-
-int persistent_blocks(const void* kernel, int threads, size_t smem) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  {
-    std::lock_guard<std::mutex> lk(g_grid_mu);
-    for (const GridEntry& e : g_grid)
-      if (e.device == dev && e.kernel == kernel && e.threads == threads && e.smem == smem) return e.blocks;
-  }
-  int sms = 0, per_sm = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
-    per_sm = 1;
-  const int blocks = sms * per_sm;
-  std::lock_guard<std::mutex> lk(g_grid_mu);
-  g_grid.push_back({dev, kernel, threads, smem, blocks});
-  return blocks;
 }
 
 static bool valid_dtype(int d) { return d == ZERO_F32 || d == ZERO_BF16 || d == ZERO_F16; }

@@ -11,9 +11,8 @@
 // small ones with microsecond launch costs each).
 //
 // Work split: the shard's destination range is cut into tiles of 8192
-// elements; a persistent grid gives each block a contiguous run of tiles, so
-// one binary search over the table per block finds the first tensor and the
-// block then walks forward.  A tile that lies inside one tensor whose source
+// elements, one block per tile (one pass); each block finds its first tensor
+// by a binary search over the table (L1/L2-resident) and walks forward.  A tile that lies inside one tensor whose source
 // address is co-aligned with the destination is copied directly with 16- or
 // 32-byte loads and 32-byte stores.  Any other tile (tensor boundaries inside
 // it, a NULL grad, source and destination misaligned relative to each other)
@@ -200,11 +199,8 @@ static zero_status launch_flatten_t(const zero_tensor* table, int32_t n_tensors,
                                     float* dst, int32_t* flag, cudaStream_t st) {
   const int64_t len = e - s;
   const int64_t ntiles = (len + kFlTile - 1) / kFlTile;
-  const void* fn = reinterpret_cast<const void*>(&flatten_kernel<DT, ACC>);
-  int64_t blocks = persistent_blocks(fn, kFlThreads, 0);
-  if (ntiles < blocks) blocks = ntiles;
-  flatten_kernel<DT, ACC><<<static_cast<unsigned>(blocks), kFlThreads, 0, st>>>(
-      table, n_tensors, s, len, ntiles, dst, aligned(dst, 32), scale, flag);
+  flatten_kernel<DT, ACC><<<one_pass_blocks(ntiles, 1), kFlThreads, 0, st>>>(table, n_tensors, s, len, ntiles, dst,
+                                                                             aligned(dst, 32), scale, flag);
   return check_launch("flatten_kernel");
 }
 
@@ -281,18 +277,11 @@ static zero_status launch_accum_t(float* acc, const void* src, int64_t n, float 
   const bool vec = head >= 0 && reinterpret_cast<uintptr_t>(src) % es == 0 &&
                    (reinterpret_cast<uintptr_t>(src) + es * static_cast<uintptr_t>(head)) % vb == 0;
   if (!vec) {
-    const void* fn = reinterpret_cast<const void*>(&accum_scalar_kernel<DT, ACC>);
-    int64_t want = (n + 255) / 256, blocks = persistent_blocks(fn, 256, 0);
-    if (want < blocks) blocks = want;
-    accum_scalar_kernel<DT, ACC><<<static_cast<unsigned>(blocks), 256, 0, st>>>(acc, src, n, scale, flag);
+    accum_scalar_kernel<DT, ACC><<<one_pass_blocks(n, 256), 256, 0, st>>>(acc, src, n, scale, flag);
     return check_launch("accum_scalar_kernel");
   }
   const int64_t nvec = (n - head) / 8;
-  const void* fn = reinterpret_cast<const void*>(&accum_kernel<DT, ACC>);
-  int64_t want = (nvec + 255) / 256, blocks = persistent_blocks(fn, 256, 0);
-  if (want < blocks) blocks = want;
-  if (blocks < 1) blocks = 1;
-  accum_kernel<DT, ACC><<<static_cast<unsigned>(blocks), 256, 0, st>>>(acc, src, head, nvec, n, scale, flag);
+  accum_kernel<DT, ACC><<<one_pass_blocks(nvec, 256), 256, 0, st>>>(acc, src, head, nvec, n, scale, flag);
   return check_launch("accum_kernel");
 }
 

@@ -11,9 +11,9 @@
 //     exactly into x*x = p + e with one fma, p is added to hi with an
 //     error-free TwoSum, and the two error terms go into lo.  The 256 thread
 //     sums are added in binary64 by a fixed shuffle/shared-memory tree and the
-//     tile's binary64 partial is stored.  A persistent grid strides over the
-//     tiles, so the partial of a tile does not depend on which block computed
-//     it or how many blocks ran.
+//     tile's binary64 partial is stored.  One block per tile (the grid loop
+//     only covers grids beyond the hardware limit), so the partial of a tile
+//     does not depend on which block computed it or how many blocks ran.
 //  2. sqnorm_finalize_kernel: one block adds the partials in a fixed order
 //     (binary64), adds the other ranks' share, takes the square root and the
 //     clip coefficient, and writes the zero_norm_result.
@@ -139,11 +139,7 @@ zero_status launch_sqnorm(const float* g, int64_t n, double extra_sqnorm, double
                           zero_norm_result* out, cudaStream_t st) {
   const int64_t ntiles = (n + kSqTile - 1) / kSqTile;
   if (ntiles > 0) {
-    const void* fn = reinterpret_cast<const void*>(&sqnorm_tiles_kernel);
-    int64_t blocks = persistent_blocks(fn, kSqThreads, 0);
-    if (ntiles < blocks) blocks = ntiles;
-    sqnorm_tiles_kernel<<<static_cast<unsigned>(blocks), kSqThreads, 0, st>>>(g, n, ntiles, aligned(g, 32),
-                                                                             partials);
+    sqnorm_tiles_kernel<<<one_pass_blocks(ntiles, 1), kSqThreads, 0, st>>>(g, n, ntiles, aligned(g, 32), partials);
     zero_status s = check_launch("sqnorm_tiles_kernel");
     if (s != ZERO_OK) return s;
   }

@@ -18,9 +18,8 @@
  *
  * Conventions for every call:
  *  - Memory.  The library allocates nothing (device or host) and keeps no
- *    state between calls beyond a per-device cache of launch sizes (and the
- *    fixed scratch array of zero_grad_sqnorm_noalloc).  The caller owns
- *    every buffer.  Pointers prefixed d_ are device addresses;
+ *    state between calls (beyond the fixed scratch array of
+ *    zero_grad_sqnorm_noalloc).  The caller owns every buffer.  Pointers prefixed d_ are device addresses;
  *    everything else is host memory.
  *  - Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *    default stream).  Device work is enqueued asynchronously on it; no call
