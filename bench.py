@@ -1,8 +1,9 @@
 """Benchmark of the flat-shard optimizer step on the Llama-7B-shaped flat buffer.
 
 One step = the whole hot path over one batch of synthetic grads:
-  flatten/cast of the 291 bf16 per-tensor grads into the fp32 flat grad (K1)
-  -> deterministic grad norm + clip coefficient (K3, two launches)
+  flatten/cast of the 291 bf16 per-tensor grads into the fp32 flat grad, the
+  same pass computing the grad norm's tile partials (K1 with the fused norm)
+  -> norm finalize + clip coefficient (K3b)
   -> fused AdamW on fp32 master/exp_avg/exp_avg_sq with the bf16 write-back (K4)
   -> device->host read of the step's grad norm (the skip-policy decision).
 Inputs are resident in HBM (135 GB, far larger than the 129 MB L2, so no
@@ -38,7 +39,6 @@ METRIC = "fused AdamW shard step: params/s and HBM GB/s as % of GB300 peak (Llam
 UNIT = "params/s"
 ADAMW_BYTES_PER_PARAM = 30      # read g,p,m,v fp32; write p,m,v fp32 + bf16 copy
 FLATTEN_BYTES_PER_PARAM = 6     # read bf16 grad, write fp32 flat grad
-SQNORM_BYTES_PER_PARAM = 4      # read fp32 flat grad
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "adamw_llama7b_traffic.txt")
 
 
@@ -232,10 +232,10 @@ def run_gpu(args):
         if ev is not None:
             ev[0].record(stream)
         zs.zero_flatten_cast(d_table, len(grads), opt.total, torch.bfloat16, 0, n, 1.0, False, opt.grad, None,
-                             stream)
+                             opt.ws, stream)
         if ev is not None:
             ev[1].record(stream)
-        zs.zero_grad_sqnorm(opt.grad, 0.0, opt.max_norm, opt.ws, opt.norm_buf, stream)
+        zs.zero_grad_sqnorm_finalize(opt.ws, n, 0.0, opt.max_norm, opt.norm_buf, stream)
         if ev is not None:
             ev[2].record(stream)
         zs.zero_adamw_step(opt.master, opt.exp_avg, opt.exp_avg_sq, opt.grad, opt.lowp, opt.lr, opt.betas[0],
@@ -310,11 +310,12 @@ def run_gpu(args):
                      "unit": "GB/s", "frac": achieved / hbm, "peak_source": peak_src,
                      "traffic": None if tpp is None else tpp * n,
                      "algorithmic_bytes_per_launch": ADAMW_BYTES_PER_PARAM * n},
-        "kernels_ms": {"flatten": statistics.mean(k1), "grad_norm": statistics.mean(k3), "adamw": statistics.mean(k4)},
-        "kernels_gbs": {"flatten": FLATTEN_BYTES_PER_PARAM * n / (statistics.mean(k1) / 1e3) / 1e9,
-                        "grad_norm": SQNORM_BYTES_PER_PARAM * n / (statistics.mean(k3) / 1e3) / 1e9,
+        "kernels_ms": {"flatten_norm": statistics.mean(k1), "norm_finalize": statistics.mean(k3),
+                       "adamw": statistics.mean(k4)},
+        "kernels_gbs": {"flatten_norm": FLATTEN_BYTES_PER_PARAM * n / (statistics.mean(k1) / 1e3) / 1e9,
                         "adamw": achieved},
-        "gpu_launches": 4 * args.steps,
+        "bytes_per_param_step": FLATTEN_BYTES_PER_PARAM + ADAMW_BYTES_PER_PARAM,
+        "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
         "e2e": {"value": n * world * args.steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": grad_bytes,
                 "d2h_bytes_per_step": zs.NORM_RESULT_BYTES, "ms_per_step": e2e_ms / args.steps},

@@ -84,9 +84,20 @@ zero_status zero_tensor_table(const void* const* ptrs, const int64_t* numels, in
   return ZERO_OK;
 }
 
+// Optional fused-norm workspace of the flatten / accumulate calls: NULL, or
+// room for one binary64 partial per 32768 output elements, 8-byte aligned.
+static zero_status check_norm_ws(const char* who, const void* ws, size_t ws_bytes, int64_t n) {
+  if (ws == nullptr) return ZERO_OK;
+  const size_t need = zero_grad_sqnorm_workspace_bytes(n);
+  if (ws_bytes < need) return fail(ZERO_EINVAL, "%s: norm workspace %zu bytes < %zu needed", who, ws_bytes, need);
+  if (!zs::aligned(ws, 8)) return fail(ZERO_EINVAL, "%s: norm workspace not 8-byte aligned", who);
+  return ZERO_OK;
+}
+
 zero_status zero_flatten_cast(const zero_tensor* d_table, int32_t n_tensors, int64_t total, zero_dtype src_dtype,
                               int64_t shard_start, int64_t shard_end, float scale, int32_t accumulate,
-                              float* d_dst, int32_t* d_found_nonfinite, void* stream) {
+                              float* d_dst, int32_t* d_found_nonfinite, void* d_norm_ws, size_t norm_ws_bytes,
+                              void* stream) {
   if (n_tensors < 0) return fail(ZERO_EINVAL, "zero_flatten_cast: n_tensors %d < 0", n_tensors);
   if (n_tensors > 0 && d_table == nullptr) return fail(ZERO_EINVAL, "zero_flatten_cast: NULL d_table");
   if (total < 0 || (n_tensors == 0 && total != 0))
@@ -98,20 +109,26 @@ zero_status zero_flatten_cast(const zero_tensor* d_table, int32_t n_tensors, int
   if (accumulate != 0 && accumulate != 1) return fail(ZERO_EINVAL, "zero_flatten_cast: accumulate must be 0 or 1");
   if (!std::isfinite(scale)) return fail(ZERO_EINVAL, "zero_flatten_cast: non-finite scale");
   if (shard_end > shard_start && d_dst == nullptr) return fail(ZERO_EINVAL, "zero_flatten_cast: NULL d_dst");
+  const zero_status w = check_norm_ws("zero_flatten_cast", d_norm_ws, norm_ws_bytes, shard_end - shard_start);
+  if (w != ZERO_OK) return w;
   if (shard_end == shard_start) return ZERO_OK;
   return zs::launch_flatten(d_table, n_tensors, src_dtype, shard_start, shard_end, scale, accumulate, d_dst,
-                            d_found_nonfinite, zs::as_stream(stream));
+                            d_found_nonfinite, static_cast<double*>(d_norm_ws), zs::as_stream(stream));
 }
 
 zero_status zero_accum(float* d_acc, const void* d_src, zero_dtype src_dtype, int64_t n, float scale,
-                       int32_t accumulate, int32_t* d_found_nonfinite, void* stream) {
+                       int32_t accumulate, int32_t* d_found_nonfinite, void* d_norm_ws, size_t norm_ws_bytes,
+                       void* stream) {
   if (n < 0) return fail(ZERO_EINVAL, "zero_accum: n %lld < 0", (long long)n);
   if (!zs::valid_dtype(src_dtype)) return fail(ZERO_EINVAL, "zero_accum: bad src_dtype %d", (int)src_dtype);
   if (accumulate != 0 && accumulate != 1) return fail(ZERO_EINVAL, "zero_accum: accumulate must be 0 or 1");
   if (!std::isfinite(scale)) return fail(ZERO_EINVAL, "zero_accum: non-finite scale");
   if (n > 0 && (d_acc == nullptr || d_src == nullptr)) return fail(ZERO_EINVAL, "zero_accum: NULL buffer");
+  const zero_status w = check_norm_ws("zero_accum", d_norm_ws, norm_ws_bytes, n);
+  if (w != ZERO_OK) return w;
   if (n == 0) return ZERO_OK;
-  return zs::launch_accum(d_acc, d_src, src_dtype, n, scale, accumulate, d_found_nonfinite, zs::as_stream(stream));
+  return zs::launch_accum(d_acc, d_src, src_dtype, n, scale, accumulate, d_found_nonfinite,
+                          static_cast<double*>(d_norm_ws), zs::as_stream(stream));
 }
 
 size_t zero_grad_sqnorm_workspace_bytes(int64_t n) {
@@ -133,6 +150,19 @@ zero_status zero_grad_sqnorm(const float* d_grad, int64_t n, double extra_sqnorm
   if (need > 0 && !zs::aligned(d_ws, 8)) return fail(ZERO_EINVAL, "zero_grad_sqnorm: workspace not 8-byte aligned");
   return zs::launch_sqnorm(d_grad, n, extra_sqnorm, max_norm, static_cast<double*>(d_ws), d_out,
                            zs::as_stream(stream));
+}
+
+zero_status zero_grad_sqnorm_finalize(const void* d_ws, int64_t n, double extra_sqnorm, double max_norm,
+                                      zero_norm_result* d_out, void* stream) {
+  if (n < 0) return fail(ZERO_EINVAL, "zero_grad_sqnorm_finalize: n %lld < 0", (long long)n);
+  if (d_out == nullptr) return fail(ZERO_EINVAL, "zero_grad_sqnorm_finalize: NULL d_out");
+  if (n > 0 && d_ws == nullptr) return fail(ZERO_EINVAL, "zero_grad_sqnorm_finalize: NULL d_ws");
+  if (n > 0 && !zs::aligned(d_ws, 8)) return fail(ZERO_EINVAL, "zero_grad_sqnorm_finalize: d_ws not 8-byte aligned");
+  if (std::isnan(max_norm) || max_norm < 0.0) return fail(ZERO_EINVAL, "zero_grad_sqnorm_finalize: bad max_norm");
+  if (!std::isfinite(extra_sqnorm) || extra_sqnorm < 0.0)
+    return fail(ZERO_EINVAL, "zero_grad_sqnorm_finalize: bad extra_sqnorm");
+  return zs::launch_sqnorm_finalize(static_cast<const double*>(d_ws), n, extra_sqnorm, max_norm, d_out,
+                                    zs::as_stream(stream));
 }
 
 zero_status zero_adamw_step(float* d_master, float* d_exp_avg, float* d_exp_avg_sq, const float* d_grad,

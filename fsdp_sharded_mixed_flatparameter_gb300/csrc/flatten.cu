@@ -21,8 +21,15 @@
 // writes the destination with loads/stores aligned to the DESTINATION.  The
 // staging buffer is padded by one word per 8 (index q -> q + q/8) so that
 // both phases are free of shared-memory bank conflicts.
+//
+// Fused grad norm (NORM = true, used on the last micro-batch): a block then
+// owns four consecutive tiles = one 32768-element norm tile and adds the
+// squares of the values it writes in the order of the norm tile contract
+// (reduce.cuh), so its partial equals bit for bit what the separate norm
+// kernel would compute from the written buffer -- without reading it again.
 #include "common.cuh"
 #include "kernels.h"
+#include "reduce.cuh"
 
 namespace zs {
 
@@ -106,114 +113,145 @@ __device__ __forceinline__ void stage_segment(const void* __restrict__ src, int6
   }
 }
 
-template <int DT, bool ACC>
+template <int DT, bool ACC, bool NORM>
 __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* __restrict__ table, int n_tensors,
                                                              int64_t shard_start, int64_t len, int64_t ntiles,
                                                              float* __restrict__ dst, bool dst_vec, float scale,
-                                                             int32_t* __restrict__ flag) {
+                                                             int32_t* __restrict__ flag,
+                                                             double* __restrict__ partials) {
   __shared__ float stage[kFlStage];
+  __shared__ double red[kFlThreads / 32];
   constexpr int es = SrcTraits<DT>::esize;
   constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
-  const int64_t t0 = ntiles * blockIdx.x / gridDim.x;
-  const int64_t t1 = ntiles * (blockIdx.x + 1) / gridDim.x;
+  constexpr int kPerBlock = NORM ? static_cast<int>(kSqTile / kFlTile) : 1;  // tiles per block
+  static_assert(!NORM || kFlThreads == kSqThreads, "norm tile contract");
+  const int64_t nblocks_work = (ntiles + kPerBlock - 1) / kPerBlock;
   bool bad = false;
-  int ti = (t0 < t1) ? find_tensor(table, n_tensors, shard_start + t0 * kFlTile) : 0;
 
-  for (int64_t tile = t0; tile < t1; ++tile) {
-    const int64_t lo = tile * kFlTile;
-    const int tlen = static_cast<int>((len - lo < kFlTile) ? (len - lo) : kFlTile);
-    const int64_t klo = shard_start + lo, khi = klo + tlen;
-    while (ti + 1 < n_tensors && __ldg(&table[ti + 1].flat_offset) <= klo) ++ti;
-    const void* tptr = table[ti].ptr;
-    const int64_t toff = __ldg(&table[ti].flat_offset), tnum = __ldg(&table[ti].numel);
-    const char* tsrc = static_cast<const char*>(tptr) + es * (klo - toff);
+  for (int64_t wb = blockIdx.x; wb < nblocks_work; wb += gridDim.x) {
+    const int64_t t0 = wb * kPerBlock;
+    const int64_t t1 = (t0 + kPerBlock < ntiles) ? t0 + kPerBlock : ntiles;
+    int ti = find_tensor(table, n_tensors, shard_start + t0 * kFlTile);
+    float hi = 0.0f, lo = 0.0f;  // this thread's share of the norm tile
 
-    const bool direct = tlen == kFlTile && dst_vec && tptr != nullptr && toff <= klo && khi <= toff + tnum &&
-                        reinterpret_cast<uintptr_t>(tsrc) % vb == 0;
-    if (direct) {
-      // 1024 groups of 8; each thread takes 4, all loads first
-      float x[4][8];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) load8_src<DT>(tsrc + es * 8 * (threadIdx.x + r * kFlThreads), x[r]);
-      float a[4][8];
-      if (ACC) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) ld8_rw(dst + lo + 8 * (threadIdx.x + r * kFlThreads), a[r]);
-      }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float y = __fmul_rn(scale, x[r][i]);
-          bad |= !finite_f(y);
-          x[r][i] = ACC ? __fadd_rn(a[r][i], y) : y;
-        }
-        st8(dst + lo + 8 * (threadIdx.x + r * kFlThreads), x[r]);
-      }
-      continue;
-    }
+    for (int64_t tile = t0; tile < t1; ++tile) {
+      const int64_t base = tile * kFlTile;
+      const int tlen = static_cast<int>((len - base < kFlTile) ? (len - base) : kFlTile);
+      const int64_t klo = shard_start + base, khi = klo + tlen;
+      while (ti + 1 < n_tensors && __ldg(&table[ti + 1].flat_offset) <= klo) ++ti;
+      const void* tptr = table[ti].ptr;
+      const int64_t toff = __ldg(&table[ti].flat_offset), tnum = __ldg(&table[ti].numel);
+      const char* tsrc = static_cast<const char*>(tptr) + es * (klo - toff);
 
-    // staged tile: walk the tensors that overlap [klo, khi)
-    int64_t k = klo;
-    int j = ti;
-    while (k < khi && j < n_tensors) {
-      const int64_t off = __ldg(&table[j].flat_offset), num = __ldg(&table[j].numel);
-      const int64_t seg_end = (off + num < khi) ? off + num : khi;
-      if (seg_end > k)
-        stage_segment<DT>(table[j].ptr, k - off, static_cast<int>(seg_end - k), static_cast<int>(k - klo), scale,
-                          stage, bad);
-      if (seg_end > k) k = seg_end;
-      ++j;
-    }
-    // a table that ends before `total` leaves the rest as zeros
-    for (int q = static_cast<int>(k - klo) + threadIdx.x; q < tlen; q += kFlThreads) stage[stage_idx(q)] = 0.0f;
-    __syncthreads();
-    const int ngroups = (tlen + 7) / 8;
-    for (int u = threadIdx.x; u < ngroups; u += kFlThreads) {
-      float y[8];
-      const int64_t d = lo + 8 * u;
-      if (dst_vec && 8 * u + 8 <= tlen) {
+      const bool direct = tlen == kFlTile && dst_vec && tptr != nullptr && toff <= klo && khi <= toff + tnum &&
+                          reinterpret_cast<uintptr_t>(tsrc) % vb == 0;
+      if (direct) {
+        // 1024 groups of 8; thread t takes groups t + 256 r, r = 0..3, all loads first
+        float x[4][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) y[i] = stage[stage_idx(8 * u + i)];
+        for (int r = 0; r < 4; ++r) load8_src<DT>(tsrc + es * 8 * (threadIdx.x + r * kFlThreads), x[r]);
+        float a[4][8];
         if (ACC) {
-          float a[8];
-          ld8_rw(dst + d, a);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) y[i] = __fadd_rn(a[i], y[i]);
+          for (int r = 0; r < 4; ++r) ld8_rw(dst + base + 8 * (threadIdx.x + r * kFlThreads), a[r]);
         }
-        st8(dst + d, y);
-      } else {
-        for (int i = 0; i < 8 && 8 * u + i < tlen; ++i) {
-          const float yi = stage[stage_idx(8 * u + i)];
-          dst[d + i] = ACC ? __fadd_rn(dst[d + i], yi) : yi;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float y = __fmul_rn(scale, x[r][i]);
+            bad |= !finite_f(y);
+            x[r][i] = ACC ? __fadd_rn(a[r][i], y) : y;
+            if (NORM) df_add_square(hi, lo, x[r][i]);
+          }
+          st8(dst + base + 8 * (threadIdx.x + r * kFlThreads), x[r]);
+        }
+        continue;
+      }
+
+      // staged tile: walk the tensors that overlap [klo, khi)
+      int64_t k = klo;
+      int j = ti;
+      while (k < khi && j < n_tensors) {
+        const int64_t off = __ldg(&table[j].flat_offset), num = __ldg(&table[j].numel);
+        const int64_t seg_end = (off + num < khi) ? off + num : khi;
+        if (seg_end > k)
+          stage_segment<DT>(table[j].ptr, k - off, static_cast<int>(seg_end - k), static_cast<int>(k - klo), scale,
+                            stage, bad);
+        if (seg_end > k) k = seg_end;
+        ++j;
+      }
+      // a table that ends before `total` leaves the rest as zeros
+      for (int q = static_cast<int>(k - klo) + threadIdx.x; q < tlen; q += kFlThreads) stage[stage_idx(q)] = 0.0f;
+      __syncthreads();
+      const int ngroups = (tlen + 7) / 8;
+      for (int u = threadIdx.x; u < ngroups; u += kFlThreads) {
+        float y[8];
+        const int64_t d = base + 8 * u;
+        if (dst_vec && 8 * u + 8 <= tlen) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) y[i] = stage[stage_idx(8 * u + i)];
+          if (ACC) {
+            float a[8];
+            ld8_rw(dst + d, a);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = __fadd_rn(a[i], y[i]);
+          }
+          if (NORM) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) df_add_square(hi, lo, y[i]);
+          }
+          st8(dst + d, y);
+        } else {
+          for (int i = 0; i < 8 && 8 * u + i < tlen; ++i) {
+            const float si = stage[stage_idx(8 * u + i)];
+            const float yi = ACC ? __fadd_rn(dst[d + i], si) : si;
+            if (NORM) df_add_square(hi, lo, yi);
+            dst[d + i] = yi;
+          }
         }
       }
+      __syncthreads();
     }
-    __syncthreads();
+    if (NORM) {
+      const double bs = block_sum<kFlThreads>(static_cast<double>(hi) + static_cast<double>(lo), red);
+      if (threadIdx.x == 0) partials[wb] = bs;
+    }
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
 }
 
-template <int DT, bool ACC>
+template <int DT, bool ACC, bool NORM>
 static zero_status launch_flatten_t(const zero_tensor* table, int32_t n_tensors, int64_t s, int64_t e, float scale,
-                                    float* dst, int32_t* flag, cudaStream_t st) {
+                                    float* dst, int32_t* flag, double* partials, cudaStream_t st) {
   const int64_t len = e - s;
   const int64_t ntiles = (len + kFlTile - 1) / kFlTile;
-  flatten_kernel<DT, ACC><<<one_pass_blocks(ntiles, 1), kFlThreads, 0, st>>>(table, n_tensors, s, len, ntiles, dst,
-                                                                             aligned(dst, 32), scale, flag);
+  const int64_t per = NORM ? kSqTile / kFlTile : 1;
+  flatten_kernel<DT, ACC, NORM><<<one_pass_blocks(ntiles, per), kFlThreads, 0, st>>>(
+      table, n_tensors, s, len, ntiles, dst, aligned(dst, 32), scale, flag, partials);
   return check_launch("flatten_kernel");
 }
 
+template <int DT, bool ACC>
+static zero_status launch_flatten_n(const zero_tensor* table, int32_t n_tensors, int64_t s, int64_t e, float scale,
+                                    float* dst, int32_t* flag, double* partials, cudaStream_t st) {
+  if (partials != nullptr)
+    return launch_flatten_t<DT, ACC, true>(table, n_tensors, s, e, scale, dst, flag, partials, st);
+  return launch_flatten_t<DT, ACC, false>(table, n_tensors, s, e, scale, dst, flag, nullptr, st);
+}
+
 zero_status launch_flatten(const zero_tensor* table, int32_t n_tensors, int src_dtype, int64_t s, int64_t e,
-                           float scale, int accumulate, float* dst, int32_t* flag, cudaStream_t st) {
+                           float scale, int accumulate, float* dst, int32_t* flag, double* partials,
+                           cudaStream_t st) {
   if (e <= s) return ZERO_OK;
   switch (src_dtype * 2 + (accumulate ? 1 : 0)) {
-    case ZERO_F32 * 2: return launch_flatten_t<ZERO_F32, false>(table, n_tensors, s, e, scale, dst, flag, st);
-    case ZERO_F32 * 2 + 1: return launch_flatten_t<ZERO_F32, true>(table, n_tensors, s, e, scale, dst, flag, st);
-    case ZERO_BF16 * 2: return launch_flatten_t<ZERO_BF16, false>(table, n_tensors, s, e, scale, dst, flag, st);
-    case ZERO_BF16 * 2 + 1: return launch_flatten_t<ZERO_BF16, true>(table, n_tensors, s, e, scale, dst, flag, st);
-    case ZERO_F16 * 2: return launch_flatten_t<ZERO_F16, false>(table, n_tensors, s, e, scale, dst, flag, st);
-    default: return launch_flatten_t<ZERO_F16, true>(table, n_tensors, s, e, scale, dst, flag, st);
+    case ZERO_F32 * 2: return launch_flatten_n<ZERO_F32, false>(table, n_tensors, s, e, scale, dst, flag, partials, st);
+    case ZERO_F32 * 2 + 1: return launch_flatten_n<ZERO_F32, true>(table, n_tensors, s, e, scale, dst, flag, partials, st);
+    case ZERO_BF16 * 2: return launch_flatten_n<ZERO_BF16, false>(table, n_tensors, s, e, scale, dst, flag, partials, st);
+    case ZERO_BF16 * 2 + 1:
+      return launch_flatten_n<ZERO_BF16, true>(table, n_tensors, s, e, scale, dst, flag, partials, st);
+    case ZERO_F16 * 2: return launch_flatten_n<ZERO_F16, false>(table, n_tensors, s, e, scale, dst, flag, partials, st);
+    default: return launch_flatten_n<ZERO_F16, true>(table, n_tensors, s, e, scale, dst, flag, partials, st);
   }
 }
 
@@ -266,6 +304,65 @@ __global__ void __launch_bounds__(256) accum_scalar_kernel(float* __restrict__ a
   if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
 }
 
+// K2 with the fused grad norm: one block per 32768-element norm tile, thread
+// t handles groups r * 256 + t (r = 0..15) of the tile, four at a time with
+// their loads first, and adds the squares of the values it writes in the
+// norm tile contract's order.  `vec`: acc is 32-byte aligned and src is
+// aligned for its 8-element vector; otherwise every element goes scalar.
+template <int DT, bool ACC>
+__global__ void __launch_bounds__(kSqThreads) accum_norm_kernel(float* __restrict__ acc, const void* __restrict__ src,
+                                                                int64_t n, int64_t ntiles, bool vec, float scale,
+                                                                int32_t* __restrict__ flag,
+                                                                double* __restrict__ partials) {
+  __shared__ double red[kSqThreads / 32];
+  constexpr int es = SrcTraits<DT>::esize;
+  const char* s8 = static_cast<const char*>(src);
+  bool bad = false;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    float hi = 0.0f, lo = 0.0f;
+    const int64_t base = tile * kSqTile;
+#pragma unroll 1
+    for (int r0 = 0; r0 < kSqVecPerThread; r0 += 4) {
+      float x[4][8], a[4][8];
+      bool full[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t k = base + (static_cast<int64_t>(r0 + q) * kSqThreads + threadIdx.x) * 8;
+        full[q] = vec && k + 8 <= n;
+        if (full[q]) {
+          load8_src<DT>(s8 + es * k, x[q]);
+          if (ACC) ld8_rw(acc + k, a[q]);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t k = base + (static_cast<int64_t>(r0 + q) * kSqThreads + threadIdx.x) * 8;
+        if (full[q]) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float y = __fmul_rn(scale, x[q][i]);
+            bad |= !finite_f(y);
+            x[q][i] = ACC ? __fadd_rn(a[q][i], y) : y;
+            df_add_square(hi, lo, x[q][i]);
+          }
+          st8(acc + k, x[q]);
+        } else {
+          for (int i = 0; i < 8 && k + i < n; ++i) {
+            const float y = __fmul_rn(scale, load_elem<DT>(src, k + i));
+            bad |= !finite_f(y);
+            const float o = ACC ? __fadd_rn(acc[k + i], y) : y;
+            df_add_square(hi, lo, o);
+            acc[k + i] = o;
+          }
+        }
+      }
+    }
+    const double bs = block_sum<kSqThreads>(static_cast<double>(hi) + static_cast<double>(lo), red);
+    if (threadIdx.x == 0) partials[tile] = bs;
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
+}
+
 template <int DT, bool ACC>
 static zero_status launch_accum_t(float* acc, const void* src, int64_t n, float scale, int32_t* flag,
                                   cudaStream_t st) {
@@ -285,16 +382,28 @@ static zero_status launch_accum_t(float* acc, const void* src, int64_t n, float 
   return check_launch("accum_kernel");
 }
 
+template <int DT, bool ACC>
+static zero_status launch_accum_n(float* acc, const void* src, int64_t n, float scale, int32_t* flag,
+                                  double* partials, cudaStream_t st) {
+  if (partials == nullptr) return launch_accum_t<DT, ACC>(acc, src, n, scale, flag, st);
+  constexpr uintptr_t vb = (DT == ZERO_F32) ? 32 : 16;
+  const bool vec = aligned(acc, 32) && aligned(src, vb);
+  const int64_t ntiles = (n + kSqTile - 1) / kSqTile;
+  accum_norm_kernel<DT, ACC><<<one_pass_blocks(ntiles, 1), kSqThreads, 0, st>>>(acc, src, n, ntiles, vec, scale, flag,
+                                                                               partials);
+  return check_launch("accum_norm_kernel");
+}
+
 zero_status launch_accum(float* acc, const void* src, int src_dtype, int64_t n, float scale, int accumulate,
-                         int32_t* flag, cudaStream_t st) {
+                         int32_t* flag, double* partials, cudaStream_t st) {
   if (n <= 0) return ZERO_OK;
   switch (src_dtype * 2 + (accumulate ? 1 : 0)) {
-    case ZERO_F32 * 2: return launch_accum_t<ZERO_F32, false>(acc, src, n, scale, flag, st);
-    case ZERO_F32 * 2 + 1: return launch_accum_t<ZERO_F32, true>(acc, src, n, scale, flag, st);
-    case ZERO_BF16 * 2: return launch_accum_t<ZERO_BF16, false>(acc, src, n, scale, flag, st);
-    case ZERO_BF16 * 2 + 1: return launch_accum_t<ZERO_BF16, true>(acc, src, n, scale, flag, st);
-    case ZERO_F16 * 2: return launch_accum_t<ZERO_F16, false>(acc, src, n, scale, flag, st);
-    default: return launch_accum_t<ZERO_F16, true>(acc, src, n, scale, flag, st);
+    case ZERO_F32 * 2: return launch_accum_n<ZERO_F32, false>(acc, src, n, scale, flag, partials, st);
+    case ZERO_F32 * 2 + 1: return launch_accum_n<ZERO_F32, true>(acc, src, n, scale, flag, partials, st);
+    case ZERO_BF16 * 2: return launch_accum_n<ZERO_BF16, false>(acc, src, n, scale, flag, partials, st);
+    case ZERO_BF16 * 2 + 1: return launch_accum_n<ZERO_BF16, true>(acc, src, n, scale, flag, partials, st);
+    case ZERO_F16 * 2: return launch_accum_n<ZERO_F16, false>(acc, src, n, scale, flag, partials, st);
+    default: return launch_accum_n<ZERO_F16, true>(acc, src, n, scale, flag, partials, st);
   }
 }
 

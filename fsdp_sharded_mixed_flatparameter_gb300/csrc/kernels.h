@@ -27,14 +27,20 @@ constexpr int64_t kSqTile = 32768;
 zero_status launch_adamw(float* p, float* m, float* v, const float* g, void* lowp, int lowp_dtype, int64_t n,
                          const AdamScalars& s, const zero_norm_result* clip, cudaStream_t st);
 
+// `partials` (nullable): also write the norm tiles' partial sums of squares
+// of the values written (one binary64 per 32768 elements of dst / acc).
 zero_status launch_flatten(const zero_tensor* table, int32_t n_tensors, int src_dtype, int64_t shard_start,
                            int64_t shard_end, float scale, int accumulate, float* dst, int32_t* flag,
-                           cudaStream_t st);
+                           double* partials, cudaStream_t st);
 
 zero_status launch_accum(float* acc, const void* src, int src_dtype, int64_t n, float scale, int accumulate,
-                         int32_t* flag, cudaStream_t st);
+                         int32_t* flag, double* partials, cudaStream_t st);
 
 zero_status launch_sqnorm(const float* g, int64_t n, double extra_sqnorm, double max_norm, double* partials,
                           zero_norm_result* out, cudaStream_t st);
+
+// Norm result from already computed tile partials (ceil(n / kSqTile) of them).
+zero_status launch_sqnorm_finalize(const double* partials, int64_t n, double extra_sqnorm, double max_norm,
+                                   zero_norm_result* out, cudaStream_t st);
 
 }  // namespace zs

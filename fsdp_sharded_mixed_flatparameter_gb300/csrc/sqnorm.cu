@@ -36,40 +36,10 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "reduce.cuh"
 
 namespace zs {
 
-constexpr int kSqThreads = 256;
-constexpr int kSqVecPerThread = 16;  // 16 x 8 = 128 elements per thread per tile
-static_assert(kSqThreads * kSqVecPerThread * 8 == kSqTile, "tile size");
-
-// hi + lo += x*x, error-free except for the rounding of lo itself
-__device__ __forceinline__ void df_add_square(float& hi, float& lo, float x) {
-  const float p = __fmul_rn(x, x);
-  const float e = __fmaf_rn(x, x, -p);  // x*x == p + e exactly
-  const float s = __fadd_rn(hi, p);     // TwoSum(hi, p) = s + t exactly
-  const float bp = __fsub_rn(s, hi);
-  const float t = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
-  hi = s;
-  lo = __fadd_rn(lo, __fadd_rn(t, e));
-}
-
-// Block-wide binary64 sum in a fixed order; the result is valid in thread 0.
-template <int THREADS>
-__device__ __forceinline__ double block_sum(double x, double* red) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x += __shfl_down_sync(0xffffffffu, x, off);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = x;
-  __syncthreads();
-  double r = 0.0;
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int w = 0; w < THREADS / 32; ++w) r += red[w];
-  }
-  __syncthreads();  // red[] may be reused by the caller's next round
-  return r;
-}
 
 // Element e of a tile belongs to thread t, vector slot r, lane i where
 // e = ((r * 256) + t) * 8 + i: each 32-byte load of a warp covers 1 KiB.
@@ -133,6 +103,13 @@ __global__ void __launch_bounds__(kFinThreads) sqnorm_finalize_kernel(const doub
     r.finite = isfinite(norm) ? 1 : 0;
     *out = r;
   }
+}
+
+zero_status launch_sqnorm_finalize(const double* partials, int64_t n, double extra_sqnorm, double max_norm,
+                                   zero_norm_result* out, cudaStream_t st) {
+  const int64_t ntiles = (n + kSqTile - 1) / kSqTile;
+  sqnorm_finalize_kernel<<<1, kFinThreads, 0, st>>>(partials, ntiles, extra_sqnorm, max_norm, out);
+  return check_launch("sqnorm_finalize_kernel");
 }
 
 zero_status launch_sqnorm(const float* g, int64_t n, double extra_sqnorm, double max_norm, double* partials,

@@ -64,6 +64,7 @@ class FlatShardAdamW:
         self.norm_buf = zs.new_norm_result(dev)
         self.found_nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
         self.t = 0
+        self._norm_ready = False  # the grad norm's tile partials are up to date in self.ws
         self._tables: Dict[tuple, Tuple[torch.Tensor, int]] = {}
 
     # ---------------------------------------------------------------- grads
@@ -85,18 +86,26 @@ class FlatShardAdamW:
         return hit[0]
 
     def flatten(self, grads: Sequence[Optional[torch.Tensor]], *, accumulate: bool, scale: float = 1.0,
-                stream=None) -> None:
-        """Flatten/cast per-tensor grads into the rank's flat fp32 grad (K1)."""
+                fuse_norm: bool = False, stream=None) -> None:
+        """Flatten/cast per-tensor grads into the rank's flat fp32 grad (K1).
+
+        fuse_norm: this is the last micro-batch; the same pass also computes the
+        grad norm's tile partials, so step() only has to finalize them.
+        """
         dts = {g.dtype for g in grads if g is not None}
         if len(dts) > 1:
             raise ValueError("all grads must share one dtype")
         dt = dts.pop() if dts else torch.float32
         zs.zero_flatten_cast(self._table(grads), len(grads), self.total, dt, self.glo, self.ghi, scale, accumulate,
-                             self.grad, self.found_nonfinite, stream)
+                             self.grad, self.found_nonfinite, self.ws if fuse_norm else None, stream)
+        self._norm_ready = fuse_norm
 
-    def accum(self, flat_src: torch.Tensor, *, accumulate: bool, scale: float = 1.0, stream=None) -> None:
-        """Accumulate a flat low-precision grad covering the grad range (K2)."""
-        zs.zero_accum(self.grad, flat_src, scale, accumulate, self.found_nonfinite, stream)
+    def accum(self, flat_src: torch.Tensor, *, accumulate: bool, scale: float = 1.0, fuse_norm: bool = False,
+              stream=None) -> None:
+        """Accumulate a flat low-precision grad covering the grad range (K2); fuse_norm as for flatten()."""
+        zs.zero_accum(self.grad, flat_src, scale, accumulate, self.found_nonfinite, self.ws if fuse_norm else None,
+                      stream)
+        self._norm_ready = fuse_norm
 
     # ----------------------------------------------------------------- step
     def shard_grad(self) -> torch.Tensor:
@@ -108,7 +117,12 @@ class FlatShardAdamW:
         When the norm turns out non-finite, K4 changes nothing on the device;
         finish_step() then leaves t unchanged.
         """
-        zs.zero_grad_sqnorm(self.grad, extra_sqnorm, self.max_norm, self.ws, self.norm_buf, stream)
+        if self._norm_ready:
+            zs.zero_grad_sqnorm_finalize(self.ws, self.grad.numel(), extra_sqnorm, self.max_norm, self.norm_buf,
+                                         stream)
+        else:
+            zs.zero_grad_sqnorm(self.grad, extra_sqnorm, self.max_norm, self.ws, self.norm_buf, stream)
+        self._norm_ready = False
         zs.zero_adamw_step(self.master, self.exp_avg, self.exp_avg_sq, self.shard_grad(), self.lowp, self.lr,
                            self.betas[0], self.betas[1], self.eps, self.weight_decay, self.t + 1, self.norm_buf,
                            stream)

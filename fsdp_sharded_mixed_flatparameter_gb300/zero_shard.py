@@ -66,8 +66,10 @@ def lib() -> ctypes.CDLL:
     i32, i64, f32, f64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double, ctypes.c_void_p
     L.zero_shard_range.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     L.zero_tensor_table.argtypes = [vp, vp, i32, vp, ctypes.POINTER(i64)]
-    L.zero_flatten_cast.argtypes = [vp, i32, i64, ctypes.c_int, i64, i64, f32, i32, vp, vp, vp]
-    L.zero_accum.argtypes = [vp, vp, ctypes.c_int, i64, f32, i32, vp, vp]
+    sz = ctypes.c_size_t
+    L.zero_flatten_cast.argtypes = [vp, i32, i64, ctypes.c_int, i64, i64, f32, i32, vp, vp, vp, sz, vp]
+    L.zero_accum.argtypes = [vp, vp, ctypes.c_int, i64, f32, i32, vp, vp, sz, vp]
+    L.zero_grad_sqnorm_finalize.argtypes = [vp, i64, f64, f64, vp, vp]
     L.zero_grad_sqnorm_workspace_bytes.argtypes = [i64]
     L.zero_grad_sqnorm_workspace_bytes.restype = ctypes.c_size_t
     L.zero_grad_sqnorm.argtypes = [vp, i64, f64, f64, vp, ctypes.c_size_t, vp, vp]
@@ -79,7 +81,7 @@ def lib() -> ctypes.CDLL:
     L.zero_last_error.argtypes = []
     L.zero_last_error.restype = ctypes.c_char_p
     for nm in ("zero_shard_range", "zero_tensor_table", "zero_flatten_cast", "zero_accum", "zero_grad_sqnorm",
-               "zero_grad_sqnorm_noalloc", "zero_adamw_step"):
+               "zero_grad_sqnorm_finalize", "zero_grad_sqnorm_noalloc", "zero_adamw_step"):
         getattr(L, nm).restype = ctypes.c_int
     _lib = L
     return L
@@ -153,9 +155,14 @@ def zero_grad_sqnorm_workspace_bytes(n: int) -> int:
 
 
 # --------------------------------------------------------------------- device
+def _ws_bytes(ws: Optional[torch.Tensor]) -> int:
+    return 0 if ws is None else ws.numel() * ws.element_size()
+
+
 def zero_flatten_cast(d_table: torch.Tensor, n_tensors: int, total: int, src_dtype: torch.dtype, shard_start: int,
                       shard_end: int, scale: float, accumulate: bool, dst: torch.Tensor,
-                      found_nonfinite: Optional[torch.Tensor] = None, stream=None) -> None:
+                      found_nonfinite: Optional[torch.Tensor] = None, norm_ws: Optional[torch.Tensor] = None,
+                      stream=None) -> None:
     if shard_end > shard_start and dst.numel() < shard_end - shard_start:
         raise ValueError("dst is smaller than the shard")
     tab = _dev(d_table, "d_table", torch.uint8, allow_none=n_tensors == 0)
@@ -164,16 +171,29 @@ def zero_flatten_cast(d_table: torch.Tensor, n_tensors: int, total: int, src_dty
     _check(lib().zero_flatten_cast(tab, n_tensors, total, _DT[src_dtype], shard_start, shard_end, scale,
                                    int(bool(accumulate)), _dev(dst, "dst", torch.float32),
                                    _dev(found_nonfinite, "found_nonfinite", torch.int32, allow_none=True),
-                                   _stream(stream)))
+                                   _dev(norm_ws, "norm_ws", allow_none=True), _ws_bytes(norm_ws), _stream(stream)))
 
 
 def zero_accum(acc: torch.Tensor, src: torch.Tensor, scale: float, accumulate: bool,
-               found_nonfinite: Optional[torch.Tensor] = None, stream=None) -> None:
+               found_nonfinite: Optional[torch.Tensor] = None, norm_ws: Optional[torch.Tensor] = None,
+               stream=None) -> None:
     if src.numel() != acc.numel():
         raise ValueError("acc and src differ in size")
     _check(lib().zero_accum(_dev(acc, "acc", torch.float32), _dev(src, "src"), _DT[src.dtype], acc.numel(), scale,
                             int(bool(accumulate)),
-                            _dev(found_nonfinite, "found_nonfinite", torch.int32, allow_none=True), _stream(stream)))
+                            _dev(found_nonfinite, "found_nonfinite", torch.int32, allow_none=True),
+                            _dev(norm_ws, "norm_ws", allow_none=True), _ws_bytes(norm_ws), _stream(stream)))
+
+
+def zero_grad_sqnorm_finalize(ws: Optional[torch.Tensor], n: int, extra_sqnorm: float, max_norm: float,
+                              out: torch.Tensor, stream=None) -> None:
+    """Norm result from the partials a fused flatten/accumulate pass wrote for an n-element grad."""
+    if out.numel() * out.element_size() < NORM_RESULT_BYTES:
+        raise ValueError("out is smaller than zero_norm_result")
+    if n > 0 and _ws_bytes(ws) < zero_grad_sqnorm_workspace_bytes(n):
+        raise ValueError("ws is smaller than the partials of n elements")
+    _check(lib().zero_grad_sqnorm_finalize(_dev(ws, "ws", allow_none=True), n, extra_sqnorm, max_norm,
+                                           _dev(out, "out"), _stream(stream)))
 
 
 def zero_grad_sqnorm(grad: torch.Tensor, extra_sqnorm: float, max_norm: float, ws: torch.Tensor,

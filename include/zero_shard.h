@@ -127,16 +127,25 @@ zero_status zero_tensor_table(const void* const* ptrs, const int64_t* numels, in
  * d_dst: fp32, shard_end - shard_start elements.
  * d_found_nonfinite: NULL, or a device int32 set to 1 when any
  *   fl(scale * x) is inf or NaN (never cleared by the call: zero it first).
+ * d_norm_ws: NULL, or a device workspace of at least
+ *   zero_grad_sqnorm_workspace_bytes(shard_end - shard_start) bytes
+ *   (8-byte aligned).  When given, the same pass also writes the grad
+ *   norm's per-tile partials of the values it writes to d_dst -- the very
+ *   partials zero_grad_sqnorm would compute from d_dst, bit for bit -- so
+ *   that zero_grad_sqnorm_finalize can produce the norm without reading the
+ *   grad again.  Pass it on the last micro-batch only.
  * Errors: ZERO_EINVAL for n_tensors < 0, d_table NULL with n_tensors > 0,
  * shard bounds outside 0 <= shard_start <= shard_end <= total, d_dst NULL
- * on a non-empty shard, a bad dtype, accumulate not 0/1, or a non-finite
- * scale.  The table's contents cannot be checked on the host: a table that
- * does not match `total` or points at too-small buffers is the caller's
- * error and reads out of bounds. */
+ * on a non-empty shard, a bad dtype, accumulate not 0/1, a non-finite
+ * scale, or a too-small / misaligned norm workspace.  The table's contents
+ * cannot be checked on the host: a table that does not match `total` or
+ * points at too-small buffers is the caller's error and reads out of
+ * bounds. */
 zero_status zero_flatten_cast(const zero_tensor* d_table, int32_t n_tensors, int64_t total,
                               zero_dtype src_dtype, int64_t shard_start, int64_t shard_end,
                               float scale, int32_t accumulate, float* d_dst,
-                              int32_t* d_found_nonfinite, void* stream);
+                              int32_t* d_found_nonfinite, void* d_norm_ws, size_t norm_ws_bytes,
+                              void* stream);
 
 /* zero_accum -- device.
  * Flat micro-batch accumulation and averaging (the ZeRO page's
@@ -146,11 +155,14 @@ zero_status zero_flatten_cast(const zero_tensor* d_table, int32_t n_tensors, int
  *   accumulate == 1:  d_acc[k] = fl(d_acc[k] + fl(scale * x[k]))
  * with x = d_src in src_dtype cast exactly to fp32.  This is the ZeRO-2/3
  * case, where the rank receives its shard's grads already flat.
- * d_found_nonfinite as for zero_flatten_cast.
+ * d_found_nonfinite and d_norm_ws (zero_grad_sqnorm_workspace_bytes(n))
+ * as for zero_flatten_cast.
  * Errors: ZERO_EINVAL for n < 0, NULL buffers with n > 0, a bad dtype,
- * accumulate not 0/1, or a non-finite scale. */
+ * accumulate not 0/1, a non-finite scale, or a too-small / misaligned norm
+ * workspace. */
 zero_status zero_accum(float* d_acc, const void* d_src, zero_dtype src_dtype, int64_t n, float scale,
-                       int32_t accumulate, int32_t* d_found_nonfinite, void* stream);
+                       int32_t accumulate, int32_t* d_found_nonfinite, void* d_norm_ws,
+                       size_t norm_ws_bytes, void* stream);
 
 /* zero_grad_sqnorm_workspace_bytes -- host only.
  * Device scratch that zero_grad_sqnorm needs for n elements: one binary64
@@ -181,6 +193,19 @@ size_t zero_grad_sqnorm_workspace_bytes(int64_t n);
  * negative or non-finite extra_sqnorm. */
 zero_status zero_grad_sqnorm(const float* d_grad, int64_t n, double extra_sqnorm, double max_norm,
                              void* d_ws, size_t ws_bytes, zero_norm_result* d_out, void* stream);
+
+/* zero_grad_sqnorm_finalize -- device.
+ * The second half of zero_grad_sqnorm: from the per-tile partials that a
+ * zero_flatten_cast / zero_accum call with a norm workspace wrote for an
+ * n-element grad buffer, add them in the fixed order, add extra_sqnorm and
+ * write the zero_norm_result (norm, clip coefficient, finite flag) exactly
+ * as zero_grad_sqnorm would for that buffer.  This fuses the grad-norm read
+ * into the last micro-batch's pass (4 bytes per parameter saved).
+ * Errors: ZERO_EINVAL for n < 0, d_out NULL, d_ws NULL or misaligned with
+ * n > 0, a negative or NaN max_norm, or a negative or non-finite
+ * extra_sqnorm. */
+zero_status zero_grad_sqnorm_finalize(const void* d_ws, int64_t n, double extra_sqnorm, double max_norm,
+                                      zero_norm_result* d_out, void* stream);
 
 /* zero_adamw_step -- device.
  * The ZeRO page's ZeRO1Optimizer.step Adam update (bias_correction1/2 with

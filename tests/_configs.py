@@ -71,7 +71,10 @@ def _host_parts(tg: W.TensorGrads, numels, offsets, a: int, b: int, nulls):
 
 
 def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk: int = 1 << 26,
-                 seed: int = 0) -> RunReport:
+                 seed: int = 0, fused: bool = True) -> RunReport:
+    """fused: the last micro-batch's flatten/accumulate also computes the grad
+    norm's partials (the norm is then only finalized); otherwise the norm is a
+    separate pass over the flat grad."""
     from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
 
     s, e = oracle.shard_range(wl.total, wl.world_size, wl.rank)
@@ -105,12 +108,12 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
             if wl.mode == "zero3":
                 src = W.flat_grads(wl, t, j, s, e, device=DEV, out=storages[j])
                 storages[j] = src
-                opt.accum(src, accumulate=j > 0, scale=scale)
+                opt.accum(src, accumulate=j > 0, scale=scale, fuse_norm=fused and j == M - 1)
                 micro.append(src)
             else:
                 tg = W.tensor_grads(wl, t, j, device=DEV, storage=storages[j])
                 storages[j] = tg.storage
-                opt.flatten(tg.tensors, accumulate=j > 0, scale=scale)
+                opt.flatten(tg.tensors, accumulate=j > 0, scale=scale, fuse_norm=fused and j == M - 1)
                 micro.append(tg)
         res = opt.step()
 

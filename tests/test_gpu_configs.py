@@ -39,7 +39,7 @@ def test_tiny_full():
 def test_tiny_short_tail_shard():
     """tiny list, 8 ranks, rank 7: the short last shard [1,104,159, 1,261,891)."""
     wl = W.tiny().with_(world_size=8, rank=7, max_norm=0.5)
-    rep = run_workload(wl, steps=3)
+    rep = run_workload(wl, steps=3, fused=False)
     assert rep.n == 157732
     _summary(rep)
 
@@ -65,7 +65,7 @@ def test_llama7b_full_size_sampled():
 
 def test_llama7b_shape_all_steps():
     wl = W.small_llama(layers=4, hidden=512, mlp=1376, vocab=3200)
-    rep = run_workload(wl, steps=W.llama7b().steps)
+    rep = run_workload(wl, steps=W.llama7b().steps, fused=False)
     _summary(rep)
 
 
@@ -79,7 +79,7 @@ def test_llama13b_zero3_rank7_full_size_sampled():
 
 def test_llama13b_zero3_shape_all_steps():
     wl = W.llama13b_zero3().with_(numels=tuple(W.llama_numels(5, 640, 1728, 4000)), max_norm=0.1)
-    rep = run_workload(wl, steps=W.llama13b_zero3().steps)
+    rep = run_workload(wl, steps=W.llama13b_zero3().steps, fused=False)
     assert all(s.ref_coef < 1.0 for s in rep.steps)
     _summary(rep)
 

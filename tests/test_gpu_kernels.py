@@ -310,3 +310,72 @@ def test_flatten_flags_nonfinite():
     assert flag.item() == 0  # the NaN lies outside the range
     zs.zero_flatten_cast(d_table, 3, total, torch.bfloat16, 0, total, 1.0, False, dst, flag)
     assert flag.item() == 1
+
+
+# ------------------------------------------------- fused norm (K1/K2 + finalize)
+def _norm_pair(zs, buf, n, extra=0.0, max_norm=1.0, fused_ws=None):
+    """Separate norm over `buf` and the finalize of `fused_ws`: (workspace, result) of each."""
+    ws_s = torch.zeros(max(zs.zero_grad_sqnorm_workspace_bytes(n), 8), dtype=torch.uint8, device=DEV)
+    out_s, out_f = zs.new_norm_result(DEV), zs.new_norm_result(DEV)
+    zs.zero_grad_sqnorm(buf, extra, max_norm, ws_s, out_s)
+    zs.zero_grad_sqnorm_finalize(fused_ws, n, extra, max_norm, out_f)
+    return ws_s, zs.decode_norm_result(out_s), zs.decode_norm_result(out_f)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_flatten_fused_norm_equals_separate_norm(dtype):
+    """The last micro-batch's flatten writes the same values and, bit for bit, the same
+    norm partials as a separate norm pass over what it wrote."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    for numels, offs in ((list(W.ragged_numels(300, seed=7, max_log2=14)), [0, 1, 3, 8, 5]),
+                         (list(W.llama_numels(2, 256, 688, 1000)), [0])):
+        host, dev = _table_case(numels, dtype, null=(2,), seed=11, elem_offsets=offs)
+        table, total = zs.zero_tensor_table(dev, numels)
+        d_table = zs.device_table(table, len(numels), DEV)
+        rawh = [raw(h) for h in host]
+        for world, rank in ((1, 0), (3, 1), (8, 7)):
+            s, e = oracle.shard_range(total, world, rank)
+            n = e - s
+            for dst_off in (0, 1):
+                D = Guarded(n, torch.float32, dst_off)
+                ws_f = torch.full((max(zs.zero_grad_sqnorm_workspace_bytes(n), 8),), 0xAB, dtype=torch.uint8,
+                                  device=DEV)
+                ref = np.zeros(n, np.float32)
+                zs.zero_flatten_cast(d_table, len(numels), total, W.torch_dtype(dtype), s, e, 0.5, False, D.t)
+                oracle.flatten(rawh, numels, dtype, s, e, 0.5, ref, accumulate=False)
+                zs.zero_flatten_cast(d_table, len(numels), total, W.torch_dtype(dtype), s, e, 0.5, True, D.t,
+                                     norm_ws=ws_f)
+                oracle.flatten(rawh, numels, dtype, s, e, 0.5, ref, accumulate=True)
+                torch.cuda.synchronize()
+                D.check_guards()
+                assert bits_equal_f32(raw(D.t), ref), (world, rank, dst_off)
+                nb = zs.zero_grad_sqnorm_workspace_bytes(n)
+                ws_s, r_s, r_f = _norm_pair(zs, D.t, n, fused_ws=ws_f)
+                assert torch.equal(ws_f[:nb], ws_s[:nb]), "fused partials differ from the separate norm"
+                assert r_f == r_s
+                cr = oracle.clip(oracle.sqnorm(ref), 0.0, 1.0)
+                assert abs(r_f.norm - cr.norm) <= 1e-12 * cr.norm
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("n", [1, 9, 32768, 32769, 262147, 1_000_003])
+def test_accum_fused_norm_equals_separate_norm(dtype, n):
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    tdt = W.torch_dtype(dtype)
+    for ao, so in ((0, 0), (3, 3), (0, 5)):
+        A = Guarded(n, torch.float32, ao)
+        ref = np.zeros(n, np.float32)
+        ws_f = torch.full((zs.zero_grad_sqnorm_workspace_bytes(n),), 0xCD, dtype=torch.uint8, device=DEV)
+        for j in range(3):
+            x = _rand(n, 70 * j + ao + so, 1e-2, tdt)
+            S = Guarded(n, tdt, so, x)
+            last = j == 2
+            zs.zero_accum(A.t, S.t, 0.125, accumulate=j > 0, norm_ws=ws_f if last else None)
+            oracle.accum(ref, raw(x), dtype, 0.125, accumulate=j > 0)
+        torch.cuda.synchronize()
+        A.check_guards()
+        assert bits_equal_f32(raw(A.t), ref), (ao, so)
+        ws_s, r_s, r_f = _norm_pair(zs, A.t, n, extra=0.5, max_norm=0.25, fused_ws=ws_f)
+        nb = zs.zero_grad_sqnorm_workspace_bytes(n)
+        assert torch.equal(ws_f[:nb], ws_s[:nb]), (ao, so)
+        assert r_f == r_s
