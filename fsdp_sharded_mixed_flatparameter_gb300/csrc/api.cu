@@ -165,6 +165,40 @@ zero_status zero_grad_sqnorm_finalize(const void* d_ws, int64_t n, double extra_
                                     zs::as_stream(stream));
 }
 
+zero_status zero_grad_sqnorm_combine(const double* d_sqnorms, int32_t n_parts, double max_norm,
+                                    zero_norm_result* d_out, void* stream) {
+  if (n_parts < 1) return fail(ZERO_EINVAL, "zero_grad_sqnorm_combine: n_parts %d < 1", n_parts);
+  if (d_sqnorms == nullptr || d_out == nullptr) return fail(ZERO_EINVAL, "zero_grad_sqnorm_combine: NULL pointer");
+  if (!zs::aligned(d_sqnorms, 8)) return fail(ZERO_EINVAL, "zero_grad_sqnorm_combine: d_sqnorms not 8-byte aligned");
+  if (std::isnan(max_norm) || max_norm < 0.0) return fail(ZERO_EINVAL, "zero_grad_sqnorm_combine: bad max_norm");
+  return zs::launch_sqnorm_combine(d_sqnorms, n_parts, max_norm, d_out, zs::as_stream(stream));
+}
+
+zero_status zero_loss_scale_update(float* scale, int32_t* growth_tracker, int32_t found_inf, double growth_factor,
+                                   double backoff_factor, int32_t growth_interval) {
+  if (scale == nullptr || growth_tracker == nullptr)
+    return fail(ZERO_EINVAL, "zero_loss_scale_update: NULL scale or growth_tracker");
+  if (!(growth_factor > 1.0) || !std::isfinite(growth_factor))
+    return fail(ZERO_EINVAL, "zero_loss_scale_update: growth_factor must be > 1 and finite");
+  if (!(backoff_factor > 0.0 && backoff_factor < 1.0))
+    return fail(ZERO_EINVAL, "zero_loss_scale_update: backoff_factor must be in (0, 1)");
+  if (growth_interval < 1) return fail(ZERO_EINVAL, "zero_loss_scale_update: growth_interval < 1");
+  if (found_inf) {
+    *scale = static_cast<float>(static_cast<double>(*scale) * backoff_factor);
+    *growth_tracker = 0;
+    return ZERO_OK;
+  }
+  const int32_t good = *growth_tracker + 1;
+  if (good >= growth_interval) {
+    const float grown = static_cast<float>(static_cast<double>(*scale) * growth_factor);
+    if (std::isfinite(grown)) *scale = grown;
+    *growth_tracker = 0;
+  } else {
+    *growth_tracker = good;
+  }
+  return ZERO_OK;
+}
+
 zero_status zero_adamw_step(float* d_master, float* d_exp_avg, float* d_exp_avg_sq, const float* d_grad,
                             void* d_param_lowp, zero_dtype lowp_dtype, int64_t n, const zero_adamw_hparams* hp,
                             int64_t step, const zero_norm_result* d_clip, void* stream) {

@@ -43,4 +43,8 @@ zero_status launch_sqnorm(const float* g, int64_t n, double extra_sqnorm, double
 zero_status launch_sqnorm_finalize(const double* partials, int64_t n, double extra_sqnorm, double max_norm,
                                    zero_norm_result* out, cudaStream_t st);
 
+// Global norm from a device vector of per-rank sums of squares (rank order).
+zero_status launch_sqnorm_combine(const double* sq, int n_parts, double max_norm, zero_norm_result* out,
+                                  cudaStream_t st);
+
 }  // namespace zs

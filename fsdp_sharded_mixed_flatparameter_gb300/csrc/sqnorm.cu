@@ -105,6 +105,30 @@ __global__ void __launch_bounds__(kFinThreads) sqnorm_finalize_kernel(const doub
   }
 }
 
+// Global norm from the ranks' local sums of squares, added in rank order by
+// one thread so that every rank derives the same binary64 total and the same
+// binary32 coefficient from the same gathered vector.
+__global__ void sqnorm_combine_kernel(const double* __restrict__ sq, int n_parts, double max_norm,
+                                      zero_norm_result* __restrict__ out) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  double total = 0.0;
+  for (int i = 0; i < n_parts; ++i) total = __dadd_rn(total, sq[i]);
+  const double norm = __dsqrt_rn(total);
+  const double q = __ddiv_rn(max_norm, __dadd_rn(norm, 1e-6));
+  zero_norm_result r;
+  r.sqnorm = total;
+  r.norm = norm;
+  r.clip_coef = (q < 1.0) ? __double2float_rn(q) : 1.0f;
+  r.finite = isfinite(norm) ? 1 : 0;
+  *out = r;
+}
+
+zero_status launch_sqnorm_combine(const double* sq, int n_parts, double max_norm, zero_norm_result* out,
+                                  cudaStream_t st) {
+  sqnorm_combine_kernel<<<1, 32, 0, st>>>(sq, n_parts, max_norm, out);
+  return check_launch("sqnorm_combine_kernel");
+}
+
 zero_status launch_sqnorm_finalize(const double* partials, int64_t n, double extra_sqnorm, double max_norm,
                                    zero_norm_result* out, cudaStream_t st) {
   const int64_t ntiles = (n + kSqTile - 1) / kSqTile;

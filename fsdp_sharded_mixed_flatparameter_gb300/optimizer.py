@@ -65,6 +65,7 @@ class FlatShardAdamW:
         self.found_nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
         self.t = 0
         self._norm_ready = False  # the grad norm's tile partials are up to date in self.ws
+        self._local_buf: Optional[torch.Tensor] = None
         self._tables: Dict[tuple, Tuple[torch.Tensor, int]] = {}
 
     # ---------------------------------------------------------------- grads
@@ -111,18 +112,35 @@ class FlatShardAdamW:
     def shard_grad(self) -> torch.Tensor:
         return self.grad[self.start - self.glo:self.end - self.glo]
 
-    def launch_step(self, extra_sqnorm: float = 0.0, stream=None) -> None:
-        """Enqueue grad norm (K3) and the AdamW step (K4) for t+1 without waiting.
-
-        When the norm turns out non-finite, K4 changes nothing on the device;
-        finish_step() then leaves t unchanged.
-        """
+    def _norm_into(self, out: torch.Tensor, extra_sqnorm: float, max_norm: float, stream) -> None:
         if self._norm_ready:
-            zs.zero_grad_sqnorm_finalize(self.ws, self.grad.numel(), extra_sqnorm, self.max_norm, self.norm_buf,
-                                         stream)
+            zs.zero_grad_sqnorm_finalize(self.ws, self.grad.numel(), extra_sqnorm, max_norm, out, stream)
         else:
-            zs.zero_grad_sqnorm(self.grad, extra_sqnorm, self.max_norm, self.ws, self.norm_buf, stream)
+            zs.zero_grad_sqnorm(self.grad, extra_sqnorm, max_norm, self.ws, out, stream)
         self._norm_ready = False
+
+    def local_sqnorm(self, stream=None) -> torch.Tensor:
+        """Enqueue this rank's sum of squares over its grad buffer; returns it as a
+        1-element float64 device tensor (the value the ranks exchange)."""
+        if self._local_buf is None:
+            self._local_buf = zs.new_norm_result(self.device)
+        self._norm_into(self._local_buf, 0.0, math.inf, stream)
+        return zs.sqnorm_view(self._local_buf)
+
+    def launch_step(self, extra_sqnorm: float = 0.0, stream=None,
+                    gathered_sqnorms: Optional[torch.Tensor] = None) -> None:
+        """Enqueue the grad norm and the AdamW step (K4) for t+1 without waiting.
+
+        gathered_sqnorms: the ranks' local sums of squares in rank order (float64,
+        on this device) for a global norm across ranks; otherwise the norm covers
+        this rank's grad buffer plus `extra_sqnorm`.  When the norm turns out
+        non-finite, K4 changes nothing on the device; finish_step() then leaves t
+        unchanged.
+        """
+        if gathered_sqnorms is not None:
+            zs.zero_grad_sqnorm_combine(gathered_sqnorms, self.max_norm, self.norm_buf, stream)
+        else:
+            self._norm_into(self.norm_buf, extra_sqnorm, self.max_norm, stream)
         zs.zero_adamw_step(self.master, self.exp_avg, self.exp_avg_sq, self.shard_grad(), self.lowp, self.lr,
                            self.betas[0], self.betas[1], self.eps, self.weight_decay, self.t + 1, self.norm_buf,
                            stream)
@@ -134,8 +152,17 @@ class FlatShardAdamW:
             self.t += 1
         return r
 
-    def step(self, extra_sqnorm: float = 0.0, stream=None) -> zs.NormResult:
-        self.launch_step(extra_sqnorm, stream)
+    def step(self, extra_sqnorm: float = 0.0, stream=None, process_group=None) -> zs.NormResult:
+        """One optimizer step.  With a torch.distributed process group of more than
+        one rank and a shard-only grad buffer (ZeRO-2/3), the clip norm is global:
+        the ranks exchange their 8-byte local sums of squares (all-gather, rank
+        order) and every rank combines the same vector, so all ranks use the same
+        coefficient and agree on skipping a non-finite step."""
+        if process_group is not None and self.glo == self.start and _world(process_group) > 1:
+            local = self.local_sqnorm(stream)
+            self.launch_step(stream=stream, gathered_sqnorms=gather_sqnorms(local, process_group))
+        else:
+            self.launch_step(extra_sqnorm, stream)
         return self.finish_step()
 
     def resident_bytes(self) -> int:
@@ -144,3 +171,19 @@ class FlatShardAdamW:
         if self.lowp is not None:
             b += self.lowp.numel() * self.lowp.element_size()
         return b
+
+
+def _world(group) -> int:
+    import torch.distributed as dist
+    return dist.get_world_size(group)
+
+
+def gather_sqnorms(local: torch.Tensor, group) -> torch.Tensor:
+    """All-gather every rank's 1-element float64 sum of squares, in rank order.
+
+    The only data exchanged by the step (8 bytes per rank).  Works with NCCL on
+    device tensors and with gloo on host tensors."""
+    import torch.distributed as dist
+    parts = [torch.empty_like(local) for _ in range(dist.get_world_size(group))]
+    dist.all_gather(parts, local.contiguous(), group=group)
+    return torch.cat(parts)

@@ -70,18 +70,21 @@ def lib() -> ctypes.CDLL:
     L.zero_flatten_cast.argtypes = [vp, i32, i64, ctypes.c_int, i64, i64, f32, i32, vp, vp, vp, sz, vp]
     L.zero_accum.argtypes = [vp, vp, ctypes.c_int, i64, f32, i32, vp, vp, sz, vp]
     L.zero_grad_sqnorm_finalize.argtypes = [vp, i64, f64, f64, vp, vp]
+    L.zero_grad_sqnorm_combine.argtypes = [vp, i32, f64, vp, vp]
     L.zero_grad_sqnorm_workspace_bytes.argtypes = [i64]
     L.zero_grad_sqnorm_workspace_bytes.restype = ctypes.c_size_t
     L.zero_grad_sqnorm.argtypes = [vp, i64, f64, f64, vp, ctypes.c_size_t, vp, vp]
     L.zero_grad_sqnorm_noalloc.argtypes = [vp, i64, f64, f64, vp, vp]
     L.zero_adamw_step.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, i64, ctypes.POINTER(zero_adamw_hparams), i64,
                                   vp, vp]
+    L.zero_loss_scale_update.argtypes = [ctypes.POINTER(f32), ctypes.POINTER(i32), i32, f64, f64, i32]
     L.zero_status_string.argtypes = [ctypes.c_int]
     L.zero_status_string.restype = ctypes.c_char_p
     L.zero_last_error.argtypes = []
     L.zero_last_error.restype = ctypes.c_char_p
     for nm in ("zero_shard_range", "zero_tensor_table", "zero_flatten_cast", "zero_accum", "zero_grad_sqnorm",
-               "zero_grad_sqnorm_finalize", "zero_grad_sqnorm_noalloc", "zero_adamw_step"):
+               "zero_grad_sqnorm_finalize", "zero_grad_sqnorm_combine", "zero_grad_sqnorm_noalloc",
+               "zero_adamw_step", "zero_loss_scale_update"):
         getattr(L, nm).restype = ctypes.c_int
     _lib = L
     return L
@@ -107,6 +110,23 @@ def _dev(t: Optional[torch.Tensor], name: str, dtype=None, allow_none: bool = Fa
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _grad_ptr(t: torch.Tensor, name: str) -> int:
+    """Address of a grad for the tensor table: a contiguous CUDA tensor, or a
+    contiguous PINNED host tensor.  Pinned host memory is mapped into the
+    device's unified address space at the same address, so the flatten
+    kernel reads it directly over the host link (the host-to-device transfer
+    and the flatten/cast become one pass).  Pageable host memory is refused."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.is_cuda:
+        return t.data_ptr()
+    if t.device.type == "cpu" and t.is_pinned():
+        return t.data_ptr()
+    raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -125,6 +145,7 @@ def zero_shard_range(total: int, world_size: int, rank: int) -> Tuple[int, int]:
 def zero_tensor_table(grads: Sequence[Optional[torch.Tensor]] = None, numels: Sequence[int] = None):
     """Host FlatParameter table for `grads` (None = no grad) or bare `numels`.
 
+    Grads are CUDA tensors or pinned host tensors (read over the host link).
     Returns (table, total) where table is a ctypes array of zero_tensor.
     """
     if numels is None:
@@ -133,10 +154,7 @@ def zero_tensor_table(grads: Sequence[Optional[torch.Tensor]] = None, numels: Se
     nm = np.ascontiguousarray(np.asarray(numels, dtype=np.int64))
     ptrs = None
     if grads is not None:
-        for i, g in enumerate(grads):
-            if g is not None:
-                _dev(g, f"grads[{i}]")
-        ptrs = (ctypes.c_void_p * n)(*[None if g is None else g.data_ptr() for g in grads])
+        ptrs = (ctypes.c_void_p * n)(*[None if g is None else _grad_ptr(g, f"grads[{i}]") for i, g in enumerate(grads)])
     table = (zero_tensor * max(n, 1))()
     total = ctypes.c_int64()
     _check(lib().zero_tensor_table(ptrs, ctypes.c_void_p(nm.ctypes.data), n, table, ctypes.byref(total)))
@@ -214,6 +232,19 @@ def zero_grad_sqnorm_noalloc(grad: torch.Tensor, extra_sqnorm: float, max_norm: 
                                           _dev(out, "out"), _stream(stream)))
 
 
+def zero_grad_sqnorm_combine(sqnorms: torch.Tensor, max_norm: float, out: torch.Tensor, stream=None) -> None:
+    """Global norm result from the ranks' local sums of squares (float64 CUDA vector, rank order)."""
+    if out.numel() * out.element_size() < NORM_RESULT_BYTES:
+        raise ValueError("out is smaller than zero_norm_result")
+    _check(lib().zero_grad_sqnorm_combine(_dev(sqnorms, "sqnorms", torch.float64), sqnorms.numel(), max_norm,
+                                          _dev(out, "out"), _stream(stream)))
+
+
+def sqnorm_view(result: torch.Tensor) -> torch.Tensor:
+    """The `sqnorm` field of a device zero_norm_result buffer as a 1-element float64 tensor view."""
+    return result[:8].view(torch.float64)
+
+
 def zero_adamw_step(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg_sq: torch.Tensor, grad: torch.Tensor,
                     param_lowp: Optional[torch.Tensor], lr: float, beta1: float, beta2: float, eps: float,
                     weight_decay: float, step: int, clip: Optional[torch.Tensor] = None, stream=None) -> None:
@@ -255,3 +286,35 @@ def decode_norm_result(buf: torch.Tensor) -> NormResult:
     raw = bytes(buf.detach().cpu().numpy().tobytes()[:NORM_RESULT_BYTES])
     r = zero_norm_result.from_buffer_copy(raw)
     return NormResult(r.sqnorm, r.norm, r.clip_coef, bool(r.finite))
+
+
+# ------------------------------------------------------------ loss scaling
+class DynamicLossScale:
+    """GradScaler-style dynamic loss scale (host policy: zero_loss_scale_update).
+
+    Multiply the loss by ``scale`` before backward; pass ``unscale_factor(accum_steps)``
+    as the flatten / accumulate ``scale`` (the unscale and the 1/accum_steps
+    averaging in one exact multiply for power-of-two values); after the step call
+    ``update(found_inf)`` with the kernels' non-finite flag.
+    """
+
+    def __init__(self, init_scale: float = 2.0 ** 16, growth_factor: float = 2.0, backoff_factor: float = 0.5,
+                 growth_interval: int = 2000):
+        self._scale = ctypes.c_float(init_scale)
+        self._good = ctypes.c_int32(0)
+        self.growth_factor, self.backoff_factor, self.growth_interval = growth_factor, backoff_factor, growth_interval
+
+    @property
+    def scale(self) -> float:
+        return self._scale.value
+
+    @property
+    def growth_tracker(self) -> int:
+        return self._good.value
+
+    def unscale_factor(self, accum_steps: int = 1) -> float:
+        return 1.0 / (float(self._scale.value) * accum_steps)
+
+    def update(self, found_inf: bool) -> None:
+        _check(lib().zero_loss_scale_update(ctypes.byref(self._scale), ctypes.byref(self._good), int(bool(found_inf)),
+                                            self.growth_factor, self.backoff_factor, self.growth_interval))

@@ -64,7 +64,9 @@ typedef enum zero_dtype {
  * the parameter has no grad; it reads as zeros (the ZeRO page's
  * _flatten_gradients fills such a tensor with torch.zeros). */
 typedef struct zero_tensor {
-  const void* ptr;     /* device address of element 0, contiguous */
+  const void* ptr;     /* address of element 0, contiguous: device memory, or pinned
+                          host memory (mapped at the same address; the kernel then
+                          reads it over the host link, fusing the transfer) */
   int64_t numel;       /* number of elements, >= 0 */
   int64_t flat_offset; /* start of this tensor in the flat buffer */
 } zero_tensor;
@@ -207,6 +209,21 @@ zero_status zero_grad_sqnorm(const float* d_grad, int64_t n, double extra_sqnorm
 zero_status zero_grad_sqnorm_finalize(const void* d_ws, int64_t n, double extra_sqnorm, double max_norm,
                                       zero_norm_result* d_out, void* stream);
 
+/* zero_grad_sqnorm_combine -- device.
+ * The global norm of clip_grad_norm_ across data-parallel ranks (ZeRO-2/3:
+ * each rank holds only its shard's grads).  d_sqnorms[r] is rank r's local
+ * sum of squares (the `sqnorm` field of its zero_grad_sqnorm /
+ * zero_grad_sqnorm_finalize result with extra_sqnorm = 0), gathered in rank
+ * order -- the one exchange of the step, 8 bytes per rank.  The values are
+ * added in index order in binary64, so every rank that combines the same
+ * gathered vector gets the same norm and the same binary32 coefficient
+ * (a tree all-reduce would not promise that).  Writes d_out like
+ * zero_grad_sqnorm.
+ * Errors: ZERO_EINVAL for n_parts < 1, NULL or misaligned pointers, or a
+ * negative or NaN max_norm. */
+zero_status zero_grad_sqnorm_combine(const double* d_sqnorms, int32_t n_parts, double max_norm,
+                                     zero_norm_result* d_out, void* stream);
+
 /* zero_adamw_step -- device.
  * The ZeRO page's ZeRO1Optimizer.step Adam update (bias_correction1/2 with
  * the step counter incremented before use; denom = sqrt(exp_avg_sq) /
@@ -267,6 +284,26 @@ zero_status zero_adamw_step(float* d_master, float* d_exp_avg, float* d_exp_avg_
  * above, and ZERO_ECUDA if the address lookup fails. */
 zero_status zero_grad_sqnorm_noalloc(const float* d_grad, int64_t n, double extra_sqnorm,
                                      double max_norm, zero_norm_result* d_out, void* stream);
+
+/* zero_loss_scale_update -- host only.
+ * Dynamic loss scaling of mixed-precision training, as the ZeRO page's
+ * Llama-7B recipe (section "组合策略：ZeRO-3 + 梯度累积 + 混合精度") configures
+ * torch.cuda.amp.GradScaler(init_scale=2^16, growth_factor=2.0,
+ * backoff_factor=0.5, growth_interval=2000) and skips the step on overflow.
+ * After a step whose grads overflowed (found_inf != 0, e.g. the
+ * d_found_nonfinite flag of zero_flatten_cast / zero_accum):
+ * *scale *= backoff_factor and the count of good steps restarts at 0.
+ * Otherwise the count grows; when it reaches growth_interval the scale is
+ * multiplied by growth_factor (kept only if still finite) and the count
+ * restarts.  Products are taken in binary64 and rounded to binary32.
+ * The unscale itself is folded into the flatten / accumulate `scale`
+ * argument: scale = 1 / (loss_scale * accum_steps), exact for the
+ * power-of-two values used in practice.
+ * Errors: ZERO_EINVAL for NULL pointers, growth_factor <= 1 or not finite,
+ * backoff_factor outside (0, 1), growth_interval < 1. */
+zero_status zero_loss_scale_update(float* scale, int32_t* growth_tracker, int32_t found_inf,
+                                   double growth_factor, double backoff_factor,
+                                   int32_t growth_interval);
 
 /* Static text for a status code. */
 const char* zero_status_string(zero_status status);

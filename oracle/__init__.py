@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
             for nm in ("orc_bf16_rne_array", "orc_f16_rne_array"):
                 getattr(L, nm).argtypes = [vp, vp, i64]
             L.orc_to_f32_array.argtypes = [vp, ctypes.c_int, vp, i64]
+            L.orc_loss_scale_update.argtypes = [ctypes.POINTER(f32), ctypes.POINTER(i32), i32, f64, f64, i32]
             _lib = L
     return _lib
 
@@ -186,6 +187,16 @@ def to_f32(x: np.ndarray, dtype: str) -> np.ndarray:
     y = np.empty(x.shape, dtype=np.float32)
     lib().orc_to_f32_array(_p(x), DTYPE_CODE[dtype], _p(y), x.size)
     return y
+
+
+def loss_scale_trajectory(found_infs, init_scale=2.0 ** 16, growth=2.0, backoff=0.5, interval=2000):
+    """Scale after each step of a GradScaler-style dynamic loss scale."""
+    sc, good = ctypes.c_float(init_scale), ctypes.c_int32(0)
+    out = []
+    for f in found_infs:
+        lib().orc_loss_scale_update(ctypes.byref(sc), ctypes.byref(good), int(bool(f)), growth, backoff, interval)
+        out.append(sc.value)
+    return out
 
 
 # ---------------------------------------------------------------- one step

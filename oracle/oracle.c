@@ -291,3 +291,25 @@ void orc_f16_rne_array(const float* x, uint16_t* y, int64_t n) {
 void orc_to_f32_array(const void* x, int dtype, float* y, int64_t n) {
   for (int64_t k = 0; k < n; ++k) y[k] = orc_load(x, dtype, k);
 }
+
+/* ----------------------------------------------------- dynamic loss scale */
+
+/* [ZeRO-NPU] section "组合策略": torch.cuda.amp.GradScaler(init_scale=2^16,
+ * growth_interval=2000, backoff_factor=0.5, growth_factor=2.0); after a step
+ * with overflowed grads the scale backs off and the good-step count
+ * restarts, and after growth_interval good steps in a row the scale grows
+ * (kept only if it stays finite).  Products in binary64, rounded to binary32. */
+void orc_loss_scale_update(float* scale, int32_t* good_steps, int32_t found_inf, double growth,
+                           double backoff, int32_t interval) {
+  if (found_inf) {
+    *scale = (float)((double)*scale * backoff);
+    *good_steps = 0;
+    return;
+  }
+  *good_steps += 1;
+  if (*good_steps >= interval) {
+    float g = (float)((double)*scale * growth);
+    if (isfinite(g)) *scale = g;
+    *good_steps = 0;
+  }
+}

@@ -160,5 +160,24 @@ def test_binding_refuses_host_tensors(L):
     cpu = torch.zeros(16)
     with pytest.raises(ValueError):
         zs.zero_adamw_step(cpu, cpu, cpu, cpu, None, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1)
+    with pytest.raises(ValueError):  # pageable host grads never reach the table
+        zs.zero_tensor_table([cpu], [16])
     with pytest.raises(ValueError):
         zs.zero_accum(cpu, cpu, 1.0, False)
+
+
+def test_loss_scale_update_matches_oracle(L):
+    """The library's host policy against the oracle's, including growth capped at float max."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    rng = np.random.default_rng(3)
+    for interval, init in ((1, 2.0 ** 16), (4, 2.0 ** 16), (7, 2.0 ** 120), (2000, 1.0)):
+        found = [bool(x) for x in rng.random(500) < 0.2]
+        sc = zs.DynamicLossScale(init, 2.0, 0.5, interval)
+        got = []
+        for f in found:
+            sc.update(f)
+            got.append(sc.scale)
+        assert got == oracle.loss_scale_trajectory(found, init, 2.0, 0.5, interval)
+    bad = zs.DynamicLossScale(2.0, 1.0, 0.5, 10)
+    with pytest.raises(zs.ZeroError):
+        bad.update(False)

@@ -1,0 +1,71 @@
+"""Mixed precision with dynamic loss scaling on the GPU vs the oracle.
+
+fp16 shard grads of a scaled loss (S * g, S = 2^16 at start) accumulate over
+4 micro-batches with the unscale folded into the accumulate scale
+1/(S * 4); an overflow injected in one micro-batch of step 3 must raise the
+non-finite flag, skip the step on both sides (state and t untouched) and back
+the scale off; the scale then grows again after `growth_interval` good steps.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from _helpers import bits_equal_f32, raw
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from fsdp_sharded_mixed_flatparameter_gb300 import build, zero_shard
+    build.build()
+    zero_shard.lib()
+
+
+def test_loss_scaled_fp16_accumulation_with_overflow_skip():
+    from fsdp_sharded_mixed_flatparameter_gb300 import DynamicLossScale, FlatShardAdamW
+    wl = W.llama13b_zero3().with_(numels=tuple(W.llama_numels(2, 256, 688, 1000)), max_norm=0.05)
+    s, e = oracle.shard_range(wl.total, wl.world_size, wl.rank)
+    n, M, interval = e - s, 4, 2
+    master = W.master_init(wl, s, e)
+    opt = FlatShardAdamW(wl.numels, world_size=wl.world_size, rank=wl.rank, lr=wl.lr, betas=wl.betas, eps=wl.eps,
+                         weight_decay=wl.weight_decay, max_norm=wl.max_norm, device=DEV, master=master.to(DEV))
+    scaler = DynamicLossScale(2.0 ** 16, 2.0, 0.5, interval)
+    st = oracle.new_state(master.numpy())
+    ref_scales, found_hist = [], []
+    ref_scale = 2.0 ** 16
+    for t in range(1, 8):
+        S = ref_scale  # the oracle side's scale decides the inputs
+        assert scaler.scale == S
+        unscale = 1.0 / (S * M)
+        acc = np.zeros(n, np.float32)
+        ref_flag = False
+        for j in range(M):
+            g = W.flat_grads(wl.with_(grad_dtype="f32", grad_std=1e-5), t, j, s, e)
+            x = (g * S).to(torch.float16)
+            if t == 3 and j == 2:
+                x[n // 3] = math.inf  # overflow in one micro-batch
+            opt.accum(x.to(DEV), accumulate=j > 0, scale=unscale, fuse_norm=j == M - 1)
+            ref_flag |= oracle.accum(acc, raw(x), "f16", unscale, accumulate=j > 0)
+        res = opt.step()
+        found = bool(opt.found_nonfinite.item())
+        opt.found_nonfinite.zero_()
+        scaler.update(found or not res.finite)
+        cr = oracle.step_reference(st, acc, lr=wl.lr, betas=wl.betas, eps=wl.eps, wd=wl.weight_decay,
+                                   max_norm=wl.max_norm)
+        assert found == ref_flag == (t == 3)
+        assert res.finite == cr.finite == (t != 3)
+        found_hist.append(ref_flag or not cr.finite)
+        ref_scale = oracle.loss_scale_trajectory(found_hist, 2.0 ** 16, 2.0, 0.5, interval)[-1]
+        assert scaler.scale == ref_scale, (t, scaler.scale, ref_scale)
+        assert opt.t == st.t == (t if t < 3 else t - 1)
+        for got, ref in ((opt.master, st.p), (opt.exp_avg, st.m), (opt.exp_avg_sq, st.v)):
+            assert bits_equal_f32(raw(got), ref), t
+        assert np.array_equal(raw(opt.lowp), st.lowp)
+    # backed off once at step 3, grew at steps 2, 5, 7
+    assert scaler.scale == 2.0 ** 16 * 2 * 0.5 * 2 * 2

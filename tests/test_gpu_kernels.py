@@ -379,3 +379,24 @@ def test_accum_fused_norm_equals_separate_norm(dtype, n):
         nb = zs.zero_grad_sqnorm_workspace_bytes(n)
         assert torch.equal(ws_f[:nb], ws_s[:nb]), (ao, so)
         assert r_f == r_s
+
+
+def test_flatten_reads_pinned_host_grads():
+    """Grads in pinned host memory: the flatten kernel reads them over the host link
+    (transfer and flatten in one pass), bit for bit as from device memory."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    numels = list(W.ragged_numels(120, seed=9, max_log2=15))
+    host, _ = _table_case(numels, "bf16", null=(4,), seed=2)
+    pinned = [None if h is None else h.pin_memory() for h in host]
+    table, total = zs.zero_tensor_table(pinned, numels)
+    d_table = zs.device_table(table, len(numels), DEV)
+    s, e = oracle.shard_range(total, 3, 1)
+    dst = torch.empty(e - s, device=DEV)
+    ws = torch.empty(zs.zero_grad_sqnorm_workspace_bytes(e - s), dtype=torch.uint8, device=DEV)
+    zs.zero_flatten_cast(d_table, len(numels), total, torch.bfloat16, s, e, 1.0, False, dst, norm_ws=ws)
+    ref = np.zeros(e - s, np.float32)
+    oracle.flatten([raw(h) for h in host], numels, "bf16", s, e, 1.0, ref, accumulate=False)
+    torch.cuda.synchronize()
+    assert bits_equal_f32(raw(dst), ref)
+    with pytest.raises(ValueError):
+        zs.zero_tensor_table([torch.zeros(4, dtype=torch.bfloat16)], [4])  # pageable host memory is refused

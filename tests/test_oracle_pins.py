@@ -463,3 +463,38 @@ def test_fp16_lowp_writeback():
     oracle.adamw(st.p, st.m, st.v, g, sc, 1.0, st.lowp, lowp_dtype="f16")
     with np.errstate(over="ignore"):
         assert np.array_equal(st.lowp, st.p.astype(np.float16).view(np.uint16))
+
+
+# ------------------------------------------------------- dynamic loss scale
+@pytest.mark.parametrize("interval", [1, 3, 50])
+def test_loss_scale_policy_vs_torch_gradscaler(interval):
+    """The oracle's scale trajectory equals torch.amp.GradScaler's for random overflow patterns."""
+    rng = np.random.default_rng(interval)
+    found = [bool(x) for x in rng.random(300) < 0.15]
+    gs = torch.amp.GradScaler("cpu", init_scale=2.0 ** 16, growth_factor=2.0, backoff_factor=0.5,
+                              growth_interval=interval)
+    p = torch.nn.Parameter(torch.zeros(2))
+    opt = torch.optim.SGD([p], lr=0.0)
+    ref = []
+    for f in found:
+        gs.scale(torch.tensor(1.0))
+        p.grad = torch.full((2,), float("inf") if f else 1.0)
+        gs.unscale_(opt)
+        gs.step(opt)
+        gs.update()
+        ref.append(gs.get_scale())
+    assert oracle.loss_scale_trajectory(found, 2.0 ** 16, 2.0, 0.5, interval) == ref
+
+
+def test_unscale_folded_into_accumulation_is_exact():
+    """Scaling each micro-batch by 1/(S*M) equals accumulating with 1/M and unscaling by 1/S afterwards
+    (GradScaler.unscale_ after accumulation), bit for bit, for power-of-two S and M."""
+    rng = np.random.default_rng(5)
+    S, M, n = 2.0 ** 16, 8, 4000
+    xs = [oracle.f16_rne((rng.standard_normal(n) * 1e-5 * S).astype(np.float32)) for _ in range(M)]
+    a = np.zeros(n, np.float32)
+    b = np.zeros(n, np.float32)
+    for j, x in enumerate(xs):
+        oracle.accum(a, x, "f16", 1.0 / (S * M), accumulate=j > 0)
+        oracle.accum(b, x, "f16", 1.0 / M, accumulate=j > 0)
+    assert np.array_equal(a, b * np.float32(1.0 / S))
