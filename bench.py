@@ -177,9 +177,11 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / passes,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "llama7b_flat (oracle sample)", "params_per_step": tot, "world_size": 1, "rank": 0},
+        "config": {"workload": wl.name, "params_per_rank": wl.total, "tensors": wl.n_tensors, "world_size": 1,
+                   "grad_dtype": "bf16", "lowp_dtype": "bf16", "max_norm": wl.max_norm},
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"first {tot} params of the Llama-7B flat list, whole step per pass"},
+                         "sample": f"each step: the oracle's whole step (flatten/cast, norm, clip, AdamW) on the "
+                                   f"first {tot} params of the Llama-7B flat list; value in params/s"},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))

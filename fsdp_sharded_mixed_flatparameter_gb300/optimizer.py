@@ -165,6 +165,26 @@ class FlatShardAdamW:
             self.launch_step(extra_sqnorm, stream)
         return self.finish_step()
 
+    # -------------------------------------------------------- checkpoint
+    def state_dict(self) -> dict:
+        """The rank's optimizer state on the host: step counter, fp32 master /
+        exp_avg / exp_avg_sq and the low-precision copy (a flat shard each)."""
+        sd = {"t": self.t, "start": self.start, "end": self.end, "master": self.master.cpu(),
+              "exp_avg": self.exp_avg.cpu(), "exp_avg_sq": self.exp_avg_sq.cpu()}
+        if self.lowp is not None:
+            sd["lowp"] = self.lowp.cpu()
+        return sd
+
+    def load_state_dict(self, sd: dict) -> None:
+        if (sd["start"], sd["end"]) != (self.start, self.end):
+            raise ValueError("state belongs to another shard")
+        self.t = int(sd["t"])
+        self.master.copy_(sd["master"])
+        self.exp_avg.copy_(sd["exp_avg"])
+        self.exp_avg_sq.copy_(sd["exp_avg_sq"])
+        if self.lowp is not None and "lowp" in sd:
+            self.lowp.copy_(sd["lowp"])
+
     def resident_bytes(self) -> int:
         """Device bytes this rank holds for the step (grad + state + low-precision copy)."""
         b = 4 * (self.grad.numel() + 3 * self.n)
