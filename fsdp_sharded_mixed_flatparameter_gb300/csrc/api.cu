@@ -108,7 +108,8 @@ zero_status zero_flatten_cast(const zero_tensor* d_table, int32_t n_tensors, int
   if (!zs::valid_dtype(src_dtype)) return fail(ZERO_EINVAL, "zero_flatten_cast: bad src_dtype %d", (int)src_dtype);
   if (accumulate != 0 && accumulate != 1) return fail(ZERO_EINVAL, "zero_flatten_cast: accumulate must be 0 or 1");
   if (!std::isfinite(scale)) return fail(ZERO_EINVAL, "zero_flatten_cast: non-finite scale");
-  if (shard_end > shard_start && d_dst == nullptr) return fail(ZERO_EINVAL, "zero_flatten_cast: NULL d_dst");
+  if (shard_end > shard_start && d_dst == nullptr && (d_norm_ws == nullptr || accumulate != 0))
+    return fail(ZERO_EINVAL, "zero_flatten_cast: NULL d_dst needs a norm workspace and accumulate == 0");
   const zero_status w = check_norm_ws("zero_flatten_cast", d_norm_ws, norm_ws_bytes, shard_end - shard_start);
   if (w != ZERO_OK) return w;
   if (shard_end == shard_start) return ZERO_OK;
@@ -199,36 +200,69 @@ zero_status zero_loss_scale_update(float* scale, int32_t* growth_tracker, int32_
   return ZERO_OK;
 }
 
+static zero_status adamw_scalars(const char* who, const zero_adamw_hparams* hp, int64_t step, zs::AdamScalars* s) {
+  if (hp == nullptr) return fail(ZERO_EINVAL, "%s: NULL hparams", who);
+  if (step < 1) return fail(ZERO_EINVAL, "%s: step %lld < 1", who, (long long)step);
+  const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
+  if (!(std::isfinite(lr) && lr >= 0.0)) return fail(ZERO_EINVAL, "%s: bad lr", who);
+  if (!(b1 >= 0.0 && b1 < 1.0 && b2 >= 0.0 && b2 < 1.0)) return fail(ZERO_EINVAL, "%s: bad betas", who);
+  if (!(std::isfinite(eps) && eps > 0.0)) return fail(ZERO_EINVAL, "%s: bad eps", who);
+  if (!(std::isfinite(wd) && wd >= 0.0)) return fail(ZERO_EINVAL, "%s: bad weight_decay", who);
+  // per-step scalars in binary64, each rounded to binary32 once
+  const double bc1 = 1.0 - std::pow(b1, static_cast<double>(step));
+  const double bc2 = 1.0 - std::pow(b2, static_cast<double>(step));
+  s->step_size = static_cast<float>(lr / bc1);
+  s->bc2_sqrt = static_cast<float>(std::sqrt(bc2));
+  s->decay = static_cast<float>(1.0 - lr * wd);
+  s->b1 = static_cast<float>(b1);
+  s->omb1 = static_cast<float>(1.0 - b1);
+  s->b2 = static_cast<float>(b2);
+  s->omb2 = static_cast<float>(1.0 - b2);
+  s->eps = static_cast<float>(eps);
+  return ZERO_OK;
+}
+
 zero_status zero_adamw_step(float* d_master, float* d_exp_avg, float* d_exp_avg_sq, const float* d_grad,
                             void* d_param_lowp, zero_dtype lowp_dtype, int64_t n, const zero_adamw_hparams* hp,
                             int64_t step, const zero_norm_result* d_clip, void* stream) {
   if (n < 0) return fail(ZERO_EINVAL, "zero_adamw_step: n %lld < 0", (long long)n);
-  if (hp == nullptr) return fail(ZERO_EINVAL, "zero_adamw_step: NULL hparams");
-  if (step < 1) return fail(ZERO_EINVAL, "zero_adamw_step: step %lld < 1", (long long)step);
+  zs::AdamScalars s;
+  const zero_status hs = adamw_scalars("zero_adamw_step", hp, step, &s);
+  if (hs != ZERO_OK) return hs;
   if (n > 0 && (d_master == nullptr || d_exp_avg == nullptr || d_exp_avg_sq == nullptr || d_grad == nullptr))
     return fail(ZERO_EINVAL, "zero_adamw_step: NULL state or grad buffer");
   if (d_param_lowp != nullptr && lowp_dtype != ZERO_BF16 && lowp_dtype != ZERO_F16)
     return fail(ZERO_EINVAL, "zero_adamw_step: lowp_dtype must be BF16 or F16");
-  const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
-  if (!(std::isfinite(lr) && lr >= 0.0)) return fail(ZERO_EINVAL, "zero_adamw_step: bad lr");
-  if (!(b1 >= 0.0 && b1 < 1.0 && b2 >= 0.0 && b2 < 1.0)) return fail(ZERO_EINVAL, "zero_adamw_step: bad betas");
-  if (!(std::isfinite(eps) && eps > 0.0)) return fail(ZERO_EINVAL, "zero_adamw_step: bad eps");
-  if (!(std::isfinite(wd) && wd >= 0.0)) return fail(ZERO_EINVAL, "zero_adamw_step: bad weight_decay");
   if (n == 0) return ZERO_OK;
-  // per-step scalars in binary64, each rounded to binary32 once
-  const double bc1 = 1.0 - std::pow(b1, static_cast<double>(step));
-  const double bc2 = 1.0 - std::pow(b2, static_cast<double>(step));
-  zs::AdamScalars s;
-  s.step_size = static_cast<float>(lr / bc1);
-  s.bc2_sqrt = static_cast<float>(std::sqrt(bc2));
-  s.decay = static_cast<float>(1.0 - lr * wd);
-  s.b1 = static_cast<float>(b1);
-  s.omb1 = static_cast<float>(1.0 - b1);
-  s.b2 = static_cast<float>(b2);
-  s.omb2 = static_cast<float>(1.0 - b2);
-  s.eps = static_cast<float>(eps);
   return zs::launch_adamw(d_master, d_exp_avg, d_exp_avg_sq, d_grad, d_param_lowp, lowp_dtype, n, s, d_clip,
                           zs::as_stream(stream));
+}
+
+zero_status zero_adamw_step_tensors(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
+                                    const zero_tensor* d_table, int32_t n_tensors, int64_t total,
+                                    zero_dtype grad_dtype, int64_t shard_start, float grad_scale,
+                                    void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
+                                    const zero_adamw_hparams* hp, int64_t step, const zero_norm_result* d_clip,
+                                    void* stream) {
+  const char* who = "zero_adamw_step_tensors";
+  if (n < 0) return fail(ZERO_EINVAL, "%s: n %lld < 0", who, (long long)n);
+  zs::AdamScalars s;
+  const zero_status hs = adamw_scalars(who, hp, step, &s);
+  if (hs != ZERO_OK) return hs;
+  if (n_tensors < 0 || (n_tensors > 0 && d_table == nullptr)) return fail(ZERO_EINVAL, "%s: bad table", who);
+  if (total < 0 || (n_tensors == 0 && total != 0)) return fail(ZERO_EINVAL, "%s: total does not fit the table", who);
+  if (shard_start < 0 || n > total - shard_start)
+    return fail(ZERO_EINVAL, "%s: [%lld, %lld) outside [0, %lld]", who, (long long)shard_start,
+                (long long)(shard_start + n), (long long)total);
+  if (!zs::valid_dtype(grad_dtype)) return fail(ZERO_EINVAL, "%s: bad grad_dtype %d", who, (int)grad_dtype);
+  if (!std::isfinite(grad_scale)) return fail(ZERO_EINVAL, "%s: non-finite grad_scale", who);
+  if (n > 0 && (d_master == nullptr || d_exp_avg == nullptr || d_exp_avg_sq == nullptr))
+    return fail(ZERO_EINVAL, "%s: NULL state buffer", who);
+  if (d_param_lowp != nullptr && lowp_dtype != ZERO_BF16 && lowp_dtype != ZERO_F16)
+    return fail(ZERO_EINVAL, "%s: lowp_dtype must be BF16 or F16", who);
+  if (n == 0) return ZERO_OK;
+  return zs::launch_adamw_table(d_master, d_exp_avg, d_exp_avg_sq, d_table, n_tensors, grad_dtype, shard_start,
+                                grad_scale, d_param_lowp, lowp_dtype, n, s, d_clip, zs::as_stream(stream));
 }
 
 }  // extern "C"

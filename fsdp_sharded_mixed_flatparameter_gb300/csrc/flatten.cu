@@ -30,90 +30,11 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "reduce.cuh"
+#include "table.cuh"
 
 namespace zs {
 
-constexpr int kFlThreads = 256;
-constexpr int kFlTile = 8192;
-constexpr int kFlStage = kFlTile + kFlTile / 8;
-
-__device__ __forceinline__ int stage_idx(int q) { return q + (q >> 3); }
-
-// last i with table[i].flat_offset <= k (the tensor that holds flat index k)
-__device__ __forceinline__ int find_tensor(const zero_tensor* __restrict__ table, int n, int64_t k) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(&table[mid].flat_offset) <= k)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  return lo;
-}
-
-template <int DT>
-struct SrcTraits {
-  static constexpr int esize = (DT == ZERO_F32) ? 4 : 2;
-};
-
-// 8 consecutive source elements starting at a 32-byte (f32) or 16-byte
-// (16-bit) aligned address, widened to binary32.
-template <int DT>
-__device__ __forceinline__ void load8_src(const void* p, float (&x)[8]) {
-  if (DT == ZERO_F32) {
-    ld8_ro(static_cast<const float*>(p), x);
-  } else {
-    const uint4 w = ld16_ro(p);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[2 * j] = half_bits_to_f32<DT>(ws[j] & 0xffffu);
-      x[2 * j + 1] = half_bits_to_f32<DT>(ws[j] >> 16);
-    }
-  }
-}
-
-// Write fl(scale * x) of source elements [j0, j0 + len) into stage[q0 ...).
-template <int DT>
-__device__ __forceinline__ void stage_segment(const void* __restrict__ src, int64_t j0, int len, int q0,
-                                              float scale, float* stage, bool& bad) {
-  if (src == nullptr) {
-    const float y = __fmul_rn(scale, 0.0f);
-    for (int e = threadIdx.x; e < len; e += kFlThreads) stage[stage_idx(q0 + e)] = y;
-    return;
-  }
-  constexpr int es = SrcTraits<DT>::esize;
-  constexpr int vb = (DT == ZERO_F32) ? 32 : 16;  // bytes of one 8-element source vector
-  const char* sp = static_cast<const char*>(src) + es * j0;
-  int h = static_cast<int>(((vb - reinterpret_cast<uintptr_t>(sp) % vb) % vb) / es);
-  if (h > len) h = len;
-  const int nv = (len - h) / 8;
-  const int body_end = h + 8 * nv;
-  for (int e = threadIdx.x; e < h; e += kFlThreads) {
-    const float y = __fmul_rn(scale, load_elem<DT>(src, j0 + e));
-    bad |= !finite_f(y);
-    stage[stage_idx(q0 + e)] = y;
-  }
-  for (int vi = threadIdx.x; vi < nv; vi += kFlThreads) {
-    float x[8];
-    load8_src<DT>(sp + es * (h + 8 * vi), x);
-    const int q = q0 + h + 8 * vi;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float y = __fmul_rn(scale, x[i]);
-      bad |= !finite_f(y);
-      stage[stage_idx(q + i)] = y;
-    }
-  }
-  for (int e = body_end + threadIdx.x; e < len; e += kFlThreads) {
-    const float y = __fmul_rn(scale, load_elem<DT>(src, j0 + e));
-    bad |= !finite_f(y);
-    stage[stage_idx(q0 + e)] = y;
-  }
-}
-
-template <int DT, bool ACC, bool NORM>
+template <int DT, bool ACC, bool NORM, bool WRITE>
 __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* __restrict__ table, int n_tensors,
                                                              int64_t shard_start, int64_t len, int64_t ntiles,
                                                              float* __restrict__ dst, bool dst_vec, float scale,
@@ -125,6 +46,7 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
   constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
   constexpr int kPerBlock = NORM ? static_cast<int>(kSqTile / kFlTile) : 1;  // tiles per block
   static_assert(!NORM || kFlThreads == kSqThreads, "norm tile contract");
+  static_assert(WRITE || (NORM && !ACC), "norm-only mode reads and squares, nothing else");
   const int64_t nblocks_work = (ntiles + kPerBlock - 1) / kPerBlock;
   bool bad = false;
 
@@ -132,7 +54,7 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
     const int64_t t0 = wb * kPerBlock;
     const int64_t t1 = (t0 + kPerBlock < ntiles) ? t0 + kPerBlock : ntiles;
     int ti = find_tensor(table, n_tensors, shard_start + t0 * kFlTile);
-    float hi = 0.0f, lo = 0.0f;  // this thread's share of the norm tile
+    NormAcc nacc;  // this thread's share of the norm tile
 
     for (int64_t tile = t0; tile < t1; ++tile) {
       const int64_t base = tile * kFlTile;
@@ -143,8 +65,8 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
       const int64_t toff = __ldg(&table[ti].flat_offset), tnum = __ldg(&table[ti].numel);
       const char* tsrc = static_cast<const char*>(tptr) + es * (klo - toff);
 
-      const bool direct = tlen == kFlTile && dst_vec && tptr != nullptr && toff <= klo && khi <= toff + tnum &&
-                          reinterpret_cast<uintptr_t>(tsrc) % vb == 0;
+      const bool direct = tlen == kFlTile && (dst_vec || !WRITE) && tptr != nullptr && toff <= klo &&
+                          khi <= toff + tnum && reinterpret_cast<uintptr_t>(tsrc) % vb == 0;
       if (direct) {
         // 1024 groups of 8; thread t takes groups t + 256 r, r = 0..3, all loads first
         float x[4][8];
@@ -162,33 +84,21 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
             const float y = __fmul_rn(scale, x[r][i]);
             bad |= !finite_f(y);
             x[r][i] = ACC ? __fadd_rn(a[r][i], y) : y;
-            if (NORM) df_add_square(hi, lo, x[r][i]);
           }
-          st8(dst + base + 8 * (threadIdx.x + r * kFlThreads), x[r]);
+          if (NORM) nacc.add8(x[r]);
+          if (WRITE) st8(dst + base + 8 * (threadIdx.x + r * kFlThreads), x[r]);
         }
         continue;
       }
 
       // staged tile: walk the tensors that overlap [klo, khi)
-      int64_t k = klo;
-      int j = ti;
-      while (k < khi && j < n_tensors) {
-        const int64_t off = __ldg(&table[j].flat_offset), num = __ldg(&table[j].numel);
-        const int64_t seg_end = (off + num < khi) ? off + num : khi;
-        if (seg_end > k)
-          stage_segment<DT>(table[j].ptr, k - off, static_cast<int>(seg_end - k), static_cast<int>(k - klo), scale,
-                            stage, bad);
-        if (seg_end > k) k = seg_end;
-        ++j;
-      }
-      // a table that ends before `total` leaves the rest as zeros
-      for (int q = static_cast<int>(k - klo) + threadIdx.x; q < tlen; q += kFlThreads) stage[stage_idx(q)] = 0.0f;
+      stage_range<DT>(table, n_tensors, ti, klo, khi, scale, stage, bad);
       __syncthreads();
       const int ngroups = (tlen + 7) / 8;
       for (int u = threadIdx.x; u < ngroups; u += kFlThreads) {
         float y[8];
         const int64_t d = base + 8 * u;
-        if (dst_vec && 8 * u + 8 <= tlen) {
+        if ((dst_vec || !WRITE) && 8 * u + 8 <= tlen) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) y[i] = stage[stage_idx(8 * u + i)];
           if (ACC) {
@@ -197,47 +107,48 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
 #pragma unroll
             for (int i = 0; i < 8; ++i) y[i] = __fadd_rn(a[i], y[i]);
           }
-          if (NORM) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) df_add_square(hi, lo, y[i]);
-          }
-          st8(dst + d, y);
+          if (NORM) nacc.add8(y);
+          if (WRITE) st8(dst + d, y);
         } else {
           for (int i = 0; i < 8 && 8 * u + i < tlen; ++i) {
             const float si = stage[stage_idx(8 * u + i)];
             const float yi = ACC ? __fadd_rn(dst[d + i], si) : si;
-            if (NORM) df_add_square(hi, lo, yi);
-            dst[d + i] = yi;
+            if (NORM) nacc.add1(i, yi);
+            if (WRITE) dst[d + i] = yi;
           }
         }
       }
       __syncthreads();
     }
     if (NORM) {
-      const double bs = block_sum<kFlThreads>(static_cast<double>(hi) + static_cast<double>(lo), red);
+      const double bs = block_sum<kFlThreads>(nacc.total(), red);
       if (threadIdx.x == 0) partials[wb] = bs;
     }
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
 }
 
-template <int DT, bool ACC, bool NORM>
+template <int DT, bool ACC, bool NORM, bool WRITE>
 static zero_status launch_flatten_t(const zero_tensor* table, int32_t n_tensors, int64_t s, int64_t e, float scale,
                                     float* dst, int32_t* flag, double* partials, cudaStream_t st) {
   const int64_t len = e - s;
   const int64_t ntiles = (len + kFlTile - 1) / kFlTile;
   const int64_t per = NORM ? kSqTile / kFlTile : 1;
-  flatten_kernel<DT, ACC, NORM><<<one_pass_blocks(ntiles, per), kFlThreads, 0, st>>>(
-      table, n_tensors, s, len, ntiles, dst, aligned(dst, 32), scale, flag, partials);
+  flatten_kernel<DT, ACC, NORM, WRITE><<<one_pass_blocks(ntiles, per), kFlThreads, 0, st>>>(
+      table, n_tensors, s, len, ntiles, dst, dst != nullptr && aligned(dst, 32), scale, flag, partials);
   return check_launch("flatten_kernel");
 }
 
 template <int DT, bool ACC>
 static zero_status launch_flatten_n(const zero_tensor* table, int32_t n_tensors, int64_t s, int64_t e, float scale,
                                     float* dst, int32_t* flag, double* partials, cudaStream_t st) {
+  if (dst == nullptr) {  // norm partials only: the grad is not written (ACC is rejected by the caller)
+    if (ACC) return ZERO_EINVAL;
+    return launch_flatten_t<DT, false, true, false>(table, n_tensors, s, e, scale, nullptr, flag, partials, st);
+  }
   if (partials != nullptr)
-    return launch_flatten_t<DT, ACC, true>(table, n_tensors, s, e, scale, dst, flag, partials, st);
-  return launch_flatten_t<DT, ACC, false>(table, n_tensors, s, e, scale, dst, flag, nullptr, st);
+    return launch_flatten_t<DT, ACC, true, true>(table, n_tensors, s, e, scale, dst, flag, partials, st);
+  return launch_flatten_t<DT, ACC, false, true>(table, n_tensors, s, e, scale, dst, flag, nullptr, st);
 }
 
 zero_status launch_flatten(const zero_tensor* table, int32_t n_tensors, int src_dtype, int64_t s, int64_t e,
@@ -319,7 +230,7 @@ __global__ void __launch_bounds__(kSqThreads) accum_norm_kernel(float* __restric
   const char* s8 = static_cast<const char*>(src);
   bool bad = false;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    float hi = 0.0f, lo = 0.0f;
+    NormAcc nacc;
     const int64_t base = tile * kSqTile;
 #pragma unroll 1
     for (int r0 = 0; r0 < kSqVecPerThread; r0 += 4) {
@@ -343,21 +254,21 @@ __global__ void __launch_bounds__(kSqThreads) accum_norm_kernel(float* __restric
             const float y = __fmul_rn(scale, x[q][i]);
             bad |= !finite_f(y);
             x[q][i] = ACC ? __fadd_rn(a[q][i], y) : y;
-            df_add_square(hi, lo, x[q][i]);
           }
+          nacc.add8(x[q]);
           st8(acc + k, x[q]);
         } else {
           for (int i = 0; i < 8 && k + i < n; ++i) {
             const float y = __fmul_rn(scale, load_elem<DT>(src, k + i));
             bad |= !finite_f(y);
             const float o = ACC ? __fadd_rn(acc[k + i], y) : y;
-            df_add_square(hi, lo, o);
+            nacc.add1(i, o);
             acc[k + i] = o;
           }
         }
       }
     }
-    const double bs = block_sum<kSqThreads>(static_cast<double>(hi) + static_cast<double>(lo), red);
+    const double bs = block_sum<kSqThreads>(nacc.total(), red);
     if (threadIdx.x == 0) partials[tile] = bs;
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);

@@ -27,6 +27,12 @@ constexpr int64_t kSqTile = 32768;
 zero_status launch_adamw(float* p, float* m, float* v, const float* g, void* lowp, int lowp_dtype, int64_t n,
                          const AdamScalars& s, const zero_norm_result* clip, cudaStream_t st);
 
+// AdamW with the grad read through the tensor table (grad_scale * x at flat
+// index shard_start + k) instead of a materialized fp32 grad.
+zero_status launch_adamw_table(float* p, float* m, float* v, const zero_tensor* table, int n_tensors, int grad_dtype,
+                               int64_t shard_start, float gscale, void* lowp, int lowp_dtype, int64_t n,
+                               const AdamScalars& s, const zero_norm_result* clip, cudaStream_t st);
+
 // `partials` (nullable): also write the norm tiles' partial sums of squares
 // of the values written (one binary64 per 32768 elements of dst / acc).
 zero_status launch_flatten(const zero_tensor* table, int32_t n_tensors, int src_dtype, int64_t shard_start,

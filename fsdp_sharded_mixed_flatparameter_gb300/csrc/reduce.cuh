@@ -1,15 +1,16 @@
 // reduce.cuh -- the grad-norm reduction pieces shared by the norm kernel
-// and the kernels that fuse the norm into their last pass (flatten,
-// accumulate).  Internal; not part of the C ABI.
+// and the kernels that fuse the norm into their pass (flatten, accumulate,
+// norm-only).  Internal; not part of the C ABI.
 //
 // Tile contract (what makes fused and separate norms agree bit for bit):
 // the flat grad buffer is cut into tiles of kSqTile = 32768 elements,
 // indexed from the buffer's element 0; one block of kSqThreads = 256
 // threads owns a tile; thread t owns the 16 groups of 8 elements
 //     e = tile * 32768 + (r * 256 + t) * 8 + i,   r = 0..15, i = 0..7,
-// and adds their squares with df_add_square in (r, i) order; elements past
-// the end add nothing.  The 256 thread sums go through block_sum in binary64
-// and the result is the tile's partial.
+// and adds their squares into a NormAcc: even i into lane 0, odd i into
+// lane 1, each lane in increasing (r, i) order; elements past the end add
+// nothing.  The thread's value is NormAcc::total(); the 256 thread values go
+// through block_sum in binary64 and the result is the tile's partial.
 #pragma once
 
 #include "common.cuh"
@@ -21,16 +22,88 @@ constexpr int kSqThreads = 256;
 constexpr int kSqVecPerThread = 16;  // 16 x 8 = 128 elements per thread per tile
 static_assert(kSqThreads * kSqVecPerThread * 8 == kSqTile, "tile size");
 
-// hi + lo += x*x, error-free except for the rounding of lo itself
-__device__ __forceinline__ void df_add_square(float& hi, float& lo, float x) {
-  const float p = __fmul_rn(x, x);
-  const float e = __fmaf_rn(x, x, -p);  // x*x == p + e exactly
-  const float s = __fadd_rn(hi, p);     // TwoSum(hi, p) = s + t exactly
-  const float bp = __fsub_rn(s, hi);
-  const float t = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
-  hi = s;
-  lo = __fadd_rn(lo, __fadd_rn(t, e));
+// Packed pair arithmetic (sm_100+): one instruction applies the IEEE
+// round-to-nearest operation to two binary32 lanes, so every lane gets
+// exactly the bits the scalar operation would give.
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
 }
+__device__ __forceinline__ void f2_unpack(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// Two double-float accumulators (lane 0: even elements, lane 1: odd ones),
+// each an unevaluated sum h + l of two binary32 values.  Adding x*x: the
+// square is split exactly as x*x = p + e (one fma); p joins h by an
+// error-free TwoSum, s + t = h + p exactly; t and e go into l.  The relative
+// error of a lane is ~n * 2^-48 -- about 1e-14 here -- and non-finite inputs
+// make the total non-finite.  Lanes are updated in pairs with packed
+// instructions (half the instructions of scalar code); add1 does the same
+// arithmetic on one lane for ragged groups, giving the same bits.
+struct NormAcc {
+  unsigned long long h = 0ull, l = 0ull;  // lane 0 in the low word
+
+  __device__ __forceinline__ void add2(float x0, float x1) {
+    const unsigned long long x = f2_pack(x0, x1);
+    const unsigned long long p = f2_mul(x, x);
+    const unsigned long long e = f2_fma(x, x, p ^ 0x8000000080000000ull);  // x*x - p, exact
+    const unsigned long long s = f2_add(h, p);
+    const unsigned long long bp = f2_sub(s, h);
+    const unsigned long long t = f2_add(f2_sub(h, f2_sub(s, bp)), f2_sub(p, bp));
+    h = s;
+    l = f2_add(l, f2_add(t, e));
+  }
+  __device__ __forceinline__ void add8(const float (&x)[8]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) add2(x[2 * j], x[2 * j + 1]);
+  }
+  // element i (0..7) of a group alone, e.g. the ragged end of a buffer
+  __device__ __forceinline__ void add1(int i, float x) {
+    float h0, h1, l0, l1;
+    f2_unpack(h, h0, h1);
+    f2_unpack(l, l0, l1);
+    float& hh = (i & 1) ? h1 : h0;
+    float& ll = (i & 1) ? l1 : l0;
+    const float p = __fmul_rn(x, x);
+    const float e = __fmaf_rn(x, x, -p);
+    const float s = __fadd_rn(hh, p);
+    const float bp = __fsub_rn(s, hh);
+    const float t = __fadd_rn(__fsub_rn(hh, __fsub_rn(s, bp)), __fsub_rn(p, bp));
+    hh = s;
+    ll = __fadd_rn(ll, __fadd_rn(t, e));
+    h = f2_pack(h0, h1);
+    l = f2_pack(l0, l1);
+  }
+  __device__ __forceinline__ double total() const {
+    float h0, h1, l0, l1;
+    f2_unpack(h, h0, h1);
+    f2_unpack(l, l0, l1);
+    return (static_cast<double>(h0) + static_cast<double>(l0)) + (static_cast<double>(h1) + static_cast<double>(l1));
+  }
+};
 
 // Block-wide binary64 sum in a fixed order; the result is valid in thread 0.
 template <int THREADS>

@@ -6,12 +6,13 @@
 //  1. sqnorm_tiles_kernel: the grad buffer is cut into fixed tiles of
 //     kSqTile = 32768 elements.  A block reduces one tile at a time: each of
 //     its 256 threads takes 128 elements (16 x 32-byte loads, two rounds of
-//     eight) and adds their squares into a double-float accumulator (an
-//     unevaluated sum hi + lo of two binary32 values): every square is split
-//     exactly into x*x = p + e with one fma, p is added to hi with an
-//     error-free TwoSum, and the two error terms go into lo.  The 256 thread
-//     sums are added in binary64 by a fixed shuffle/shared-memory tree and the
-//     tile's binary64 partial is stored.  One block per tile (the grid loop
+//     eight) and adds their squares into two double-float accumulators
+//     (unevaluated sums h + l of two binary32 values, even and odd elements,
+//     updated together by packed f32x2 instructions): every square is split
+//     exactly into x*x = p + e with one fma, p is added to h with an
+//     error-free TwoSum, and the two error terms go into l (reduce.cuh).  The
+//     256 thread sums are added in binary64 by a fixed shuffle/shared-memory
+//     tree and the tile's binary64 partial is stored.  One block per tile (the grid loop
 //     only covers grids beyond the hardware limit), so the partial of a tile
 //     does not depend on which block computed it or how many blocks ran.
 //  2. sqnorm_finalize_kernel: one block adds the partials in a fixed order
@@ -21,12 +22,13 @@
 // Accuracy: the double-float sum carries about 48 significant bits, so the
 // relative error of the sum of squares is ~1e-14 (binary64 beyond the
 // thread level), about as good as the compensated binary64 sum of the CPU
-// oracle.  That is what makes the binary32 clip coefficient -- and with it
+// oracle.  (The accumulation order and helpers live in reduce.cuh, shared
+// with the kernels that fuse the norm into their pass.)  That is what makes the binary32 clip coefficient -- and with it
 // the whole AdamW step -- agree bit for bit with the oracle in practice: a
 // coarser norm would move the coefficient by an ulp now and then, and where
 // p*(1-lr*wd) and the Adam update nearly cancel, that ulp is a large
-// relative error of the new parameter.  The extra arithmetic (~10 binary32
-// operations per element) hides under the 4 bytes/element memory stream.
+// relative error of the new parameter.  The extra arithmetic (~5 packed
+// instructions per element) hides under the 4 bytes/element memory stream.
 // Limits: squares outside the binary32 range (|g| >= 2^64 overflows to a
 // non-finite norm, |g| < 2^-75 underflows toward 0) are where the result can
 // differ from the binary64 oracle; gradients never come near either.
@@ -46,7 +48,7 @@ namespace zs {
 // The thread adds its 128 squares in that (r, i) order.
 template <bool VEC>
 __device__ __forceinline__ double thread_tile_sum(const float* __restrict__ g, int64_t base, int64_t n) {
-  float hi = 0.0f, lo = 0.0f;
+  NormAcc acc;
 #pragma unroll
   for (int round = 0; round < 2; ++round) {
     float x[8][8];
@@ -61,12 +63,9 @@ __device__ __forceinline__ double thread_tile_sum(const float* __restrict__ g, i
       }
     }
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) df_add_square(hi, lo, x[r][i]);
-    }
+    for (int r = 0; r < 8; ++r) acc.add8(x[r]);  // out-of-range elements are 0 and add nothing
   }
-  return static_cast<double>(hi) + static_cast<double>(lo);
+  return acc.total();
 }
 
 __global__ void __launch_bounds__(kSqThreads) sqnorm_tiles_kernel(const float* __restrict__ g, int64_t n,

@@ -1,0 +1,115 @@
+// table.cuh -- reading grads through the FlatParameter tensor table:
+// locating the tensor that holds a flat index, 8-element vector loads of a
+// grad source, and staging a range of the flat buffer into shared memory
+// with loads aligned to each SOURCE tensor.  Shared by the flatten kernel and
+// the AdamW kernel that reads grads straight from the table.  Internal.
+#pragma once
+
+#include "common.cuh"
+
+namespace zs {
+
+constexpr int kFlThreads = 256;
+constexpr int kFlTile = 8192;
+constexpr int kFlStage = kFlTile + kFlTile / 8;
+
+__device__ __forceinline__ int stage_idx(int q) { return q + (q >> 3); }
+
+// last i with table[i].flat_offset <= k (the tensor that holds flat index k)
+__device__ __forceinline__ int find_tensor(const zero_tensor* __restrict__ table, int n, int64_t k) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(&table[mid].flat_offset) <= k)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int DT>
+struct SrcTraits {
+  static constexpr int esize = (DT == ZERO_F32) ? 4 : 2;
+};
+
+// 8 consecutive source elements starting at a 32-byte (f32) or 16-byte
+// (16-bit) aligned address, widened to binary32.
+template <int DT>
+__device__ __forceinline__ void load8_src(const void* p, float (&x)[8]) {
+  if (DT == ZERO_F32) {
+    ld8_ro(static_cast<const float*>(p), x);
+  } else {
+    const uint4 w = ld16_ro(p);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = half_bits_to_f32<DT>(ws[j] & 0xffffu);
+      x[2 * j + 1] = half_bits_to_f32<DT>(ws[j] >> 16);
+    }
+  }
+}
+
+// Write fl(scale * x) of source elements [j0, j0 + len) into stage[q0 ...).
+template <int DT>
+__device__ __forceinline__ void stage_segment(const void* __restrict__ src, int64_t j0, int len, int q0,
+                                              float scale, float* stage, bool& bad) {
+  if (src == nullptr) {
+    const float y = __fmul_rn(scale, 0.0f);
+    for (int e = threadIdx.x; e < len; e += kFlThreads) stage[stage_idx(q0 + e)] = y;
+    return;
+  }
+  constexpr int es = SrcTraits<DT>::esize;
+  constexpr int vb = (DT == ZERO_F32) ? 32 : 16;  // bytes of one 8-element source vector
+  const char* sp = static_cast<const char*>(src) + es * j0;
+  int h = static_cast<int>(((vb - reinterpret_cast<uintptr_t>(sp) % vb) % vb) / es);
+  if (h > len) h = len;
+  const int nv = (len - h) / 8;
+  const int body_end = h + 8 * nv;
+  for (int e = threadIdx.x; e < h; e += kFlThreads) {
+    const float y = __fmul_rn(scale, load_elem<DT>(src, j0 + e));
+    bad |= !finite_f(y);
+    stage[stage_idx(q0 + e)] = y;
+  }
+  for (int vi = threadIdx.x; vi < nv; vi += kFlThreads) {
+    float x[8];
+    load8_src<DT>(sp + es * (h + 8 * vi), x);
+    const int q = q0 + h + 8 * vi;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float y = __fmul_rn(scale, x[i]);
+      bad |= !finite_f(y);
+      stage[stage_idx(q + i)] = y;
+    }
+  }
+  for (int e = body_end + threadIdx.x; e < len; e += kFlThreads) {
+    const float y = __fmul_rn(scale, load_elem<DT>(src, j0 + e));
+    bad |= !finite_f(y);
+    stage[stage_idx(q0 + e)] = y;
+  }
+}
+
+// Stage fl(scale * x) of the flat range [klo, khi) into stage[0, khi - klo):
+// walk the tensors from ti (the one holding klo) forward, each segment read
+// with loads aligned to its source; whatever the table does not cover reads
+// as zeros.  Every thread of the block must call it (the caller syncs).
+template <int DT>
+__device__ __forceinline__ void stage_range(const zero_tensor* __restrict__ table, int n_tensors, int ti, int64_t klo,
+                                            int64_t khi, float scale, float* stage, bool& bad) {
+  int64_t k = klo;
+  int j = ti;
+  while (k < khi && j < n_tensors) {
+    const int64_t off = __ldg(&table[j].flat_offset), num = __ldg(&table[j].numel);
+    const int64_t seg_end = (off + num < khi) ? off + num : khi;
+    if (seg_end > k) {
+      stage_segment<DT>(table[j].ptr, k - off, static_cast<int>(seg_end - k), static_cast<int>(k - klo), scale,
+                        stage, bad);
+      k = seg_end;
+    }
+    ++j;
+  }
+  const int tlen = static_cast<int>(khi - klo);
+  for (int q = static_cast<int>(k - klo) + threadIdx.x; q < tlen; q += kFlThreads) stage[stage_idx(q)] = 0.0f;
+}
+
+}  // namespace zs

@@ -33,7 +33,7 @@ class FlatShardAdamW:
                  betas: Tuple[float, float] = (0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0,
                  max_norm: float = math.inf, lowp_dtype: Optional[torch.dtype] = torch.bfloat16,
                  grad_range: str = "shard", device="cuda", master: Optional[torch.Tensor] = None,
-                 lowp_out: Optional[torch.Tensor] = None):
+                 lowp_out: Optional[torch.Tensor] = None, grad_buffer: bool = True):
         if grad_range not in ("shard", "full"):
             raise ValueError("grad_range must be 'shard' or 'full'")
         self.device = torch.device(device)
@@ -45,7 +45,8 @@ class FlatShardAdamW:
         self.glo, self.ghi = (0, self.total) if grad_range == "full" else (self.start, self.end)
         self.lr, self.betas, self.eps, self.weight_decay, self.max_norm = lr, tuple(betas), eps, weight_decay, max_norm
         dev = self.device
-        self.grad = torch.empty(self.ghi - self.glo, dtype=torch.float32, device=dev)
+        # the fp32 flat grad; not needed when every step goes through step_tensors()
+        self.grad = torch.empty(self.ghi - self.glo if grad_buffer else 0, dtype=torch.float32, device=dev)
         if master is None:
             master = torch.zeros(self.n, dtype=torch.float32, device=dev)
         if master.numel() != self.n or master.dtype != torch.float32:
@@ -59,7 +60,7 @@ class FlatShardAdamW:
             self.lowp = torch.empty(self.n, dtype=lowp_dtype, device=dev)
         else:
             self.lowp = None
-        self.ws = torch.empty(max(zs.zero_grad_sqnorm_workspace_bytes(self.grad.numel()), 8), dtype=torch.uint8,
+        self.ws = torch.empty(max(zs.zero_grad_sqnorm_workspace_bytes(self.ghi - self.glo), 8), dtype=torch.uint8,
                               device=dev)
         self.norm_buf = zs.new_norm_result(dev)
         self.found_nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -165,6 +166,34 @@ class FlatShardAdamW:
             self.launch_step(extra_sqnorm, stream)
         return self.finish_step()
 
+    def step_tensors(self, grads: Sequence[Optional[torch.Tensor]], *, scale: float = 1.0, stream=None,
+                     process_group=None) -> zs.NormResult:
+        """One step straight from per-tensor grads, for a step without micro-batch
+        accumulation: a norm pass reads the grads through the FlatParameter table
+        without writing them, then AdamW reads them again through the table.  No
+        fp32 flat grad is written (30 instead of 36 bytes per parameter); the result
+        is bit-identical to flatten(scale) + step()."""
+        dts = {g.dtype for g in grads if g is not None}
+        if len(dts) > 1:
+            raise ValueError("all grads must share one dtype")
+        dt = dts.pop() if dts else torch.float32
+        table = self._table(grads)
+        zs.zero_flatten_cast(table, len(grads), self.total, dt, self.glo, self.ghi, scale, False, None,
+                             self.found_nonfinite, self.ws, stream)
+        if process_group is not None and self.glo == self.start and _world(process_group) > 1:
+            if self._local_buf is None:
+                self._local_buf = zs.new_norm_result(self.device)
+            zs.zero_grad_sqnorm_finalize(self.ws, self.ghi - self.glo, 0.0, math.inf, self._local_buf, stream)
+            gathered = gather_sqnorms(zs.sqnorm_view(self._local_buf), process_group)
+            zs.zero_grad_sqnorm_combine(gathered, self.max_norm, self.norm_buf, stream)
+        else:
+            zs.zero_grad_sqnorm_finalize(self.ws, self.ghi - self.glo, 0.0, self.max_norm, self.norm_buf, stream)
+        self._norm_ready = False
+        zs.zero_adamw_step_tensors(self.master, self.exp_avg, self.exp_avg_sq, table, len(grads), self.total, dt,
+                                   self.start, scale, self.lowp, self.lr, self.betas[0], self.betas[1], self.eps,
+                                   self.weight_decay, self.t + 1, self.norm_buf, stream)
+        return self.finish_step()
+
     # -------------------------------------------------------- checkpoint
     def state_dict(self) -> dict:
         """The rank's optimizer state on the host: step counter, fp32 master /
@@ -187,7 +216,7 @@ class FlatShardAdamW:
 
     def resident_bytes(self) -> int:
         """Device bytes this rank holds for the step (grad + state + low-precision copy)."""
-        b = 4 * (self.grad.numel() + 3 * self.n)
+        b = 4 * (self.grad.numel() + 3 * self.n)  # grad is empty without a grad buffer
         if self.lowp is not None:
             b += self.lowp.numel() * self.lowp.element_size()
         return b

@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
     L.zero_grad_sqnorm_noalloc.argtypes = [vp, i64, f64, f64, vp, vp]
     L.zero_adamw_step.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, i64, ctypes.POINTER(zero_adamw_hparams), i64,
                                   vp, vp]
+    L.zero_adamw_step_tensors.argtypes = [vp, vp, vp, vp, i32, i64, ctypes.c_int, i64, f32, vp, ctypes.c_int, i64,
+                                          ctypes.POINTER(zero_adamw_hparams), i64, vp, vp]
     L.zero_loss_scale_update.argtypes = [ctypes.POINTER(f32), ctypes.POINTER(i32), i32, f64, f64, i32]
     L.zero_status_string.argtypes = [ctypes.c_int]
     L.zero_status_string.restype = ctypes.c_char_p
@@ -84,7 +86,7 @@ def lib() -> ctypes.CDLL:
     L.zero_last_error.restype = ctypes.c_char_p
     for nm in ("zero_shard_range", "zero_tensor_table", "zero_flatten_cast", "zero_accum", "zero_grad_sqnorm",
                "zero_grad_sqnorm_finalize", "zero_grad_sqnorm_combine", "zero_grad_sqnorm_noalloc",
-               "zero_adamw_step", "zero_loss_scale_update"):
+               "zero_adamw_step", "zero_adamw_step_tensors", "zero_loss_scale_update"):
         getattr(L, nm).restype = ctypes.c_int
     _lib = L
     return L
@@ -181,13 +183,13 @@ def zero_flatten_cast(d_table: torch.Tensor, n_tensors: int, total: int, src_dty
                       shard_end: int, scale: float, accumulate: bool, dst: torch.Tensor,
                       found_nonfinite: Optional[torch.Tensor] = None, norm_ws: Optional[torch.Tensor] = None,
                       stream=None) -> None:
-    if shard_end > shard_start and dst.numel() < shard_end - shard_start:
+    if dst is not None and shard_end > shard_start and dst.numel() < shard_end - shard_start:
         raise ValueError("dst is smaller than the shard")
     tab = _dev(d_table, "d_table", torch.uint8, allow_none=n_tensors == 0)
     if n_tensors > 0 and d_table.numel() < n_tensors * TENSOR_ENTRY_BYTES:
         raise ValueError("d_table holds fewer entries than n_tensors")
     _check(lib().zero_flatten_cast(tab, n_tensors, total, _DT[src_dtype], shard_start, shard_end, scale,
-                                   int(bool(accumulate)), _dev(dst, "dst", torch.float32),
+                                   int(bool(accumulate)), _dev(dst, "dst", torch.float32, allow_none=norm_ws is not None),
                                    _dev(found_nonfinite, "found_nonfinite", torch.int32, allow_none=True),
                                    _dev(norm_ws, "norm_ws", allow_none=True), _ws_bytes(norm_ws), _stream(stream)))
 
@@ -266,6 +268,34 @@ def zero_adamw_step(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg_sq: tor
                                  _dev(exp_avg_sq, "exp_avg_sq", torch.float32), _dev(grad, "grad", torch.float32),
                                  _dev(param_lowp, "param_lowp", allow_none=True), lowp_dt, n, ctypes.byref(hp), step,
                                  _dev(clip, "clip", allow_none=True), _stream(stream)))
+
+
+def zero_adamw_step_tensors(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg_sq: torch.Tensor,
+                            d_table: torch.Tensor, n_tensors: int, total: int, grad_dtype: torch.dtype,
+                            shard_start: int, grad_scale: float, param_lowp: Optional[torch.Tensor], lr: float,
+                            beta1: float, beta2: float, eps: float, weight_decay: float, step: int,
+                            clip: Optional[torch.Tensor] = None, stream=None) -> None:
+    """AdamW over [shard_start, shard_start + n) with the grads read through the tensor table."""
+    n = master.numel()
+    for t, nm in ((exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq")):
+        if t.numel() != n:
+            raise ValueError(f"{nm} differs in size from master")
+    if n_tensors > 0 and d_table.numel() < n_tensors * TENSOR_ENTRY_BYTES:
+        raise ValueError("d_table holds fewer entries than n_tensors")
+    lowp_dt = ZERO_BF16
+    if param_lowp is not None:
+        if param_lowp.numel() != n or param_lowp.dtype not in (torch.bfloat16, torch.float16):
+            raise ValueError("param_lowp must be bf16/f16 with master's size")
+        lowp_dt = _DT[param_lowp.dtype]
+    if clip is not None and clip.numel() * clip.element_size() < NORM_RESULT_BYTES:
+        raise ValueError("clip is smaller than zero_norm_result")
+    hp = zero_adamw_hparams(lr, beta1, beta2, eps, weight_decay)
+    _check(lib().zero_adamw_step_tensors(_dev(master, "master", torch.float32), _dev(exp_avg, "exp_avg", torch.float32),
+                                         _dev(exp_avg_sq, "exp_avg_sq", torch.float32),
+                                         _dev(d_table, "d_table", torch.uint8, allow_none=n_tensors == 0), n_tensors,
+                                         total, _DT[grad_dtype], shard_start, grad_scale,
+                                         _dev(param_lowp, "param_lowp", allow_none=True), lowp_dt, n, ctypes.byref(hp),
+                                         step, _dev(clip, "clip", allow_none=True), _stream(stream)))
 
 
 # ------------------------------------------------------------ norm result I/O

@@ -126,7 +126,11 @@ zero_status zero_tensor_table(const void* const* ptrs, const int64_t* numels, in
  * d_table: device array of n_tensors entries as built by zero_tensor_table
  *   (sorted by flat_offset, contiguous, ending at `total`).
  * src_dtype: dtype of every grad in the table (F32, BF16 or F16).
- * d_dst: fp32, shard_end - shard_start elements.
+ * d_dst: fp32, shard_end - shard_start elements; or NULL together with a
+ *   norm workspace and accumulate == 0: then only the norm partials of the
+ *   values are written (the grad is not materialized -- for a step without
+ *   micro-batch accumulation whose update reads the grads through the table,
+ *   see zero_adamw_step_tensors).
  * d_found_nonfinite: NULL, or a device int32 set to 1 when any
  *   fl(scale * x) is inf or NaN (never cleared by the call: zero it first).
  * d_norm_ws: NULL, or a device workspace of at least
@@ -304,6 +308,31 @@ zero_status zero_grad_sqnorm_noalloc(const float* d_grad, int64_t n, double extr
 zero_status zero_loss_scale_update(float* scale, int32_t* growth_tracker, int32_t found_inf,
                                    double growth_factor, double backoff_factor,
                                    int32_t growth_interval);
+
+/* zero_adamw_step_tensors -- device.
+ * zero_adamw_step with the grad read straight from the per-tensor grads
+ * through the FlatParameter table instead of from a materialized fp32 flat
+ * grad: for k in [0, n) the grad is fl(grad_scale * x) where x is the grad
+ * element at flat index shard_start + k (0 for a tensor without grad), cast
+ * exactly to binary32 -- the value zero_flatten_cast(..., scale =
+ * grad_scale, accumulate = 0) would have written -- and the update is then
+ * the same operation sequence, so the result is bit-identical to flatten +
+ * zero_adamw_step.  For a step without micro-batch accumulation this is the
+ * whole flatten/cast row fused away: the step reads the bf16 grads twice
+ * (norm pass with d_dst = NULL, then this) and never writes the 4-byte fp32
+ * grad, 30 instead of 36 bytes per parameter, and the fp32 grad buffer
+ * (4 bytes/param of HBM) is not needed at all.
+ * d_table / n_tensors / total / grad_dtype as for zero_flatten_cast; the
+ * other arguments as for zero_adamw_step.
+ * Errors: those of zero_adamw_step, plus a bad table, [shard_start,
+ * shard_start + n) outside [0, total], a bad grad_dtype or a non-finite
+ * grad_scale. */
+zero_status zero_adamw_step_tensors(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
+                                    const zero_tensor* d_table, int32_t n_tensors, int64_t total,
+                                    zero_dtype grad_dtype, int64_t shard_start, float grad_scale,
+                                    void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
+                                    const zero_adamw_hparams* hp, int64_t step,
+                                    const zero_norm_result* d_clip, void* stream);
 
 /* Static text for a status code. */
 const char* zero_status_string(zero_status status);

@@ -71,10 +71,12 @@ def _host_parts(tg: W.TensorGrads, numels, offsets, a: int, b: int, nulls):
 
 
 def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk: int = 1 << 26,
-                 seed: int = 0, fused: bool = True) -> RunReport:
+                 seed: int = 0, fused: bool = True, direct: bool = False) -> RunReport:
     """fused: the last micro-batch's flatten/accumulate also computes the grad
     norm's partials (the norm is then only finalized); otherwise the norm is a
-    separate pass over the flat grad."""
+    separate pass over the flat grad.  direct: one micro-batch of per-tensor
+    grads, stepped with step_tensors() (no fp32 grad buffer at all)."""
+    assert not direct or (wl.micro_batches == 1 and wl.mode != "zero3")
     from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
 
     s, e = oracle.shard_range(wl.total, wl.world_size, wl.rank)
@@ -84,7 +86,8 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
     master = W.master_init(wl, s, e, device=DEV)
     opt = FlatShardAdamW(wl.numels, world_size=wl.world_size, rank=wl.rank, lr=wl.lr, betas=wl.betas, eps=wl.eps,
                          weight_decay=wl.weight_decay, max_norm=wl.max_norm, lowp_dtype=lowp_dt,
-                         grad_range="full" if wl.mode == "zero1" else "shard", device=DEV, master=master.clone())
+                         grad_range="full" if wl.mode == "zero1" else "shard", device=DEV, master=master.clone(),
+                         grad_buffer=not direct)
     assert (opt.start, opt.end) == (s, e)
     if sample is None or sample >= n:
         idx = None
@@ -113,9 +116,10 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
             else:
                 tg = W.tensor_grads(wl, t, j, device=DEV, storage=storages[j])
                 storages[j] = tg.storage
-                opt.flatten(tg.tensors, accumulate=j > 0, scale=scale, fuse_norm=fused and j == M - 1)
+                if not direct:
+                    opt.flatten(tg.tensors, accumulate=j > 0, scale=scale, fuse_norm=fused and j == M - 1)
                 micro.append(tg)
-        res = opt.step()
+        res = opt.step_tensors(micro[0].tensors) if direct else opt.step()
 
         # ---- oracle side: accumulate every element (chunked) for the norm
         sq_parts = []

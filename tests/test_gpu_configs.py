@@ -63,6 +63,18 @@ def test_llama7b_full_size_sampled():
     _summary(rep)
 
 
+def test_llama7b_full_size_direct_path_sampled():
+    """The benchmark's direct path (norm pass + AdamW through the tensor table, no fp32 grad) at full size."""
+    rep = run_workload(W.llama7b(), steps=1, sample=1_000_000, direct=True)
+    assert rep.n == 6738415616
+    _summary(rep)
+
+
+def test_ragged_direct_path_full():
+    rep = run_workload(W.ragged(), steps=2, direct=True)
+    _summary(rep)
+
+
 def test_llama7b_shape_all_steps():
     wl = W.small_llama(layers=4, hidden=512, mlp=1376, vocab=3200)
     rep = run_workload(wl, steps=W.llama7b().steps, fused=False)
