@@ -417,6 +417,92 @@ def run_gpu(args):
     return 0
 
 
+def run_config(args):
+    """One configuration's whole step on one GPU (its micro-batches, fused norm on the
+    last one, AdamW), inputs resident; prints one JSON line with the per-kernel split."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    wl = W.ALL[args.workload]()
+    if args.small:
+        # profiling case: the same distribution on ~10x fewer parameters
+        if wl.name.startswith("ragged"):
+            wl = wl.with_(name=wl.name + "_2000", numels=tuple(W.ragged_numels(2000, seed=0)))
+        elif wl.name.startswith("llama13b"):
+            wl = wl.with_(name=wl.name + "_5l", numels=tuple(W.llama_numels(5, 5120, 13824, 32000)))
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    s, e = zs.zero_shard_range(wl.total, wl.world_size, wl.rank)
+    n = e - s
+    opt = FlatShardAdamW(wl.numels, world_size=wl.world_size, rank=wl.rank, lr=wl.lr, betas=wl.betas, eps=wl.eps,
+                         weight_decay=wl.weight_decay, max_norm=wl.max_norm,
+                         grad_range="full" if wl.mode == "zero1" else "shard", device=dev,
+                         master=W.master_init(wl, s, e, device=dev))
+    M = wl.micro_batches
+    esize = W.torch_dtype(wl.grad_dtype).itemsize
+    if wl.mode == "zero3":
+        micro = [W.flat_grads(wl, 1, j, s, e, device=dev) for j in range(M)]
+    else:
+        micro = [W.tensor_grads(wl, 1, j, device=dev).tensors for j in range(M)]
+    src_bytes = M * opt.grad.numel() * esize  # each pass reads the grad range's elements once
+    stream = torch.cuda.current_stream(dev)
+
+    tables = [] if wl.mode == "zero3" else [opt._resolve(m) for m in micro]  # built once, like registered grads
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        for j in range(M):
+            if wl.mode == "zero3":
+                opt.accum(micro[j], accumulate=j > 0, scale=1.0 / M, fuse_norm=j == M - 1, stream=stream)
+            else:
+                table, count, dt = tables[j]
+                zs.zero_flatten_cast(table, count, opt.total, dt, opt.glo, opt.ghi, 1.0 / M, j > 0, opt.grad, None,
+                                     opt.ws if j == M - 1 else None, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        zs.zero_grad_sqnorm_finalize(opt.ws, opt.grad.numel(), 0.0, opt.max_norm, opt.norm_buf, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        zs.zero_adamw_step(opt.master, opt.exp_avg, opt.exp_avg_sq, opt.shard_grad(), opt.lowp, opt.lr,
+                           opt.betas[0], opt.betas[1], opt.eps, opt.weight_decay, opt.t + 1, opt.norm_buf, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        if not opt.finish_step().finite:
+            raise RuntimeError("non-finite grad norm in the benchmark")
+
+    for _ in range(args.warmup):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / args.steps
+    t_grad = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs)
+    t_k4 = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in evs)
+    peaks, _ = measured_peaks()
+    grad_elems = opt.grad.numel()
+    # grad passes: every micro-batch reads its source; the first writes the fp32 grad, later ones read+write it
+    grad_bytes = src_bytes + 4 * grad_elems * (1 + 2 * (M - 1))
+    line = {
+        "metric": METRIC, "value": n / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "params_per_rank": n, "tensors": wl.n_tensors, "world_size": wl.world_size,
+                   "rank": wl.rank, "micro_batches": M, "grad_dtype": wl.grad_dtype, "mode": wl.mode,
+                   "grad_buffer_elems": grad_elems},
+        "kernels_ms": {"flatten_or_accum_with_norm": t_grad, "adamw": t_k4},
+        "kernels_gbs": {"flatten_or_accum_with_norm": grad_bytes / (t_grad / 1e3) / 1e9,
+                        "adamw": ADAMW_BYTES_PER_PARAM * n / (t_k4 / 1e3) / 1e9},
+        "adamw_frac_of_measured_hbm": ADAMW_BYTES_PER_PARAM * n / (t_k4 / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -424,13 +510,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="llama7b_flat", choices=sorted(W.ALL),
+                    help="another configuration's step (a table row, not the headline line)")
     ap.add_argument("--small", action="store_true",
-                    help="profiling case for ncu: a 1-layer Llama-7B-shaped list (268M params), not a bench line")
+                    help="profiling case for ncu (a smaller list of the same shape), not a bench line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         raise SystemExit("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != "llama7b_flat":
+        return run_config(args)
     return run_gpu(args)
 
 

@@ -71,7 +71,24 @@ __device__ __forceinline__ void stage_segment(const void* __restrict__ src, int6
     bad |= !finite_f(y);
     stage[stage_idx(q0 + e)] = y;
   }
-  for (int vi = threadIdx.x; vi < nv; vi += kFlThreads) {
+  // body: four source vectors in flight per thread (loads first), then one at a time
+  int vi = threadIdx.x;
+  for (; vi + 3 * kFlThreads < nv; vi += 4 * kFlThreads) {
+    float x[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) load8_src<DT>(sp + es * (h + 8 * (vi + u * kFlThreads)), x[u]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = q0 + h + 8 * (vi + u * kFlThreads);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float y = __fmul_rn(scale, x[u][i]);
+        bad |= !finite_f(y);
+        stage[stage_idx(q + i)] = y;
+      }
+    }
+  }
+  for (; vi < nv; vi += kFlThreads) {
     float x[8];
     load8_src<DT>(sp + es * (h + 8 * vi), x);
     const int q = q0 + h + 8 * vi;

@@ -67,6 +67,7 @@ class FlatShardAdamW:
         self.t = 0
         self._norm_ready = False  # the grad norm's tile partials are up to date in self.ws
         self._local_buf: Optional[torch.Tensor] = None
+        self._registered = None
         self._tables: Dict[tuple, Tuple[torch.Tensor, int]] = {}
 
     # ---------------------------------------------------------------- grads
@@ -87,18 +88,37 @@ class FlatShardAdamW:
             self._tables[key] = hit
         return hit[0]
 
-    def flatten(self, grads: Sequence[Optional[torch.Tensor]], *, accumulate: bool, scale: float = 1.0,
-                fuse_norm: bool = False, stream=None) -> None:
-        """Flatten/cast per-tensor grads into the rank's flat fp32 grad (K1).
+    def register_grads(self, grads: Sequence[Optional[torch.Tensor]]) -> None:
+        """Fix the per-tensor grads once (e.g. views into one flat grad storage, as
+        FSDP's FlatParameter keeps them).  flatten() / step_tensors() called without
+        grads then reuse the device table and do no per-tensor host work, which
+        matters for lists of thousands of tensors."""
+        self._registered = (self._table(grads), len(grads), self._grad_dtype(grads))
+
+    @staticmethod
+    def _grad_dtype(grads) -> torch.dtype:
+        dts = {g.dtype for g in grads if g is not None}
+        if len(dts) > 1:
+            raise ValueError("all grads must share one dtype")
+        return dts.pop() if dts else torch.float32
+
+    def _resolve(self, grads):
+        if grads is None:
+            if self._registered is None:
+                raise ValueError("no grads given and none registered")
+            return self._registered
+        return self._table(grads), len(grads), self._grad_dtype(grads)
+
+    def flatten(self, grads: Optional[Sequence[Optional[torch.Tensor]]] = None, *, accumulate: bool,
+                scale: float = 1.0, fuse_norm: bool = False, stream=None) -> None:
+        """Flatten/cast per-tensor grads (or the registered ones) into the rank's flat
+        fp32 grad (K1).
 
         fuse_norm: this is the last micro-batch; the same pass also computes the
         grad norm's tile partials, so step() only has to finalize them.
         """
-        dts = {g.dtype for g in grads if g is not None}
-        if len(dts) > 1:
-            raise ValueError("all grads must share one dtype")
-        dt = dts.pop() if dts else torch.float32
-        zs.zero_flatten_cast(self._table(grads), len(grads), self.total, dt, self.glo, self.ghi, scale, accumulate,
+        table, count, dt = self._resolve(grads)
+        zs.zero_flatten_cast(table, count, self.total, dt, self.glo, self.ghi, scale, accumulate,
                              self.grad, self.found_nonfinite, self.ws if fuse_norm else None, stream)
         self._norm_ready = fuse_norm
 
@@ -166,19 +186,15 @@ class FlatShardAdamW:
             self.launch_step(extra_sqnorm, stream)
         return self.finish_step()
 
-    def step_tensors(self, grads: Sequence[Optional[torch.Tensor]], *, scale: float = 1.0, stream=None,
-                     process_group=None) -> zs.NormResult:
+    def step_tensors(self, grads: Optional[Sequence[Optional[torch.Tensor]]] = None, *, scale: float = 1.0,
+                     stream=None, process_group=None) -> zs.NormResult:
         """One step straight from per-tensor grads, for a step without micro-batch
         accumulation: a norm pass reads the grads through the FlatParameter table
         without writing them, then AdamW reads them again through the table.  No
         fp32 flat grad is written (30 instead of 36 bytes per parameter); the result
         is bit-identical to flatten(scale) + step()."""
-        dts = {g.dtype for g in grads if g is not None}
-        if len(dts) > 1:
-            raise ValueError("all grads must share one dtype")
-        dt = dts.pop() if dts else torch.float32
-        table = self._table(grads)
-        zs.zero_flatten_cast(table, len(grads), self.total, dt, self.glo, self.ghi, scale, False, None,
+        table, count, dt = self._resolve(grads)
+        zs.zero_flatten_cast(table, count, self.total, dt, self.glo, self.ghi, scale, False, None,
                              self.found_nonfinite, self.ws, stream)
         if process_group is not None and self.glo == self.start and _world(process_group) > 1:
             if self._local_buf is None:
@@ -189,7 +205,7 @@ class FlatShardAdamW:
         else:
             zs.zero_grad_sqnorm_finalize(self.ws, self.ghi - self.glo, 0.0, self.max_norm, self.norm_buf, stream)
         self._norm_ready = False
-        zs.zero_adamw_step_tensors(self.master, self.exp_avg, self.exp_avg_sq, table, len(grads), self.total, dt,
+        zs.zero_adamw_step_tensors(self.master, self.exp_avg, self.exp_avg_sq, table, count, self.total, dt,
                                    self.start, scale, self.lowp, self.lr, self.betas[0], self.betas[1], self.eps,
                                    self.weight_decay, self.t + 1, self.norm_buf, stream)
         return self.finish_step()

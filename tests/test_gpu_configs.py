@@ -8,6 +8,7 @@ smaller lists with the whole shard compared.
 """
 import math
 
+import numpy as np
 import pytest
 import torch
 
@@ -157,3 +158,53 @@ def test_resume_and_determinism_bit_identical():
         assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), name
         assert torch.equal(x.view(torch.uint8), z.view(torch.uint8)), name
     assert a.t == c.t == d.t == 4
+
+
+def test_empty_and_single_element_shards():
+    """More ranks than elements: empty shards step as no-ops (t still advances: the
+    norm of nothing is 0), one-element shards update like the oracle."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
+    import oracle
+    dev = torch.device("cuda:0")
+    numels = [3, 2]
+    g = [torch.tensor([1e-3, -2e-3, 3e-3], dtype=torch.bfloat16), torch.tensor([4e-3, 0.0], dtype=torch.bfloat16)]
+    full = np.zeros(5, np.float32)
+    oracle.flatten([x.view(torch.int16).numpy().view(np.uint16) for x in g], numels, "bf16", 0, 5, 1.0, full, False)
+    for rank in range(8):
+        s, e = oracle.shard_range(5, 8, rank)
+        p0 = torch.linspace(-1, 1, 5)[s:e].contiguous()
+        opt = FlatShardAdamW(numels, world_size=8, rank=rank, lr=1e-2, max_norm=1.0, device=dev, master=p0.to(dev))
+        for direct in (False, True):
+            if direct:
+                r = opt.step_tensors([x.to(dev) for x in g])
+            else:
+                opt.flatten([x.to(dev) for x in g], accumulate=False, fuse_norm=True)
+                r = opt.step()
+            assert r.finite
+        st = oracle.new_state(p0.numpy())
+        for _ in range(2):
+            oracle.step_reference(st, np.ascontiguousarray(full[s:e]), lr=1e-2, betas=(0.9, 0.999), eps=1e-8, wd=0.0,
+                                  max_norm=1.0)
+        assert opt.t == st.t == 2 and opt.n == e - s
+        assert np.array_equal(opt.master.cpu().numpy(), st.p)
+
+
+def test_registered_grads_match_passed_grads():
+    """register_grads() once, then flatten()/step_tensors() without grads: same bits as passing them."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
+    dev = torch.device("cuda:0")
+    wl = W.small_ragged(n_tensors=800, world_size=2, rank=0, max_norm=0.5)
+    s, e = __import__("oracle").shard_range(wl.total, 2, 0)
+    master = W.master_init(wl, s, e)
+    kw = dict(world_size=2, rank=0, lr=wl.lr, max_norm=wl.max_norm, device=dev)
+    a = FlatShardAdamW(wl.numels, master=master.to(dev), **kw)
+    b = FlatShardAdamW(wl.numels, master=master.to(dev), **kw)
+    tg = W.tensor_grads(wl, 1, 0, device=dev)
+    b.register_grads(tg.tensors)
+    for t in range(2):
+        a.flatten(tg.tensors, accumulate=False, fuse_norm=True)
+        b.flatten(accumulate=False, fuse_norm=True)
+        assert a.step() == b.step()
+    assert a.step_tensors(tg.tensors) == b.step_tensors()
+    for name in ("master", "exp_avg", "exp_avg_sq", "lowp"):
+        assert torch.equal(getattr(a, name).view(torch.uint8), getattr(b, name).view(torch.uint8))
