@@ -53,7 +53,7 @@ def measured_peaks():
 def adamw_source_hash():
     import hashlib
     h = hashlib.sha256()
-    for f in ("adamw.cu", "common.cuh"):
+    for f in ("adamw.cu", "adam.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "fsdp_sharded_mixed_flatparameter_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -63,9 +63,9 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
       while (ti + 1 < n_tensors && __ldg(&table[ti + 1].flat_offset) <= klo) ++ti;
       const void* tptr = table[ti].ptr;
       const int64_t toff = __ldg(&table[ti].flat_offset), tnum = __ldg(&table[ti].numel);
-      const char* tsrc = static_cast<const char*>(tptr) + es * (klo - toff);
+      const char* tsrc = tptr ? static_cast<const char*>(tptr) + es * (klo - toff) : nullptr;
 
-      const bool direct = tlen == kFlTile && (dst_vec || !WRITE) && tptr != nullptr && toff <= klo &&
+      const bool direct = tlen == kFlTile && (dst_vec || !WRITE) && tsrc != nullptr && toff <= klo &&
                           khi <= toff + tnum && reinterpret_cast<uintptr_t>(tsrc) % vb == 0;
       if (direct) {
         // 1024 groups of 8; thread t takes groups t + 256 r, r = 0..3, all loads first
