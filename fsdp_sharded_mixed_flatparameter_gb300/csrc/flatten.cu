@@ -27,6 +27,21 @@
 // squares of the values it writes in the order of the norm tile contract
 // (reduce.cuh), so its partial equals bit for bit what the separate norm
 // kernel would compute from the written buffer -- without reading it again.
+//
+// Norm only (WRITE = false: the direct AdamW path needs the norm of the
+// grads but not the flat copy): the pass reads 2 bytes per element and is
+// bound by instruction issue and latency rather than DRAM, so (a) one bulk
+// prefetch per block pulls its source range into L2 before the loads, and
+// (b) for 16-bit grads with a power-of-two scale (EXACT = 1; 2 when the
+// scale is 1 and the multiply goes away) every value fl(scale * w) has a
+// square with no rounding residual, so the in-tensor tiles use
+// NormAcc::add2_exact (same bits, fewer FMA-pipe operations) and replace the
+// per-element finiteness test by one packed fma per pair, z = v * 0 + z,
+// which stays +0 while every v is finite and turns NaN at the first inf/NaN.
+// (The same shortcut in the writing pass measured ~4 % slower there, where
+// DRAM is the bound, so the writing pass keeps the general code.)
+#include <string.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "reduce.cuh"
@@ -34,27 +49,43 @@
 
 namespace zs {
 
-template <int DT, bool ACC, bool NORM, bool WRITE>
+template <int DT, bool ACC, bool NORM, bool WRITE, int EXACT>
 __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* __restrict__ table, int n_tensors,
                                                              int64_t shard_start, int64_t len, int64_t ntiles,
                                                              float* __restrict__ dst, bool dst_vec, float scale,
                                                              int32_t* __restrict__ flag,
                                                              double* __restrict__ partials) {
   __shared__ float stage[kFlStage];
-  __shared__ double red[kFlThreads / 32];
+  __shared__ float2 red[kFlThreads / 32];
   constexpr int es = SrcTraits<DT>::esize;
   constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
   constexpr int kPerBlock = NORM ? static_cast<int>(kSqTile / kFlTile) : 1;  // tiles per block
   static_assert(!NORM || kFlThreads == kSqThreads, "norm tile contract");
   static_assert(WRITE || (NORM && !ACC), "norm-only mode reads and squares, nothing else");
+  static_assert(!EXACT || (DT != ZERO_F32 && !WRITE), "exact squares: norm-only pass over 16-bit grads");
   const int64_t nblocks_work = (ntiles + kPerBlock - 1) / kPerBlock;
   bool bad = false;
+  const unsigned long long scale2 = f2_pack(scale, scale);
+  unsigned long long zprobe = 0ull;  // EXACT: both lanes +0 while every value is finite
 
   for (int64_t wb = blockIdx.x; wb < nblocks_work; wb += gridDim.x) {
     const int64_t t0 = wb * kPerBlock;
     const int64_t t1 = (t0 + kPerBlock < ntiles) ? t0 + kPerBlock : ntiles;
     int ti = find_tensor(table, n_tensors, shard_start + t0 * kFlTile);
     NormAcc nacc;  // this thread's share of the norm tile
+    if (!WRITE && threadIdx.x == 0) {
+      // Norm only: the block's loads are 2-4 bytes per element, too few in
+      // flight to cover DRAM latency, so one bulk prefetch pulls the block's
+      // whole source range (up to 64 KB of a 16-bit tensor) into L2 first.
+      const int64_t k0 = shard_start + t0 * kFlTile;
+      const int64_t k1 = shard_start + ((t1 * kFlTile < len) ? t1 * kFlTile : len);
+      const zero_tensor tt = table[ti];
+      if (tt.ptr != nullptr && tt.flat_offset <= k0 && k1 <= tt.flat_offset + tt.numel) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(tt.ptr) + es * (k0 - tt.flat_offset);
+        const uintptr_t a0 = (a + 15) & ~uintptr_t(15), a1 = (a + es * (k1 - k0)) & ~uintptr_t(15);
+        if (a1 > a0) prefetch_l2_bulk(reinterpret_cast<const void*>(a0), static_cast<uint32_t>(a1 - a0));
+      }
+    }
 
     for (int64_t tile = t0; tile < t1; ++tile) {
       const int64_t base = tile * kFlTile;
@@ -67,6 +98,25 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
 
       const bool direct = tlen == kFlTile && (dst_vec || !WRITE) && tsrc != nullptr && toff <= klo &&
                           khi <= toff + tnum && reinterpret_cast<uintptr_t>(tsrc) % vb == 0;
+      if (EXACT && direct) {
+        // 1024 groups of 8 (16 bytes of source each); thread t takes groups t + 256 r, loads first
+        uint4 w[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) w[r] = ld16_ro(tsrc + 16 * (threadIdx.x + r * kFlThreads));
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const uint32_t ws[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const unsigned long long w2 =
+                f2_pack(half_bits_to_f32<DT>(ws[j] & 0xffffu), half_bits_to_f32<DT>(ws[j] >> 16));
+            const unsigned long long v = (EXACT == 2) ? w2 : f2_mul(w2, scale2);
+            zprobe = f2_fma(v, 0ull, zprobe);
+            nacc.add2_exact(v);
+          }
+        }
+        continue;
+      }
       if (direct) {
         // 1024 groups of 8; thread t takes groups t + 256 r, r = 0..3, all loads first
         float x[4][8];
@@ -121,11 +171,25 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
       __syncthreads();
     }
     if (NORM) {
-      const double bs = block_sum<kFlThreads>(nacc.total(), red);
+      const double bs = block_sum_norm<kFlThreads>(nacc, red);
       if (threadIdx.x == 0) partials[wb] = bs;
     }
   }
+  if (EXACT) {
+    float z0, z1;
+    f2_unpack(zprobe, z0, z1);
+    bad |= (z0 != 0.0f) || (z1 != 0.0f);  // NaN compares unequal
+  }
   if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
+}
+
+// A normal binary32 power of two (either sign): fl(scale * w) then keeps the
+// significand of a 16-bit w.
+static bool pow2_scale(float scale) {
+  uint32_t b;
+  memcpy(&b, &scale, sizeof b);
+  const uint32_t ex = (b >> 23) & 0xffu;
+  return (b & 0x7fffffu) == 0u && ex != 0u && ex != 0xffu;
 }
 
 template <int DT, bool ACC, bool NORM, bool WRITE>
@@ -134,8 +198,22 @@ static zero_status launch_flatten_t(const zero_tensor* table, int32_t n_tensors,
   const int64_t len = e - s;
   const int64_t ntiles = (len + kFlTile - 1) / kFlTile;
   const int64_t per = NORM ? kSqTile / kFlTile : 1;
-  flatten_kernel<DT, ACC, NORM, WRITE><<<one_pass_blocks(ntiles, per), kFlThreads, 0, st>>>(
-      table, n_tensors, s, len, ntiles, dst, dst != nullptr && aligned(dst, 32), scale, flag, partials);
+  const unsigned grid = one_pass_blocks(ntiles, per);
+  const bool dst_vec = dst != nullptr && aligned(dst, 32);
+  if constexpr (DT != ZERO_F32 && !WRITE) {
+    if (scale == 1.0f) {
+      flatten_kernel<DT, ACC, NORM, WRITE, 2><<<grid, kFlThreads, 0, st>>>(table, n_tensors, s, len, ntiles, dst,
+                                                                          dst_vec, scale, flag, partials);
+      return check_launch("flatten_kernel");
+    }
+    if (pow2_scale(scale)) {
+      flatten_kernel<DT, ACC, NORM, WRITE, 1><<<grid, kFlThreads, 0, st>>>(table, n_tensors, s, len, ntiles, dst,
+                                                                          dst_vec, scale, flag, partials);
+      return check_launch("flatten_kernel");
+    }
+  }
+  flatten_kernel<DT, ACC, NORM, WRITE, 0><<<grid, kFlThreads, 0, st>>>(table, n_tensors, s, len, ntiles, dst,
+                                                                          dst_vec, scale, flag, partials);
   return check_launch("flatten_kernel");
 }
 
@@ -225,7 +303,7 @@ __global__ void __launch_bounds__(kSqThreads) accum_norm_kernel(float* __restric
                                                                 int64_t n, int64_t ntiles, bool vec, float scale,
                                                                 int32_t* __restrict__ flag,
                                                                 double* __restrict__ partials) {
-  __shared__ double red[kSqThreads / 32];
+  __shared__ float2 red[kSqThreads / 32];
   constexpr int es = SrcTraits<DT>::esize;
   const char* s8 = static_cast<const char*>(src);
   bool bad = false;
@@ -268,7 +346,7 @@ __global__ void __launch_bounds__(kSqThreads) accum_norm_kernel(float* __restric
         }
       }
     }
-    const double bs = block_sum<kSqThreads>(nacc.total(), red);
+    const double bs = block_sum_norm<kSqThreads>(nacc, red);
     if (threadIdx.x == 0) partials[tile] = bs;
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);

@@ -9,8 +9,15 @@
 //     e = tile * 32768 + (r * 256 + t) * 8 + i,   r = 0..15, i = 0..7,
 // and adds their squares into a NormAcc: even i into lane 0, odd i into
 // lane 1, each lane in increasing (r, i) order; elements past the end add
-// nothing.  The thread's value is NormAcc::total(); the 256 thread values go
-// through block_sum in binary64 and the result is the tile's partial.
+// nothing.  The thread's value is NormAcc::value(), lane 0 + lane 1 as a
+// double-float; block_sum_norm adds the 256 thread values in double-float
+// (a shuffle tree down each warp, then the 8 warp values in warp order) and
+// the tile's partial is the binary64 sum of the result's two words.
+//
+// Everything up to the partial runs on the FP32 pipes: binary64 arithmetic
+// is a small fraction of the binary32 rate on GB300, and a per-thread
+// binary64 reduction was measured to keep that pipe ~40 % busy in the
+// norm-only pass.
 #pragma once
 
 #include "common.cuh"
@@ -55,6 +62,11 @@ __device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsig
   return d;
 }
 
+// A double-float: the unevaluated sum h + l of two binary32 values.
+struct DF {
+  float h, l;
+};
+
 // Two double-float accumulators (lane 0: even elements, lane 1: odd ones),
 // each an unevaluated sum h + l of two binary32 values.  Adding x*x: the
 // square is split exactly as x*x = p + e (one fma); p joins h by an
@@ -80,6 +92,26 @@ struct NormAcc {
 #pragma unroll
     for (int j = 0; j < 4; ++j) add2(x[2 * j], x[2 * j + 1]);
   }
+  // add2 for a packed pair whose squares leave no residual: e = x*x - p
+  // rounds to a zero in both lanes.  That holds for every fl(s * w) with w a
+  // bf16 or f16 value and s a power of two: the square of a significand of
+  // at most 11 bits fits binary32's 24 exactly, and where it underflows the
+  // residual is at most half of the smallest subnormal, which rounds to a
+  // zero (the tie goes to the even 0).  t + e then differs from t at most
+  // in the sign of a zero, and l -- +0 at the start, never -0 after, since a
+  // sum is -0 only when both terms are -- gets the same l + (t + e) = l + t.
+  // So this gives exactly add2's bits with three fewer instructions.  (An
+  // ordered Fast2Sum in place of TwoSum gives the same error term with fewer
+  // FMA-pipe operations, but needs scalar max/min and repacking; it measured
+  // no faster.)
+  __device__ __forceinline__ void add2_exact(unsigned long long x) {
+    const unsigned long long p = f2_mul(x, x);
+    const unsigned long long s = f2_add(h, p);
+    const unsigned long long bp = f2_sub(s, h);
+    const unsigned long long t = f2_add(f2_sub(h, f2_sub(s, bp)), f2_sub(p, bp));
+    h = s;
+    l = f2_add(l, t);
+  }
   // element i (0..7) of a group alone, e.g. the ragged end of a buffer
   __device__ __forceinline__ void add1(int i, float x) {
     float h0, h1, l0, l1;
@@ -97,15 +129,62 @@ struct NormAcc {
     h = f2_pack(h0, h1);
     l = f2_pack(l0, l1);
   }
-  __device__ __forceinline__ double total() const {
-    float h0, h1, l0, l1;
-    f2_unpack(h, h0, h1);
-    f2_unpack(l, l0, l1);
-    return (static_cast<double>(h0) + static_cast<double>(l0)) + (static_cast<double>(h1) + static_cast<double>(l1));
-  }
+  __device__ __forceinline__ DF value() const;
 };
 
-// Block-wide binary64 sum in a fixed order; the result is valid in thread 0.
+// s + e = a + b exactly, s = fl(a + b) (TwoSum: no condition on a, b).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// (a.h + a.l) + (b.h + b.l): the heads by TwoSum, the tails and its error
+// added, then renormalised by Fast2Sum (the head sum dominates the tail
+// sum).  For sums of squares (no cancellation) the relative error is a few
+// units of 2^-48; an inf or NaN anywhere makes the result non-finite.
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  float s, e;
+  two_sum(a.h, b.h, s, e);
+  const float t = __fadd_rn(__fadd_rn(a.l, b.l), e);
+  const float hh = __fadd_rn(s, t);
+  return DF{hh, __fsub_rn(t, __fsub_rn(hh, s))};
+}
+
+__device__ __forceinline__ DF NormAcc::value() const {
+  float h0, h1, l0, l1;
+  f2_unpack(h, h0, h1);
+  f2_unpack(l, l0, l1);
+  return df_add(DF{h0, l0}, DF{h1, l1});
+}
+
+// The tile partial of the tile contract: the block's 256 NormAcc values in
+// double-float, in a fixed order, rounded once to binary64.  Valid in
+// thread 0; every thread of the block must call it.
+template <int THREADS>
+__device__ __forceinline__ double block_sum_norm(const NormAcc& acc, float2* red) {
+  DF x = acc.value();
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const DF y{__shfl_down_sync(0xffffffffu, x.h, off), __shfl_down_sync(0xffffffffu, x.l, off)};
+    x = df_add(x, y);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = make_float2(x.h, x.l);
+  __syncthreads();
+  double r = 0.0;
+  if (threadIdx.x == 0) {
+    DF a{red[0].x, red[0].y};
+#pragma unroll
+    for (int w = 1; w < THREADS / 32; ++w) a = df_add(a, DF{red[w].x, red[w].y});
+    r = static_cast<double>(a.h) + static_cast<double>(a.l);
+  }
+  __syncthreads();  // red[] may be reused by the caller's next round
+  return r;
+}
+
+// Block-wide binary64 sum in a fixed order (the finalize over tile
+// partials); the result is valid in thread 0.
 template <int THREADS>
 __device__ __forceinline__ double block_sum(double x, double* red) {
 #pragma unroll

@@ -11,17 +11,18 @@
 //     updated together by packed f32x2 instructions): every square is split
 //     exactly into x*x = p + e with one fma, p is added to h with an
 //     error-free TwoSum, and the two error terms go into l (reduce.cuh).  The
-//     256 thread sums are added in binary64 by a fixed shuffle/shared-memory
-//     tree and the tile's binary64 partial is stored.  One block per tile (the grid loop
+//     256 thread sums are added in double-float by a fixed shuffle/shared-
+//     memory tree and the tile's partial is stored rounded to binary64.  One
+//     block per tile (the grid loop
 //     only covers grids beyond the hardware limit), so the partial of a tile
 //     does not depend on which block computed it or how many blocks ran.
 //  2. sqnorm_finalize_kernel: one block adds the partials in a fixed order
 //     (binary64), adds the other ranks' share, takes the square root and the
 //     clip coefficient, and writes the zero_norm_result.
 //
-// Accuracy: the double-float sum carries about 48 significant bits, so the
+// Accuracy: the double-float sums carry about 48 significant bits, so the
 // relative error of the sum of squares is ~1e-14 (binary64 beyond the
-// thread level), about as good as the compensated binary64 sum of the CPU
+// tile level), about as good as the compensated binary64 sum of the CPU
 // oracle.  (The accumulation order and helpers live in reduce.cuh, shared
 // with the kernels that fuse the norm into their pass.)  That is what makes the binary32 clip coefficient -- and with it
 // the whole AdamW step -- agree bit for bit with the oracle in practice: a
@@ -47,7 +48,7 @@ namespace zs {
 // e = ((r * 256) + t) * 8 + i: each 32-byte load of a warp covers 1 KiB.
 // The thread adds its 128 squares in that (r, i) order.
 template <bool VEC>
-__device__ __forceinline__ double thread_tile_sum(const float* __restrict__ g, int64_t base, int64_t n) {
+__device__ __forceinline__ NormAcc thread_tile_sum(const float* __restrict__ g, int64_t base, int64_t n) {
   NormAcc acc;
 #pragma unroll
   for (int round = 0; round < 2; ++round) {
@@ -65,18 +66,18 @@ __device__ __forceinline__ double thread_tile_sum(const float* __restrict__ g, i
 #pragma unroll
     for (int r = 0; r < 8; ++r) acc.add8(x[r]);  // out-of-range elements are 0 and add nothing
   }
-  return acc.total();
+  return acc;
 }
 
 __global__ void __launch_bounds__(kSqThreads) sqnorm_tiles_kernel(const float* __restrict__ g, int64_t n,
                                                                   int64_t ntiles, bool vec_ok,
                                                                   double* __restrict__ partials) {
-  __shared__ double red[kSqThreads / 32];
+  __shared__ float2 red[kSqThreads / 32];
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const int64_t base = tile * kSqTile;
-    const double ts = (vec_ok && base + kSqTile <= n) ? thread_tile_sum<true>(g, base, n)
-                                                      : thread_tile_sum<false>(g, base, n);
-    const double bs = block_sum<kSqThreads>(ts, red);
+    const NormAcc ts = (vec_ok && base + kSqTile <= n) ? thread_tile_sum<true>(g, base, n)
+                                                       : thread_tile_sum<false>(g, base, n);
+    const double bs = block_sum_norm<kSqThreads>(ts, red);
     if (threadIdx.x == 0) partials[tile] = bs;
   }
 }

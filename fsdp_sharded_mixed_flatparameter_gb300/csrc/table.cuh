@@ -28,6 +28,12 @@ __device__ __forceinline__ int find_tensor(const zero_tensor* __restrict__ table
   return lo;
 }
 
+// Ask the TMA unit to bring [p, p + bytes) into L2 (no data is returned;
+// p 16-byte aligned, bytes a multiple of 16, the range inside one allocation).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 template <int DT>
 struct SrcTraits {
   static constexpr int esize = (DT == ZERO_F32) ? 4 : 2;

@@ -185,8 +185,8 @@ size_t zero_grad_sqnorm_workspace_bytes(int64_t n);
  *   clip_coef = max_norm / (norm + 1e-6) if that is < 1, else 1 (binary32)
  *   finite = isfinite(norm)   -- the page skips the step when it is not
  * The squares are summed in fixed tiles of 32768 elements (exact squares
- * added into a double-float binary32 pair within a thread, binary64 across
- * threads and tiles, relative error ~1e-14), so the result does not depend
+ * added into double-float binary32 pairs within a tile, binary64 across
+ * tiles, relative error ~1e-14), so the result does not depend
  * on the GPU or the launch size and matches a binary64 sum to ~14 digits.
  * Squares beyond the binary32 range (|g| >= 2^64) give a non-finite norm.
  * extra_sqnorm is the other ranks' share of a global norm (0 for a norm over

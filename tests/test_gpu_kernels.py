@@ -381,6 +381,110 @@ def test_accum_fused_norm_equals_separate_norm(dtype, n):
         assert r_f == r_s
 
 
+def _spread_bits(n, dtype, rng):
+    """16-bit patterns over most of the format's range: random sign, exponent and
+    significand, subnormals and zeros included (squares from underflow to ~2^80)."""
+    sign = rng.integers(0, 2, n).astype(np.uint16) << 15
+    if dtype == "bf16":
+        ex = rng.integers(0, 168, n).astype(np.uint16) << 7
+        man = rng.integers(0, 128, n).astype(np.uint16)
+    else:
+        ex = rng.integers(0, 31, n).astype(np.uint16) << 10
+        man = rng.integers(0, 1024, n).astype(np.uint16)
+    return sign | ex | man
+
+
+def _bits_tensors(numels, dtype, seed, elem_offsets=(0,)):
+    rng = np.random.default_rng(seed)
+    tdt = W.torch_dtype(dtype)
+    host, dev = [], []
+    for i, n in enumerate(numels):
+        bits = _spread_bits(n, dtype, rng)
+        x = torch.from_numpy(bits.view(np.int16).copy()).view(tdt)
+        off = elem_offsets[i % len(elem_offsets)]
+        base = torch.zeros(n + off + 8, dtype=tdt, device=DEV)
+        base[off:off + n].copy_(x.to(DEV))
+        host.append(x)
+        dev.append(base[off:off + n])
+    return host, dev
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_exact_square_norm_equals_separate_norm(dtype):
+    """The norm-only pass over 16-bit grads with a power-of-two scale takes the
+    exact-square path (no residual term, packed non-finite probe).  Its partials equal
+    bit for bit those of the writing pass with the fused norm and of the separate norm
+    over the written buffer, over values from underflowing squares to ~2^80; a
+    non-power-of-two scale takes the general path and agrees the same way."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    tdt = W.torch_dtype(dtype)
+    cases = ((list(W.llama_numels(2, 256, 688, 1000)), (0,)),                     # in-tensor tiles
+             (list(W.ragged_numels(200, seed=9, max_log2=15)), (0, 1, 3, 8, 5)))  # staged tiles
+    for numels, offs in cases:
+        host, dev = _bits_tensors(numels, dtype, seed=len(numels), elem_offsets=offs)
+        table, total = zs.zero_tensor_table(dev, numels)
+        d_table = zs.device_table(table, len(numels), DEV)
+        rawh = [raw(h) for h in host]
+        for world, rank in ((1, 0), (3, 1)):
+            s, e = oracle.shard_range(total, world, rank)
+            n = e - s
+            nb = zs.zero_grad_sqnorm_workspace_bytes(n)
+            for scale in (1.0, 0.125, 2.0 ** -20, 4.0, 0.3):
+                ref = np.zeros(n, np.float32)
+                bad_ref = oracle.flatten(rawh, numels, dtype, s, e, scale, ref, accumulate=False)
+                plain = torch.empty(n, device=DEV)
+                fused = torch.empty(n, device=DEV)
+                ws_a = torch.full((nb,), 0x5A, dtype=torch.uint8, device=DEV)
+                ws_b = torch.full((nb,), 0xA5, dtype=torch.uint8, device=DEV)
+                flags = torch.zeros(3, dtype=torch.int32, device=DEV)
+                zs.zero_flatten_cast(d_table, len(numels), total, tdt, s, e, scale, False, plain, flags[0:1])
+                zs.zero_flatten_cast(d_table, len(numels), total, tdt, s, e, scale, False, None, flags[1:2],
+                                     norm_ws=ws_a)
+                zs.zero_flatten_cast(d_table, len(numels), total, tdt, s, e, scale, False, fused, flags[2:3],
+                                     norm_ws=ws_b)
+                torch.cuda.synchronize()
+                assert bits_equal_f32(raw(plain), ref) and torch.equal(plain.view(torch.int32),
+                                                                       fused.view(torch.int32)), scale
+                assert flags.tolist() == [int(bad_ref)] * 3, (scale, flags.tolist())
+                ws_s, r_s, r_a = _norm_pair(zs, plain, n, fused_ws=ws_a)
+                assert torch.equal(ws_a, ws_s[:nb]), (numels[:2], world, rank, scale)
+                assert torch.equal(ws_b, ws_s[:nb]), (numels[:2], world, rank, scale)
+                assert r_a == r_s
+                if math.isfinite(r_s.norm):
+                    cr = oracle.clip(oracle.sqnorm(ref), 0.0, 1.0)
+                    assert abs(r_s.norm - cr.norm) <= 1e-12 * cr.norm
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_exact_square_norm_flags_nonfinite(dtype):
+    """The packed probe of the exact-square path raises the flag for inf and NaN grads,
+    in in-tensor and staged tiles alike, and only for them: a finite bf16 grad whose
+    square overflows binary32 makes the norm non-finite without raising the flag."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    tdt = W.torch_dtype(dtype)
+    numels = list(W.llama_numels(1, 256, 688, 1000))
+    specials = [math.inf, -math.inf, math.nan] + ([2.0 ** 70] if dtype == "bf16" else [])
+    for value in specials:
+        for where in ((0, 5000), (4, 40000), (1, 5000), (len(numels) - 1, numels[-1] - 1)):  # in-tensor, staged
+            g = torch.Generator().manual_seed(3)
+            host = [(torch.randn(n, generator=g) * 1e-2).to(tdt) for n in numels]
+            host[where[0]][where[1]] = value
+            dev = [h.to(DEV) for h in host]
+            table, total = zs.zero_tensor_table(dev, numels)
+            d_table = zs.device_table(table, len(numels), DEV)
+            nb = zs.zero_grad_sqnorm_workspace_bytes(total)
+            ws = torch.zeros(nb, dtype=torch.uint8, device=DEV)
+            flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+            zs.zero_flatten_cast(d_table, len(numels), total, tdt, 0, total, 1.0, False, None, flag, norm_ws=ws)
+            out = zs.new_norm_result(DEV)
+            zs.zero_grad_sqnorm_finalize(ws, total, 0.0, 1.0, out)
+            r = zs.decode_norm_result(out)
+            ref = np.zeros(total, np.float32)
+            bad_ref = oracle.flatten([raw(h) for h in host], numels, dtype, 0, total, 1.0, ref, accumulate=False)
+            assert flag.item() == int(bad_ref) == int(not math.isfinite(value)), (value, where)
+            assert not math.isfinite(r.norm) and not r.finite, (value, where)
+
+
 def test_flatten_reads_pinned_host_grads():
     """Grads in pinned host memory: the flatten kernel reads them over the host link
     (transfer and flatten in one pass), bit for bit as from device memory."""
