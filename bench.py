@@ -149,18 +149,98 @@ def oracle_step_rate(wl: W.Workload, sample_params: int, min_seconds: float, max
     st = oracle.new_state(p)
     flat = np.empty(tot, np.float32)
     passes, t0 = 0, time.perf_counter()
+    stage = [0.0, 0.0, 0.0]
     while True:
+        ta = time.perf_counter()
         oracle.flatten(grads, numels, "bf16", 0, tot, 1.0, flat, accumulate=False)
+        tb = time.perf_counter()
         sq = oracle.sqnorm(flat)
         cr = oracle.clip(sq, 0.0, wl.max_norm)
+        tc = time.perf_counter()
         st.t += 1
         sc = oracle.adamw_scalars(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay, st.t)
         oracle.adamw(st.p, st.m, st.v, flat, sc, cr.coef, st.lowp)
+        td = time.perf_counter()
+        stage[0] += tb - ta
+        stage[1] += tc - tb
+        stage[2] += td - tc
         passes += 1
         el = time.perf_counter() - t0
         if el >= min_seconds or passes >= max_passes:
             break
+    oracle_step_rate.last_stages = {k: tot * passes / v for k, v in zip(("flatten", "sqnorm", "adamw"), stage)}
     return tot * passes / el, tot, passes, el
+
+
+def _sample_list(numels, lo: int, count: int):
+    """Sizes of the pieces of the tensor list that cover flat positions [lo, lo + count)."""
+    out, pos = [], 0
+    for n in numels:
+        a, b = max(pos, lo), min(pos + n, lo + count)
+        if b > a:
+            out.append(b - a)
+        pos += n
+        if pos >= lo + count:
+            break
+    return out
+
+
+def oracle_config_rates(wl: W.Workload, sample_params: int = 1 << 23, min_seconds: float = 2.0, max_reps: int = 5):
+    """Time the oracle's stages for one configuration on a bounded sample, single-threaded:
+    the grad pass of every micro-batch (per-tensor flatten/cast, or the flat accumulation of
+    ZeRO-3 shard grads), the sum of squares and clip, and AdamW.  Returns the per-stage
+    rates (elements/s) and the whole step's params/s extrapolated to the configuration's
+    sizes (M grad passes and one norm over the grad range, AdamW over the shard)."""
+    import oracle
+    s, e = oracle.shard_range(wl.total, wl.world_size, wl.rank)
+    n = e - s
+    glo, ghi = (0, wl.total) if wl.mode == "zero1" else (s, e)
+    S = min(sample_params, ghi - glo)
+    A = min(sample_params, n)
+    rng = np.random.default_rng(wl.seed)
+    lowp = {"bf16": torch.bfloat16, "f16": torch.float16}
+
+    def raw16(x):
+        return torch.from_numpy(x).to(lowp[wl.grad_dtype]).view(torch.int16).numpy().view(np.uint16)
+
+    def draw(k):
+        x = (rng.standard_normal(k) * wl.grad_std).astype(np.float32)
+        return x if wl.grad_dtype == "f32" else raw16(x)
+
+    pieces = _sample_list(wl.numels, glo, S)
+    srcs = [draw(k) for k in pieces]
+    flat_src = draw(S)
+    acc = np.empty(S, np.float32)
+    st = oracle.new_state((rng.standard_normal(A) * wl.init_std).astype(np.float32))
+    gA = (rng.standard_normal(A) * wl.grad_std).astype(np.float32)
+    M = wl.micro_batches
+    t_grad = t_norm = t_adam = 0.0
+    reps = 0
+    while reps < max_reps and (reps == 0 or t_grad + t_norm + t_adam < min_seconds):
+        t0 = time.perf_counter()
+        for j in range(M):
+            if wl.mode == "zero3":
+                oracle.accum(acc, flat_src, wl.grad_dtype, 1.0 / M, accumulate=j > 0)
+            else:
+                oracle.flatten(srcs, pieces, wl.grad_dtype, 0, S, 1.0 / M, acc, accumulate=j > 0)
+        t1 = time.perf_counter()
+        cr = oracle.clip(oracle.sqnorm(acc), 0.0, wl.max_norm)
+        t2 = time.perf_counter()
+        st.t += 1
+        sc = oracle.adamw_scalars(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay, st.t)
+        oracle.adamw(st.p, st.m, st.v, gA, sc, cr.coef, st.lowp)
+        t3 = time.perf_counter()
+        t_grad += t1 - t0
+        t_norm += t2 - t1
+        t_adam += t3 - t2
+        reps += 1
+    r_grad, r_norm, r_adam = M * S * reps / t_grad, S * reps / t_norm, A * reps / t_adam
+    step_s = M * (ghi - glo) / r_grad + (ghi - glo) / r_norm + n / r_adam
+    return {"value": n / step_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"each stage timed on a sample ({S} grad elements x {M} micro-batches, {A} AdamW params, "
+                      f"{reps} reps in {t_grad + t_norm + t_adam:.1f} s); value = shard params / "
+                      f"(the step's time extrapolated from the stage rates)",
+            "stages_elems_per_s": {"grad_pass": r_grad, "sqnorm": r_norm, "adamw": r_adam}}
 
 
 def run_reference(args):
@@ -410,7 +490,8 @@ def run_gpu(args):
         rate, tot, passes, el = oracle_step_rate(base, 1 << 25, 10.0, 50)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"first {tot} params of the Llama-7B flat list, {passes} whole-step "
-                                          f"passes in {el:.1f} s"}
+                                          f"passes in {el:.1f} s",
+                                "stages_elems_per_s": oracle_step_rate.last_stages}
     print(json.dumps(line))
     if pg is not None:
         pg.destroy_process_group()
@@ -499,6 +580,8 @@ def run_config(args):
                         "adamw": ADAMW_BYTES_PER_PARAM * n / (t_k4 / 1e3) / 1e9},
         "adamw_frac_of_measured_hbm": ADAMW_BYTES_PER_PARAM * n / (t_k4 / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
     }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_config_rates(wl)
     print(json.dumps(line))
     return 0
 
