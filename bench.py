@@ -498,6 +498,42 @@ def run_gpu(args):
     return 0
 
 
+def graph_step_ms(args, wl, s, e, dev, micro, stream) -> float:
+    """ms per step of the configuration's whole step replayed from a CUDA graph: a
+    capturable optimizer (device step count), all micro-batches' grad passes with the
+    fused norm on the last, finalize, prepare and AdamW captured once."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
+    opt = FlatShardAdamW(wl.numels, world_size=wl.world_size, rank=wl.rank, lr=wl.lr, betas=wl.betas, eps=wl.eps,
+                         weight_decay=wl.weight_decay, max_norm=wl.max_norm,
+                         grad_range="full" if wl.mode == "zero1" else "shard", device=dev,
+                         master=W.master_init(wl, s, e, device=dev), capturable=True)
+    M = wl.micro_batches
+    if wl.mode != "zero3":
+        for m in micro:
+            opt._table(m)  # device tables built before capture
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for j in range(M):
+            if wl.mode == "zero3":
+                opt.accum(micro[j], accumulate=j > 0, scale=1.0 / M, fuse_norm=j == M - 1)
+            else:
+                opt.flatten(micro[j], accumulate=j > 0, scale=1.0 / M, fuse_norm=j == M - 1)
+        opt.launch_step()
+    for _ in range(args.warmup):
+        graph.replay()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    if not opt.finish_step().finite:
+        raise RuntimeError("non-finite grad norm in the benchmark")
+    return a.elapsed_time(b) / args.steps
+
+
 def run_config(args):
     """One configuration's whole step on one GPU (its micro-batches, fused norm on the
     last one, AdamW), inputs resident; prints one JSON line with the per-kernel split."""
@@ -564,6 +600,7 @@ def run_config(args):
     ms = a.elapsed_time(b) / args.steps
     t_grad = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs)
     t_k4 = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in evs)
+    graph_ms = graph_step_ms(args, wl, s, e, dev, micro, stream) if n <= (1 << 31) else None
     peaks, _ = measured_peaks()
     grad_elems = opt.grad.numel()
     # grad passes: every micro-batch reads its source; the first writes the fp32 grad, later ones read+write it
@@ -580,6 +617,10 @@ def run_config(args):
                         "adamw": ADAMW_BYTES_PER_PARAM * n / (t_k4 / 1e3) / 1e9},
         "adamw_frac_of_measured_hbm": ADAMW_BYTES_PER_PARAM * n / (t_k4 / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
     }
+    if graph_ms is not None:
+        line["graph"] = {"ms_per_step": graph_ms, "value": n / (graph_ms / 1e3), "unit": UNIT,
+                         "what": "the same step captured once in a CUDA graph (step count and skip decision on the "
+                                 "device) and replayed back to back, no host work or device-to-host read per step"}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_config_rates(wl)
     print(json.dumps(line))

@@ -25,4 +25,26 @@ __device__ __forceinline__ void adam_update(float& p, float& m, float& v, float 
   p = __fsub_rn(p, __fmul_rn(s.step_size, u));
 }
 
+// The scalars of the step a kernel applies: the host-computed ones, or
+// (DEVS) those zero_adamw_prepare_device left in device memory, where
+// apply == 0 means the step is skipped (returns false).
+template <bool DEVS>
+__device__ __forceinline__ bool step_scalars(const AdamScalars& hs, const zero_adamw_device_state* ds,
+                                             AdamScalars& s) {
+  if (!DEVS) {
+    s = hs;
+    return true;
+  }
+  if (!ds->apply) return false;
+  s.step_size = ds->scalars[0];
+  s.bc2_sqrt = ds->scalars[1];
+  s.decay = ds->scalars[2];
+  s.b1 = ds->scalars[3];
+  s.omb1 = ds->scalars[4];
+  s.b2 = ds->scalars[5];
+  s.omb2 = ds->scalars[6];
+  s.eps = ds->scalars[7];
+  return true;
+}
+
 }  // namespace zs

@@ -34,12 +34,17 @@ __device__ __forceinline__ void adam_scalar(int64_t k, float* __restrict__ p, fl
 
 // LOWP: 0 (no copy), ZERO_BF16 or ZERO_F16.  LW: widest store (bytes) the
 // low-precision pointer's alignment allows for a group of 8: 16, 8, 4 or 2.
-template <int LOWP, int LW>
+// DEVS: scalars and skip decision from the device step state `ds` (graph-
+// capturable steps) instead of the host-computed `hs`.
+template <int LOWP, int LW, bool DEVS>
 __global__ void __launch_bounds__(256) adamw_v8_kernel(float* __restrict__ p, float* __restrict__ m,
                                                        float* __restrict__ v, const float* __restrict__ g,
                                                        void* __restrict__ lowp, int64_t head, int64_t nvec,
-                                                       int64_t n, AdamScalars s,
+                                                       int64_t n, AdamScalars hs,
+                                                       const zero_adamw_device_state* __restrict__ ds,
                                                        const zero_norm_result* __restrict__ clip) {
+  AdamScalars s;
+  if (!step_scalars<DEVS>(hs, ds, s)) return;  // the prepared step is skipped
   float coef = 1.0f;
   if (clip != nullptr) {
     if (!clip->finite) return;  // non-finite grad norm: the step is skipped
@@ -88,11 +93,14 @@ __global__ void __launch_bounds__(256) adamw_v8_kernel(float* __restrict__ p, fl
 }
 
 // Any alignment: one element per thread per iteration.
-template <int LOWP>
+template <int LOWP, bool DEVS>
 __global__ void __launch_bounds__(256) adamw_scalar_kernel(float* __restrict__ p, float* __restrict__ m,
                                                            float* __restrict__ v, const float* __restrict__ g,
-                                                           void* __restrict__ lowp, int64_t n, AdamScalars s,
+                                                           void* __restrict__ lowp, int64_t n, AdamScalars hs,
+                                                           const zero_adamw_device_state* __restrict__ ds,
                                                            const zero_norm_result* __restrict__ clip) {
+  AdamScalars s;
+  if (!step_scalars<DEVS>(hs, ds, s)) return;
   float coef = 1.0f;
   if (clip != nullptr) {
     if (!clip->finite) return;
@@ -105,39 +113,49 @@ __global__ void __launch_bounds__(256) adamw_scalar_kernel(float* __restrict__ p
 
 template <int LOWP, int LW>
 static zero_status launch_v8(float* p, float* m, float* v, const float* g, void* lowp, int64_t head,
-                             int64_t nvec, int64_t n, const AdamScalars& s, const zero_norm_result* clip,
-                             cudaStream_t st) {
-  adamw_v8_kernel<LOWP, LW><<<one_pass_blocks(nvec, 256), 256, 0, st>>>(p, m, v, g, lowp, head, nvec, n, s, clip);
+                             int64_t nvec, int64_t n, const AdamScalars& s, const zero_adamw_device_state* ds,
+                             const zero_norm_result* clip, cudaStream_t st) {
+  if (ds != nullptr)
+    adamw_v8_kernel<LOWP, LW, true><<<one_pass_blocks(nvec, 256), 256, 0, st>>>(p, m, v, g, lowp, head, nvec, n, s,
+                                                                                 ds, clip);
+  else
+    adamw_v8_kernel<LOWP, LW, false><<<one_pass_blocks(nvec, 256), 256, 0, st>>>(p, m, v, g, lowp, head, nvec, n, s,
+                                                                                  nullptr, clip);
   return check_launch("adamw_v8_kernel");
 }
 
 template <int LOWP>
 static zero_status launch_lowp(float* p, float* m, float* v, const float* g, void* lowp, int64_t n,
-                               const AdamScalars& s, const zero_norm_result* clip, cudaStream_t st) {
+                               const AdamScalars& s, const zero_adamw_device_state* ds, const zero_norm_result* clip,
+                               cudaStream_t st) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p) % 32;
   const bool coaligned = (a % 4 == 0) && reinterpret_cast<uintptr_t>(m) % 32 == a &&
                          reinterpret_cast<uintptr_t>(v) % 32 == a && reinterpret_cast<uintptr_t>(g) % 32 == a &&
                          (LOWP == 0 || reinterpret_cast<uintptr_t>(lowp) % 2 == 0);
   if (!coaligned) {
-    adamw_scalar_kernel<LOWP><<<one_pass_blocks(n, 256), 256, 0, st>>>(p, m, v, g, lowp, n, s, clip);
+    if (ds != nullptr)
+      adamw_scalar_kernel<LOWP, true><<<one_pass_blocks(n, 256), 256, 0, st>>>(p, m, v, g, lowp, n, s, ds, clip);
+    else
+      adamw_scalar_kernel<LOWP, false><<<one_pass_blocks(n, 256), 256, 0, st>>>(p, m, v, g, lowp, n, s, nullptr, clip);
     return check_launch("adamw_scalar_kernel");
   }
   int64_t head = static_cast<int64_t>((32 - a) % 32) / 4;
   if (head > n) head = n;
   const int64_t nvec = (n - head) / 8;
-  if (LOWP == 0) return launch_v8<0, 16>(p, m, v, g, lowp, head, nvec, n, s, clip, st);
+  if (LOWP == 0) return launch_v8<0, 16>(p, m, v, g, lowp, head, nvec, n, s, ds, clip, st);
   const uintptr_t la = (reinterpret_cast<uintptr_t>(lowp) + 2 * static_cast<uintptr_t>(head)) % 16;
-  if (la == 0) return launch_v8<LOWP, 16>(p, m, v, g, lowp, head, nvec, n, s, clip, st);
-  if (la % 8 == 0) return launch_v8<LOWP, 8>(p, m, v, g, lowp, head, nvec, n, s, clip, st);
-  if (la % 4 == 0) return launch_v8<LOWP, 4>(p, m, v, g, lowp, head, nvec, n, s, clip, st);
-  return launch_v8<LOWP, 2>(p, m, v, g, lowp, head, nvec, n, s, clip, st);
+  if (la == 0) return launch_v8<LOWP, 16>(p, m, v, g, lowp, head, nvec, n, s, ds, clip, st);
+  if (la % 8 == 0) return launch_v8<LOWP, 8>(p, m, v, g, lowp, head, nvec, n, s, ds, clip, st);
+  if (la % 4 == 0) return launch_v8<LOWP, 4>(p, m, v, g, lowp, head, nvec, n, s, ds, clip, st);
+  return launch_v8<LOWP, 2>(p, m, v, g, lowp, head, nvec, n, s, ds, clip, st);
 }
 
 zero_status launch_adamw(float* p, float* m, float* v, const float* g, void* lowp, int lowp_dtype, int64_t n,
-                         const AdamScalars& s, const zero_norm_result* clip, cudaStream_t st) {
-  if (lowp == nullptr) return launch_lowp<0>(p, m, v, g, nullptr, n, s, clip, st);
-  if (lowp_dtype == ZERO_BF16) return launch_lowp<ZERO_BF16>(p, m, v, g, lowp, n, s, clip, st);
-  return launch_lowp<ZERO_F16>(p, m, v, g, lowp, n, s, clip, st);
+                         const AdamScalars& s, const zero_adamw_device_state* ds, const zero_norm_result* clip,
+                         cudaStream_t st) {
+  if (lowp == nullptr) return launch_lowp<0>(p, m, v, g, nullptr, n, s, ds, clip, st);
+  if (lowp_dtype == ZERO_BF16) return launch_lowp<ZERO_BF16>(p, m, v, g, lowp, n, s, ds, clip, st);
+  return launch_lowp<ZERO_F16>(p, m, v, g, lowp, n, s, ds, clip, st);
 }
 
 }  // namespace zs

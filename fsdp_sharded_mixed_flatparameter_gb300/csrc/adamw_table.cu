@@ -19,13 +19,16 @@ namespace zs {
 // the state with coalesced scalar accesses.
 constexpr int kAtBlock = 2048;
 
-template <int DT, int LOWP, int LW>
+template <int DT, int LOWP, int LW, bool DEVS>
 __global__ void __launch_bounds__(256) adamw_table_kernel(float* __restrict__ p, float* __restrict__ m,
                                                           float* __restrict__ v, const zero_tensor* __restrict__ table,
                                                           int n_tensors, int64_t shard_start, int64_t n, float gscale,
-                                                          void* __restrict__ lowp, bool state_vec, AdamScalars s,
+                                                          void* __restrict__ lowp, bool state_vec, AdamScalars hs,
+                                                          const zero_adamw_device_state* __restrict__ ds,
                                                           const zero_norm_result* __restrict__ clip) {
   __shared__ float stage[kAtBlock + kAtBlock / 8];
+  AdamScalars s;
+  if (!step_scalars<DEVS>(hs, ds, s)) return;  // the prepared step is skipped
   float coef = 1.0f;
   if (clip != nullptr) {
     if (!clip->finite) return;  // non-finite grad norm: the step is skipped
@@ -98,51 +101,55 @@ __global__ void __launch_bounds__(256) adamw_table_kernel(float* __restrict__ p,
 template <int DT, int LOWP, int LW>
 static zero_status launch_table_t(float* p, float* m, float* v, const zero_tensor* table, int n_tensors,
                                   int64_t shard_start, int64_t n, float gscale, void* lowp, bool state_vec,
-                                  const AdamScalars& s, const zero_norm_result* clip, cudaStream_t st) {
-  adamw_table_kernel<DT, LOWP, LW><<<one_pass_blocks(n, kAtBlock), 256, 0, st>>>(
-      p, m, v, table, n_tensors, shard_start, n, gscale, lowp, state_vec, s, clip);
+                                  const AdamScalars& s, const zero_adamw_device_state* ds,
+                                  const zero_norm_result* clip, cudaStream_t st) {
+  if (ds != nullptr)
+    adamw_table_kernel<DT, LOWP, LW, true><<<one_pass_blocks(n, kAtBlock), 256, 0, st>>>(
+        p, m, v, table, n_tensors, shard_start, n, gscale, lowp, state_vec, s, ds, clip);
+  else
+    adamw_table_kernel<DT, LOWP, LW, false><<<one_pass_blocks(n, kAtBlock), 256, 0, st>>>(
+        p, m, v, table, n_tensors, shard_start, n, gscale, lowp, state_vec, s, nullptr, clip);
   return check_launch("adamw_table_kernel");
 }
 
 template <int DT, int LOWP>
 static zero_status launch_table_lw(float* p, float* m, float* v, const zero_tensor* table, int n_tensors,
                                    int64_t shard_start, int64_t n, float gscale, void* lowp, const AdamScalars& s,
-                                   const zero_norm_result* clip, cudaStream_t st) {
-  const bool state_vec = aligned(p, 32) && aligned(m, 32) && aligned(v, 32);
-  if (LOWP == 0)
-    return launch_table_t<DT, 0, 16>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, state_vec, s, clip, st);
+                                   const zero_adamw_device_state* ds, const zero_norm_result* clip, cudaStream_t st) {
+  const bool sv = aligned(p, 32) && aligned(m, 32) && aligned(v, 32);
   const uintptr_t la = reinterpret_cast<uintptr_t>(lowp) % 16;
-  if (la == 0)
-    return launch_table_t<DT, LOWP, 16>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, state_vec, s, clip,
-                                        st);
+  if (LOWP == 0 || la == 0)
+    return launch_table_t<DT, LOWP, 16>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, sv, s, ds, clip, st);
   if (la % 8 == 0)
-    return launch_table_t<DT, LOWP, 8>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, state_vec, s, clip, st);
+    return launch_table_t<DT, LOWP, 8>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, sv, s, ds, clip, st);
   if (la % 4 == 0)
-    return launch_table_t<DT, LOWP, 4>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, state_vec, s, clip, st);
-  return launch_table_t<DT, LOWP, 2>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, state_vec, s, clip, st);
+    return launch_table_t<DT, LOWP, 4>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, sv, s, ds, clip, st);
+  return launch_table_t<DT, LOWP, 2>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, sv, s, ds, clip, st);
 }
 
 template <int DT>
 static zero_status launch_table_dt(float* p, float* m, float* v, const zero_tensor* table, int n_tensors,
                                    int64_t shard_start, int64_t n, float gscale, void* lowp, int lowp_dtype,
-                                   const AdamScalars& s, const zero_norm_result* clip, cudaStream_t st) {
+                                   const AdamScalars& s, const zero_adamw_device_state* ds,
+                                   const zero_norm_result* clip, cudaStream_t st) {
   if (lowp == nullptr)
-    return launch_table_lw<DT, 0>(p, m, v, table, n_tensors, shard_start, n, gscale, nullptr, s, clip, st);
+    return launch_table_lw<DT, 0>(p, m, v, table, n_tensors, shard_start, n, gscale, nullptr, s, ds, clip, st);
   if (lowp_dtype == ZERO_BF16)
-    return launch_table_lw<DT, ZERO_BF16>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, s, clip, st);
-  return launch_table_lw<DT, ZERO_F16>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, s, clip, st);
+    return launch_table_lw<DT, ZERO_BF16>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, s, ds, clip, st);
+  return launch_table_lw<DT, ZERO_F16>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, s, ds, clip, st);
 }
 
 zero_status launch_adamw_table(float* p, float* m, float* v, const zero_tensor* table, int n_tensors, int grad_dtype,
                                int64_t shard_start, float gscale, void* lowp, int lowp_dtype, int64_t n,
-                               const AdamScalars& s, const zero_norm_result* clip, cudaStream_t st) {
+                               const AdamScalars& s, const zero_adamw_device_state* ds,
+                               const zero_norm_result* clip, cudaStream_t st) {
   if (grad_dtype == ZERO_F32)
-    return launch_table_dt<ZERO_F32>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, lowp_dtype, s, clip,
+    return launch_table_dt<ZERO_F32>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, lowp_dtype, s, ds, clip,
                                      st);
   if (grad_dtype == ZERO_BF16)
-    return launch_table_dt<ZERO_BF16>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, lowp_dtype, s, clip,
+    return launch_table_dt<ZERO_BF16>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, lowp_dtype, s, ds, clip,
                                       st);
-  return launch_table_dt<ZERO_F16>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, lowp_dtype, s, clip, st);
+  return launch_table_dt<ZERO_F16>(p, m, v, table, n_tensors, shard_start, n, gscale, lowp, lowp_dtype, s, ds, clip, st);
 }
 
 }  // namespace zs

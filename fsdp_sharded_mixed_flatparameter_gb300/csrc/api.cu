@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 
+#include "adam_scalars.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -208,17 +209,19 @@ static zero_status adamw_scalars(const char* who, const zero_adamw_hparams* hp, 
   if (!(b1 >= 0.0 && b1 < 1.0 && b2 >= 0.0 && b2 < 1.0)) return fail(ZERO_EINVAL, "%s: bad betas", who);
   if (!(std::isfinite(eps) && eps > 0.0)) return fail(ZERO_EINVAL, "%s: bad eps", who);
   if (!(std::isfinite(wd) && wd >= 0.0)) return fail(ZERO_EINVAL, "%s: bad weight_decay", who);
-  // per-step scalars in binary64, each rounded to binary32 once
-  const double bc1 = 1.0 - std::pow(b1, static_cast<double>(step));
-  const double bc2 = 1.0 - std::pow(b2, static_cast<double>(step));
-  s->step_size = static_cast<float>(lr / bc1);
-  s->bc2_sqrt = static_cast<float>(std::sqrt(bc2));
-  s->decay = static_cast<float>(1.0 - lr * wd);
-  s->b1 = static_cast<float>(b1);
-  s->omb1 = static_cast<float>(1.0 - b1);
-  s->b2 = static_cast<float>(b2);
-  s->omb2 = static_cast<float>(1.0 - b2);
-  s->eps = static_cast<float>(eps);
+  // per-step scalars in binary64, each rounded to binary32 once (the device
+  // step state of graph-captured steps uses the same code)
+  *s = zs::adam_scalars(lr, b1, b2, eps, wd, step);
+  return ZERO_OK;
+}
+
+zero_status zero_adamw_scalars(const zero_adamw_hparams* hp, int64_t step, float* out) {
+  if (out == nullptr) return fail(ZERO_EINVAL, "zero_adamw_scalars: NULL out");
+  zs::AdamScalars s;
+  const zero_status st = adamw_scalars("zero_adamw_scalars", hp, step, &s);
+  if (st != ZERO_OK) return st;
+  const float v[8] = {s.step_size, s.bc2_sqrt, s.decay, s.b1, s.omb1, s.b2, s.omb2, s.eps};
+  for (int i = 0; i < 8; ++i) out[i] = v[i];
   return ZERO_OK;
 }
 
@@ -234,8 +237,8 @@ zero_status zero_adamw_step(float* d_master, float* d_exp_avg, float* d_exp_avg_
   if (d_param_lowp != nullptr && lowp_dtype != ZERO_BF16 && lowp_dtype != ZERO_F16)
     return fail(ZERO_EINVAL, "zero_adamw_step: lowp_dtype must be BF16 or F16");
   if (n == 0) return ZERO_OK;
-  return zs::launch_adamw(d_master, d_exp_avg, d_exp_avg_sq, d_grad, d_param_lowp, lowp_dtype, n, s, d_clip,
-                          zs::as_stream(stream));
+  return zs::launch_adamw(d_master, d_exp_avg, d_exp_avg_sq, d_grad, d_param_lowp, lowp_dtype, n, s, nullptr,
+                          d_clip, zs::as_stream(stream));
 }
 
 zero_status zero_adamw_step_tensors(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
@@ -262,7 +265,68 @@ zero_status zero_adamw_step_tensors(float* d_master, float* d_exp_avg, float* d_
     return fail(ZERO_EINVAL, "%s: lowp_dtype must be BF16 or F16", who);
   if (n == 0) return ZERO_OK;
   return zs::launch_adamw_table(d_master, d_exp_avg, d_exp_avg_sq, d_table, n_tensors, grad_dtype, shard_start,
-                                grad_scale, d_param_lowp, lowp_dtype, n, s, d_clip, zs::as_stream(stream));
+                                grad_scale, d_param_lowp, lowp_dtype, n, s, nullptr, d_clip, zs::as_stream(stream));
+}
+
+// ------------------------------------------------------------- graph-capturable steps
+static zero_status check_state(const char* who, const void* d_state) {
+  if (d_state == nullptr) return fail(ZERO_EINVAL, "%s: NULL d_state", who);
+  if (!zs::aligned(d_state, 8)) return fail(ZERO_EINVAL, "%s: d_state not 8-byte aligned", who);
+  return ZERO_OK;
+}
+
+zero_status zero_adamw_prepare_device(const zero_adamw_hparams* d_hp, const zero_norm_result* d_clip,
+                                      zero_adamw_device_state* d_state, void* stream) {
+  const char* who = "zero_adamw_prepare_device";
+  if (d_hp == nullptr) return fail(ZERO_EINVAL, "%s: NULL d_hp", who);
+  if (!zs::aligned(d_hp, 8)) return fail(ZERO_EINVAL, "%s: d_hp not 8-byte aligned", who);
+  const zero_status c = check_state(who, d_state);
+  if (c != ZERO_OK) return c;
+  return zs::launch_adamw_prepare(d_hp, d_clip, d_state, zs::as_stream(stream));
+}
+
+zero_status zero_adamw_step_device(float* d_master, float* d_exp_avg, float* d_exp_avg_sq, const float* d_grad,
+                                   void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
+                                   const zero_adamw_device_state* d_state, const zero_norm_result* d_clip,
+                                   void* stream) {
+  const char* who = "zero_adamw_step_device";
+  if (n < 0) return fail(ZERO_EINVAL, "%s: n %lld < 0", who, (long long)n);
+  const zero_status c = check_state(who, d_state);
+  if (c != ZERO_OK) return c;
+  if (n > 0 && (d_master == nullptr || d_exp_avg == nullptr || d_exp_avg_sq == nullptr || d_grad == nullptr))
+    return fail(ZERO_EINVAL, "%s: NULL state or grad buffer", who);
+  if (d_param_lowp != nullptr && lowp_dtype != ZERO_BF16 && lowp_dtype != ZERO_F16)
+    return fail(ZERO_EINVAL, "%s: lowp_dtype must be BF16 or F16", who);
+  if (n == 0) return ZERO_OK;
+  return zs::launch_adamw(d_master, d_exp_avg, d_exp_avg_sq, d_grad, d_param_lowp, lowp_dtype, n, zs::AdamScalars{},
+                          d_state, d_clip, zs::as_stream(stream));
+}
+
+zero_status zero_adamw_step_tensors_device(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
+                                           const zero_tensor* d_table, int32_t n_tensors, int64_t total,
+                                           zero_dtype grad_dtype, int64_t shard_start, float grad_scale,
+                                           void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
+                                           const zero_adamw_device_state* d_state, const zero_norm_result* d_clip,
+                                           void* stream) {
+  const char* who = "zero_adamw_step_tensors_device";
+  if (n < 0) return fail(ZERO_EINVAL, "%s: n %lld < 0", who, (long long)n);
+  const zero_status c = check_state(who, d_state);
+  if (c != ZERO_OK) return c;
+  if (n_tensors < 0 || (n_tensors > 0 && d_table == nullptr)) return fail(ZERO_EINVAL, "%s: bad table", who);
+  if (total < 0 || (n_tensors == 0 && total != 0)) return fail(ZERO_EINVAL, "%s: total does not fit the table", who);
+  if (shard_start < 0 || n > total - shard_start)
+    return fail(ZERO_EINVAL, "%s: [%lld, %lld) outside [0, %lld]", who, (long long)shard_start,
+                (long long)(shard_start + n), (long long)total);
+  if (!zs::valid_dtype(grad_dtype)) return fail(ZERO_EINVAL, "%s: bad grad_dtype %d", who, (int)grad_dtype);
+  if (!std::isfinite(grad_scale)) return fail(ZERO_EINVAL, "%s: non-finite grad_scale", who);
+  if (n > 0 && (d_master == nullptr || d_exp_avg == nullptr || d_exp_avg_sq == nullptr))
+    return fail(ZERO_EINVAL, "%s: NULL state buffer", who);
+  if (d_param_lowp != nullptr && lowp_dtype != ZERO_BF16 && lowp_dtype != ZERO_F16)
+    return fail(ZERO_EINVAL, "%s: lowp_dtype must be BF16 or F16", who);
+  if (n == 0) return ZERO_OK;
+  return zs::launch_adamw_table(d_master, d_exp_avg, d_exp_avg_sq, d_table, n_tensors, grad_dtype, shard_start,
+                                grad_scale, d_param_lowp, lowp_dtype, n, zs::AdamScalars{}, d_state, d_clip,
+                                zs::as_stream(stream));
 }
 
 }  // extern "C"

@@ -10,8 +10,8 @@
 
 namespace zs {
 
-// Per-step AdamW scalars, computed in binary64 on the host and rounded to
-// binary32 once (bias corrections of the ZeRO page's ZeRO1Optimizer.step).
+// Per-step AdamW scalars, computed in binary64 and rounded to binary32 once
+// (bias corrections of the ZeRO page's ZeRO1Optimizer.step; adam_scalars.cuh).
 struct AdamScalars {
   float step_size;  // lr / (1 - beta1^t)
   float bc2_sqrt;   // sqrt(1 - beta2^t)
@@ -24,14 +24,22 @@ struct AdamScalars {
 // Elements per binary64 partial of the grad-norm reduction.
 constexpr int64_t kSqTile = 32768;
 
+// `ds` (nullable): take the scalars and the skip decision from the device
+// step state instead of `s` (graph-capturable steps).
 zero_status launch_adamw(float* p, float* m, float* v, const float* g, void* lowp, int lowp_dtype, int64_t n,
-                         const AdamScalars& s, const zero_norm_result* clip, cudaStream_t st);
+                         const AdamScalars& s, const zero_adamw_device_state* ds, const zero_norm_result* clip,
+                         cudaStream_t st);
 
 // AdamW with the grad read through the tensor table (grad_scale * x at flat
 // index shard_start + k) instead of a materialized fp32 grad.
 zero_status launch_adamw_table(float* p, float* m, float* v, const zero_tensor* table, int n_tensors, int grad_dtype,
                                int64_t shard_start, float gscale, void* lowp, int lowp_dtype, int64_t n,
-                               const AdamScalars& s, const zero_norm_result* clip, cudaStream_t st);
+                               const AdamScalars& s, const zero_adamw_device_state* ds,
+                               const zero_norm_result* clip, cudaStream_t st);
+
+// One thread: advance the device step state (see zero_adamw_prepare_device).
+zero_status launch_adamw_prepare(const zero_adamw_hparams* hp, const zero_norm_result* clip,
+                                 zero_adamw_device_state* state, cudaStream_t st);
 
 // `partials` (nullable): also write the norm tiles' partial sums of squares
 // of the values written (one binary64 per 32768 elements of dst / acc).

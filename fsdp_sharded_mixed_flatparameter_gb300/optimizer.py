@@ -11,6 +11,12 @@ incremented before use, skipping the step when the grad norm is not finite
 All arithmetic runs in libzeroshard's kernels; this class only allocates
 buffers with PyTorch and keeps the host-side step counter.
 
+Graph capture (``capturable=True``): the step counter and the skip decision
+live on the device (zero_adamw_prepare_device), so flatten/accumulate plus
+``launch_step()`` (or ``launch_step_tensors()``) make no host synchronisation
+and can be captured once in a ``torch.cuda.CUDAGraph`` and replayed as whole
+steps; the results are bit-identical to the host-counter steps.
+
 Grad range: for ZeRO-2/3 and FSDP the rank holds grads of its own shard
 only (``grad_range="shard"``, norm over the shard plus ``extra_sqnorm`` from
 the other ranks).  For ZeRO-1 every rank holds the whole averaged flat grad
@@ -33,7 +39,7 @@ class FlatShardAdamW:
                  betas: Tuple[float, float] = (0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0,
                  max_norm: float = math.inf, lowp_dtype: Optional[torch.dtype] = torch.bfloat16,
                  grad_range: str = "shard", device="cuda", master: Optional[torch.Tensor] = None,
-                 lowp_out: Optional[torch.Tensor] = None, grad_buffer: bool = True):
+                 lowp_out: Optional[torch.Tensor] = None, grad_buffer: bool = True, capturable: bool = False):
         if grad_range not in ("shard", "full"):
             raise ValueError("grad_range must be 'shard' or 'full'")
         self.device = torch.device(device)
@@ -64,11 +70,41 @@ class FlatShardAdamW:
                               device=dev)
         self.norm_buf = zs.new_norm_result(dev)
         self.found_nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.t = 0
+        self.capturable = capturable
+        self._t = 0
+        if capturable:
+            self._dev_hp = zs.device_hparams(lr, self.betas[0], self.betas[1], eps, weight_decay, dev)
+            self._dev_state = zs.new_adamw_device_state(dev)
         self._norm_ready = False  # the grad norm's tile partials are up to date in self.ws
         self._local_buf: Optional[torch.Tensor] = None
         self._registered = None
         self._tables: Dict[tuple, Tuple[torch.Tensor, int]] = {}
+
+    # ------------------------------------------------------- step counter
+    @property
+    def t(self) -> int:
+        """Steps applied so far (with capturable=True read from the device: a sync)."""
+        if self.capturable:
+            return zs.decode_adamw_device_state(self._dev_state).step
+        return self._t
+
+    @t.setter
+    def t(self, value: int) -> None:
+        if self.capturable:
+            self._dev_state.copy_(zs.new_adamw_device_state(self.device, int(value)))
+        else:
+            self._t = int(value)
+
+    def set_hparams(self, lr: Optional[float] = None, weight_decay: Optional[float] = None) -> None:
+        """Change lr / weight decay (e.g. a schedule).  With capturable=True the device copy
+        is rewritten in place, so a captured graph uses the new values at its next replay."""
+        if lr is not None:
+            self.lr = lr
+        if weight_decay is not None:
+            self.weight_decay = weight_decay
+        if self.capturable:
+            zs.device_hparams(self.lr, self.betas[0], self.betas[1], self.eps, self.weight_decay, self.device,
+                              out=self._dev_hp)
 
     # ---------------------------------------------------------------- grads
     def _table(self, grads: Sequence[Optional[torch.Tensor]]) -> torch.Tensor:
@@ -162,15 +198,21 @@ class FlatShardAdamW:
             zs.zero_grad_sqnorm_combine(gathered_sqnorms, self.max_norm, self.norm_buf, stream)
         else:
             self._norm_into(self.norm_buf, extra_sqnorm, self.max_norm, stream)
-        zs.zero_adamw_step(self.master, self.exp_avg, self.exp_avg_sq, self.shard_grad(), self.lowp, self.lr,
-                           self.betas[0], self.betas[1], self.eps, self.weight_decay, self.t + 1, self.norm_buf,
-                           stream)
+        if self.capturable:
+            zs.zero_adamw_prepare_device(self._dev_hp, self.norm_buf, self._dev_state, stream)
+            zs.zero_adamw_step_device(self.master, self.exp_avg, self.exp_avg_sq, self.shard_grad(), self.lowp,
+                                      self._dev_state, self.norm_buf, stream)
+        else:
+            zs.zero_adamw_step(self.master, self.exp_avg, self.exp_avg_sq, self.shard_grad(), self.lowp, self.lr,
+                               self.betas[0], self.betas[1], self.eps, self.weight_decay, self._t + 1,
+                               self.norm_buf, stream)
 
     def finish_step(self) -> zs.NormResult:
-        """Read the step's grad norm (a device->host copy that waits for the step)."""
+        """Read the step's grad norm (a device->host copy that waits for the step).
+        With capturable=True the device already advanced (or kept) the step count."""
         r = zs.decode_norm_result(self.norm_buf)
-        if r.finite:
-            self.t += 1
+        if r.finite and not self.capturable:
+            self._t += 1
         return r
 
     def step(self, extra_sqnorm: float = 0.0, stream=None, process_group=None) -> zs.NormResult:
@@ -193,6 +235,12 @@ class FlatShardAdamW:
         without writing them, then AdamW reads them again through the table.  No
         fp32 flat grad is written (30 instead of 36 bytes per parameter); the result
         is bit-identical to flatten(scale) + step()."""
+        self.launch_step_tensors(grads, scale=scale, stream=stream, process_group=process_group)
+        return self.finish_step()
+
+    def launch_step_tensors(self, grads: Optional[Sequence[Optional[torch.Tensor]]] = None, *, scale: float = 1.0,
+                            stream=None, process_group=None) -> None:
+        """Enqueue step_tensors() without waiting (capturable with registered grads)."""
         table, count, dt = self._resolve(grads)
         zs.zero_flatten_cast(table, count, self.total, dt, self.glo, self.ghi, scale, False, None,
                              self.found_nonfinite, self.ws, stream)
@@ -205,10 +253,15 @@ class FlatShardAdamW:
         else:
             zs.zero_grad_sqnorm_finalize(self.ws, self.ghi - self.glo, 0.0, self.max_norm, self.norm_buf, stream)
         self._norm_ready = False
-        zs.zero_adamw_step_tensors(self.master, self.exp_avg, self.exp_avg_sq, table, count, self.total, dt,
-                                   self.start, scale, self.lowp, self.lr, self.betas[0], self.betas[1], self.eps,
-                                   self.weight_decay, self.t + 1, self.norm_buf, stream)
-        return self.finish_step()
+        if self.capturable:
+            zs.zero_adamw_prepare_device(self._dev_hp, self.norm_buf, self._dev_state, stream)
+            zs.zero_adamw_step_tensors_device(self.master, self.exp_avg, self.exp_avg_sq, table, count, self.total,
+                                              dt, self.start, scale, self.lowp, self._dev_state, self.norm_buf,
+                                              stream)
+        else:
+            zs.zero_adamw_step_tensors(self.master, self.exp_avg, self.exp_avg_sq, table, count, self.total, dt,
+                                       self.start, scale, self.lowp, self.lr, self.betas[0], self.betas[1],
+                                       self.eps, self.weight_decay, self._t + 1, self.norm_buf, stream)
 
     # -------------------------------------------------------- checkpoint
     def state_dict(self) -> dict:

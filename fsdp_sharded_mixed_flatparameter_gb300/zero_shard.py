@@ -44,7 +44,14 @@ class zero_adamw_hparams(ctypes.Structure):
                 ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double)]
 
 
+class zero_adamw_device_state(ctypes.Structure):
+    _fields_ = [("step", ctypes.c_int64), ("apply", ctypes.c_int32), ("status", ctypes.c_int32),
+                ("scalars", ctypes.c_float * 8)]
+
+
 NORM_RESULT_BYTES = ctypes.sizeof(zero_norm_result)
+HPARAMS_BYTES = ctypes.sizeof(zero_adamw_hparams)
+DEVICE_STATE_BYTES = ctypes.sizeof(zero_adamw_device_state)
 TENSOR_ENTRY_BYTES = ctypes.sizeof(zero_tensor)
 
 _lib = None
@@ -80,13 +87,19 @@ def lib() -> ctypes.CDLL:
     L.zero_adamw_step_tensors.argtypes = [vp, vp, vp, vp, i32, i64, ctypes.c_int, i64, f32, vp, ctypes.c_int, i64,
                                           ctypes.POINTER(zero_adamw_hparams), i64, vp, vp]
     L.zero_loss_scale_update.argtypes = [ctypes.POINTER(f32), ctypes.POINTER(i32), i32, f64, f64, i32]
+    L.zero_adamw_scalars.argtypes = [ctypes.POINTER(zero_adamw_hparams), i64, vp]
+    L.zero_adamw_prepare_device.argtypes = [vp, vp, vp, vp]
+    L.zero_adamw_step_device.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, i64, vp, vp, vp]
+    L.zero_adamw_step_tensors_device.argtypes = [vp, vp, vp, vp, i32, i64, ctypes.c_int, i64, f32, vp, ctypes.c_int,
+                                                 i64, vp, vp, vp]
     L.zero_status_string.argtypes = [ctypes.c_int]
     L.zero_status_string.restype = ctypes.c_char_p
     L.zero_last_error.argtypes = []
     L.zero_last_error.restype = ctypes.c_char_p
     for nm in ("zero_shard_range", "zero_tensor_table", "zero_flatten_cast", "zero_accum", "zero_grad_sqnorm",
                "zero_grad_sqnorm_finalize", "zero_grad_sqnorm_combine", "zero_grad_sqnorm_noalloc",
-               "zero_adamw_step", "zero_adamw_step_tensors", "zero_loss_scale_update"):
+               "zero_adamw_step", "zero_adamw_step_tensors", "zero_loss_scale_update", "zero_adamw_scalars",
+               "zero_adamw_prepare_device", "zero_adamw_step_device", "zero_adamw_step_tensors_device"):
         getattr(L, nm).restype = ctypes.c_int
     _lib = L
     return L
@@ -296,6 +309,109 @@ def zero_adamw_step_tensors(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg
                                          total, _DT[grad_dtype], shard_start, grad_scale,
                                          _dev(param_lowp, "param_lowp", allow_none=True), lowp_dt, n, ctypes.byref(hp),
                                          step, _dev(clip, "clip", allow_none=True), _stream(stream)))
+
+
+# ------------------------------------------------- graph-capturable steps
+def zero_adamw_scalars(lr: float, beta1: float, beta2: float, eps: float, weight_decay: float, step: int) -> np.ndarray:
+    """The 8 binary32 scalars of step `step` (host): step_size, sqrt(1-beta2^t), 1-lr*wd,
+    beta1, 1-beta1, beta2, 1-beta2, eps."""
+    out = np.zeros(8, dtype=np.float32)
+    hp = zero_adamw_hparams(lr, beta1, beta2, eps, weight_decay)
+    _check(lib().zero_adamw_scalars(ctypes.byref(hp), step, ctypes.c_void_p(out.ctypes.data)))
+    return out
+
+
+def device_hparams(lr: float, beta1: float, beta2: float, eps: float, weight_decay: float, device,
+                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """A zero_adamw_hparams in device memory (uint8 bytes); rewrites `out` in place when given."""
+    hp = zero_adamw_hparams(lr, beta1, beta2, eps, weight_decay)
+    host = torch.frombuffer(bytearray(bytes(memoryview(hp))), dtype=torch.uint8)
+    if out is None:
+        return host.to(device)
+    out.copy_(host)
+    return out
+
+
+def new_adamw_device_state(device, step: int = 0) -> torch.Tensor:
+    """Device buffer for one zero_adamw_device_state with the step count set (0: fresh)."""
+    st = zero_adamw_device_state(step, 0, 0)
+    return torch.frombuffer(bytearray(bytes(memoryview(st))), dtype=torch.uint8).to(device)
+
+
+class AdamwDeviceState(NamedTuple):
+    step: int
+    apply: bool
+    status: int
+    scalars: np.ndarray
+
+
+def decode_adamw_device_state(buf: torch.Tensor) -> AdamwDeviceState:
+    raw = bytes(buf.detach().cpu().numpy().tobytes()[:DEVICE_STATE_BYTES])
+    r = zero_adamw_device_state.from_buffer_copy(raw)
+    return AdamwDeviceState(r.step, bool(r.apply), r.status, np.array(list(r.scalars), dtype=np.float32))
+
+
+def _state_arg(state: torch.Tensor):
+    if state.numel() * state.element_size() < DEVICE_STATE_BYTES:
+        raise ValueError("state is smaller than zero_adamw_device_state")
+    return _dev(state, "state")
+
+
+def zero_adamw_prepare_device(d_hp: torch.Tensor, clip: Optional[torch.Tensor], state: torch.Tensor,
+                              stream=None) -> None:
+    """Advance the device step state for the next step (skipped on a non-finite norm)."""
+    if d_hp.numel() * d_hp.element_size() < HPARAMS_BYTES:
+        raise ValueError("d_hp is smaller than zero_adamw_hparams")
+    if clip is not None and clip.numel() * clip.element_size() < NORM_RESULT_BYTES:
+        raise ValueError("clip is smaller than zero_norm_result")
+    _check(lib().zero_adamw_prepare_device(_dev(d_hp, "d_hp"), _dev(clip, "clip", allow_none=True),
+                                           _state_arg(state), _stream(stream)))
+
+
+def _lowp_arg(param_lowp: Optional[torch.Tensor], n: int):
+    if param_lowp is None:
+        return None, ZERO_BF16
+    if param_lowp.numel() != n or param_lowp.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("param_lowp must be bf16/f16 with master's size")
+    return _dev(param_lowp, "param_lowp"), _DT[param_lowp.dtype]
+
+
+def zero_adamw_step_device(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg_sq: torch.Tensor,
+                           grad: torch.Tensor, param_lowp: Optional[torch.Tensor], state: torch.Tensor,
+                           clip: Optional[torch.Tensor] = None, stream=None) -> None:
+    """zero_adamw_step with the scalars and skip decision of the device step state."""
+    n = master.numel()
+    for t, nm in ((exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq"), (grad, "grad")):
+        if t.numel() != n:
+            raise ValueError(f"{nm} differs in size from master")
+    if clip is not None and clip.numel() * clip.element_size() < NORM_RESULT_BYTES:
+        raise ValueError("clip is smaller than zero_norm_result")
+    lp, lowp_dt = _lowp_arg(param_lowp, n)
+    _check(lib().zero_adamw_step_device(_dev(master, "master", torch.float32), _dev(exp_avg, "exp_avg", torch.float32),
+                                        _dev(exp_avg_sq, "exp_avg_sq", torch.float32),
+                                        _dev(grad, "grad", torch.float32), lp, lowp_dt, n, _state_arg(state),
+                                        _dev(clip, "clip", allow_none=True), _stream(stream)))
+
+
+def zero_adamw_step_tensors_device(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg_sq: torch.Tensor,
+                                   d_table: torch.Tensor, n_tensors: int, total: int, grad_dtype: torch.dtype,
+                                   shard_start: int, grad_scale: float, param_lowp: Optional[torch.Tensor],
+                                   state: torch.Tensor, clip: Optional[torch.Tensor] = None, stream=None) -> None:
+    """zero_adamw_step_tensors with the scalars and skip decision of the device step state."""
+    n = master.numel()
+    for t, nm in ((exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq")):
+        if t.numel() != n:
+            raise ValueError(f"{nm} differs in size from master")
+    if n_tensors > 0 and d_table.numel() < n_tensors * TENSOR_ENTRY_BYTES:
+        raise ValueError("d_table holds fewer entries than n_tensors")
+    if clip is not None and clip.numel() * clip.element_size() < NORM_RESULT_BYTES:
+        raise ValueError("clip is smaller than zero_norm_result")
+    lp, lowp_dt = _lowp_arg(param_lowp, n)
+    _check(lib().zero_adamw_step_tensors_device(
+        _dev(master, "master", torch.float32), _dev(exp_avg, "exp_avg", torch.float32),
+        _dev(exp_avg_sq, "exp_avg_sq", torch.float32), _dev(d_table, "d_table", torch.uint8, allow_none=n_tensors == 0),
+        n_tensors, total, _DT[grad_dtype], shard_start, grad_scale, lp, lowp_dt, n, _state_arg(state),
+        _dev(clip, "clip", allow_none=True), _stream(stream)))
 
 
 # ------------------------------------------------------------ norm result I/O

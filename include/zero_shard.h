@@ -246,7 +246,7 @@ zero_status zero_grad_sqnorm_combine(const double* d_sqnorms, int32_t n_parts, d
  *   p = p - (lr / (1-beta1^t)) * (m / d)
  *   lowp = round_to_nearest_even(p)
  * where the per-step scalars are computed in binary64 on the host and
- * rounded to binary32 once.  d_master, d_exp_avg, d_exp_avg_sq (fp32, n,
+ * rounded to binary32 once (zero_adamw_scalars).  d_master, d_exp_avg, d_exp_avg_sq (fp32, n,
  * updated in place), d_grad (fp32, n).  d_param_lowp: NULL or n elements of
  * lowp_dtype (BF16, or F16 for the ZeRO-3 page's fp16 local chunk); the
  * rank's slice of the full low-precision FlatParameter may start at any
@@ -333,6 +333,73 @@ zero_status zero_adamw_step_tensors(float* d_master, float* d_exp_avg, float* d_
                                     void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
                                     const zero_adamw_hparams* hp, int64_t step,
                                     const zero_norm_result* d_clip, void* stream);
+
+/* ---------------------------------------------------------------------
+ * Graph-capturable steps.  No counterpart on the source pages: the pages'
+ * loops keep the step count on the host and read the grad norm there to
+ * decide on skipping.  These calls keep both on the device, so one whole
+ * step (flatten / accumulate with the fused norm, finalize, prepare, AdamW)
+ * can be captured once in a CUDA graph and replayed with no host work and
+ * no device-to-host read per step.  The results are bit-identical to the
+ * host-counter calls above.
+ * --------------------------------------------------------------------- */
+
+/* Device-resident step state of one optimizer (48 bytes, 8-byte aligned,
+ * in device memory).  Zero it before the first step; `step` may be set to
+ * resume from a checkpoint. */
+typedef struct zero_adamw_device_state {
+  int64_t step;     /* t: steps applied so far */
+  int32_t apply;    /* written by zero_adamw_prepare_device: 1 = the prepared step
+                       runs, 0 = it is skipped (non-finite norm or bad hparams) */
+  int32_t status;   /* ZERO_OK, or ZERO_EINVAL when the hyper-parameters read on
+                       the device were outside the ranges zero_adamw_step accepts */
+  float scalars[8]; /* step_size, sqrt(1-beta2^t), 1-lr*wd, beta1, 1-beta1, beta2,
+                       1-beta2, eps of the prepared step, each rounded once */
+} zero_adamw_device_state;
+
+/* zero_adamw_scalars -- host only.
+ * The per-step scalars zero_adamw_step uses for step t (>= 1), in the order
+ * of zero_adamw_device_state.scalars: bias corrections 1 - beta^t with
+ * beta^t by binary powering in double-double (the correctly rounded power
+ * but for near-ties), then lr / (1-beta1^t), sqrt(1-beta2^t), 1 - lr*wd in
+ * binary64, each rounded to binary32 once.  out: 8 floats, host memory.
+ * Errors: ZERO_EINVAL for NULL hp/out, step < 1, or hyper-parameters
+ * outside the ranges of zero_adamw_step. */
+zero_status zero_adamw_scalars(const zero_adamw_hparams* hp, int64_t step, float* out);
+
+/* zero_adamw_prepare_device -- device (one thread).
+ * The device half of the pages' skip policy and step counter: if d_clip is
+ * NULL or its `finite` is 1, and the hyper-parameters at d_hp (device
+ * memory, read when the kernel runs, so a schedule may rewrite them between
+ * replays) are valid, then step += 1, the scalars of that step are stored
+ * (the same bits zero_adamw_scalars gives) and apply = 1; otherwise apply =
+ * 0 and step is unchanged (status = ZERO_EINVAL for bad hyper-parameters).
+ * Errors (host): ZERO_EINVAL for NULL d_hp or d_state or a d_state that is
+ * not 8-byte aligned; ZERO_ECUDA for a failed launch. */
+zero_status zero_adamw_prepare_device(const zero_adamw_hparams* d_hp, const zero_norm_result* d_clip,
+                                      zero_adamw_device_state* d_state, void* stream);
+
+/* zero_adamw_step_device -- device.
+ * zero_adamw_step with the scalars and the skip decision taken from
+ * d_state, as the last zero_adamw_prepare_device on the stream left them:
+ * nothing changes when apply is 0.  d_clip supplies the clip coefficient as
+ * for zero_adamw_step (NULL: 1).
+ * Errors: those of zero_adamw_step without the hyper-parameter checks, plus
+ * NULL or misaligned d_state. */
+zero_status zero_adamw_step_device(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
+                                   const float* d_grad, void* d_param_lowp, zero_dtype lowp_dtype,
+                                   int64_t n, const zero_adamw_device_state* d_state,
+                                   const zero_norm_result* d_clip, void* stream);
+
+/* zero_adamw_step_tensors_device -- device.
+ * zero_adamw_step_tensors with the scalars and the skip decision from
+ * d_state, as zero_adamw_step_device. */
+zero_status zero_adamw_step_tensors_device(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
+                                           const zero_tensor* d_table, int32_t n_tensors, int64_t total,
+                                           zero_dtype grad_dtype, int64_t shard_start, float grad_scale,
+                                           void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
+                                           const zero_adamw_device_state* d_state,
+                                           const zero_norm_result* d_clip, void* stream);
 
 /* Static text for a status code. */
 const char* zero_status_string(zero_status status);

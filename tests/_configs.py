@@ -71,11 +71,14 @@ def _host_parts(tg: W.TensorGrads, numels, offsets, a: int, b: int, nulls):
 
 
 def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk: int = 1 << 26,
-                 seed: int = 0, fused: bool = True, direct: bool = False) -> RunReport:
+                 seed: int = 0, fused: bool = True, direct: bool = False, graph: bool = False) -> RunReport:
     """fused: the last micro-batch's flatten/accumulate also computes the grad
     norm's partials (the norm is then only finalized); otherwise the norm is a
     separate pass over the flat grad.  direct: one micro-batch of per-tensor
-    grads, stepped with step_tensors() (no fp32 grad buffer at all)."""
+    grads, stepped with step_tensors() (no fp32 grad buffer at all).  graph: a
+    capturable optimizer (step count and skip decision on the device); the
+    first step's grad passes and step are captured in one CUDA graph and every
+    step replays it over grads rewritten in place."""
     assert not direct or (wl.micro_batches == 1 and wl.mode != "zero3")
     from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
 
@@ -87,7 +90,7 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
     opt = FlatShardAdamW(wl.numels, world_size=wl.world_size, rank=wl.rank, lr=wl.lr, betas=wl.betas, eps=wl.eps,
                          weight_decay=wl.weight_decay, max_norm=wl.max_norm, lowp_dtype=lowp_dt,
                          grad_range="full" if wl.mode == "zero1" else "shard", device=DEV, master=master.clone(),
-                         grad_buffer=not direct)
+                         grad_buffer=not direct, capturable=graph)
     assert (opt.start, opt.end) == (s, e)
     if sample is None or sample >= n:
         idx = None
@@ -104,6 +107,18 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
     scale = 1.0 / M
     report = RunReport(wl.name, n)
     storages = [None] * M
+    captured = None
+
+    def enqueue(micro):
+        for j in range(M):
+            if wl.mode == "zero3":
+                opt.accum(micro[j], accumulate=j > 0, scale=scale, fuse_norm=fused and j == M - 1)
+            elif not direct:
+                opt.flatten(micro[j].tensors, accumulate=j > 0, scale=scale, fuse_norm=fused and j == M - 1)
+        if direct:
+            opt.launch_step_tensors(micro[0].tensors)
+        else:
+            opt.launch_step()
 
     for t in range(1, steps + 1):
         micro = []
@@ -111,15 +126,24 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
             if wl.mode == "zero3":
                 src = W.flat_grads(wl, t, j, s, e, device=DEV, out=storages[j])
                 storages[j] = src
-                opt.accum(src, accumulate=j > 0, scale=scale, fuse_norm=fused and j == M - 1)
                 micro.append(src)
             else:
                 tg = W.tensor_grads(wl, t, j, device=DEV, storage=storages[j])
                 storages[j] = tg.storage
-                if not direct:
-                    opt.flatten(tg.tensors, accumulate=j > 0, scale=scale, fuse_norm=fused and j == M - 1)
                 micro.append(tg)
-        res = opt.step_tensors(micro[0].tensors) if direct else opt.step()
+        if graph:
+            if captured is None:
+                if wl.mode != "zero3":
+                    for tg in micro:
+                        opt._table(tg.tensors)  # device tables built before capture (no copies inside it)
+                torch.cuda.synchronize()
+                captured = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(captured):
+                    enqueue(micro)
+            captured.replay()
+        else:
+            enqueue(micro)
+        res = opt.finish_step()
 
         # ---- oracle side: accumulate every element (chunked) for the norm
         sq_parts = []

@@ -136,6 +136,22 @@ def test_invalid_arguments_return_einval_before_any_launch(L):
                              zero_adamw_hparams(1e-3, .9, .999, 0.0, 0), zero_adamw_hparams(1e-3, .9, .999, 1e-8, -1),
                              zero_adamw_hparams(math.nan, .9, .999, 1e-8, 0)]):
         cases.append(L.zero_adamw_step(FAKE, FAKE, FAKE, FAKE, None, 1, 10, ctypes.byref(bad), 1, None, None))
+    # graph-capturable calls (device step state)
+    cases += [
+        L.zero_adamw_prepare_device(None, None, FAKE, None),                                   # NULL hp
+        L.zero_adamw_prepare_device(FAKE, None, None, None),                                   # NULL state
+        L.zero_adamw_prepare_device(FAKE, None, ctypes.c_void_p(0x1004), None),                # misaligned state
+        L.zero_adamw_step_device(FAKE, FAKE, FAKE, FAKE, None, 1, 10, None, None, None),       # NULL state
+        L.zero_adamw_step_device(FAKE, FAKE, FAKE, None, None, 1, 10, FAKE, None, None),       # NULL grad
+        L.zero_adamw_step_device(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 10, FAKE, None, None),       # F32 lowp
+        L.zero_adamw_step_device(FAKE, FAKE, FAKE, FAKE, None, 1, -1, FAKE, None, None),       # n < 0
+        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, None, 2, 10, 1, 0, 1.0, None, 1, 5, FAKE, None, None),
+        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 6, 1.0, None, 1, 5, FAKE, None, None),
+        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 0, 1.0, None, 1, 5, None, None, None),
+        L.zero_adamw_scalars(ctypes.byref(hp), 0, FAKE),                                       # step 0
+        L.zero_adamw_scalars(None, 1, FAKE),                                                   # NULL hp
+        L.zero_adamw_scalars(ctypes.byref(hp), 1, None),                                       # NULL out
+    ]
     assert cases == [1] * len(cases), [i for i, c in enumerate(cases) if c != 1]
     assert len(L.zero_last_error()) > 0
 
@@ -146,6 +162,22 @@ def test_empty_calls_are_noops_without_a_gpu(L):
     assert L.zero_flatten_cast(None, 0, 0, 1, 0, 0, 1.0, 0, None, None, None, 0, None) == 0
     assert L.zero_accum(None, None, 1, 0, 1.0, 0, None, None, 0, None) == 0
     assert L.zero_adamw_step(None, None, None, None, None, 1, 0, ctypes.byref(hp), 1, None, None) == 0
+
+
+def test_adamw_scalars_match_oracle(L):
+    """The per-step scalars (bias corrections by double-double binary powering, shared with
+    the device step state) equal the oracle's pow-based ones bit for bit over the first
+    100,000 steps and a sparse sweep to 10^7 steps, for every configuration's hyper-parameters
+    and a few more betas."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    hps = {(w.lr, w.betas[0], w.betas[1], w.eps, w.weight_decay) for w in (f() for f in W.ALL.values())}
+    hps |= {(1e-3, 0.8, 0.99, 1e-6, 0.01), (6e-4, 0.0, 0.98, 1e-8, 0.0), (2e-5, 0.99, 0.9999, 1e-12, 0.3)}
+    steps = list(range(1, 100_001)) + list(range(100_001, 10_000_000, 9973))
+    for hp in sorted(hps):
+        for t in steps:
+            got, ref = zs.zero_adamw_scalars(*hp, t), oracle.adamw_scalars(*hp, t)
+            if not np.array_equal(got.view(np.uint32), ref.view(np.uint32)):
+                raise AssertionError((hp, t, got, ref))
 
 
 def test_status_strings(L):
