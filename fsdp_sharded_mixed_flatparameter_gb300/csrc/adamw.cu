@@ -21,9 +21,10 @@
 namespace zs {
 
 template <int LOWP>
-__device__ __forceinline__ void adam_scalar(int64_t k, float* __restrict__ p, float* __restrict__ m,
+__device__ __forceinline__ void adam_scalar(int64_t k, int64_t n, float* __restrict__ p, float* __restrict__ m,
                                             float* __restrict__ v, const float* __restrict__ g,
                                             void* __restrict__ lowp, float coef, const AdamScalars& s) {
+  if (!ZS_CHECK(k >= 0 && k < n, 1, k)) return;
   float pk = p[k], mk = m[k], vk = v[k];
   adam_update(pk, mk, vk, g[k], coef, s);
   p[k] = pk;
@@ -53,11 +54,15 @@ __global__ void __launch_bounds__(256) adamw_v8_kernel(float* __restrict__ p, fl
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t body_end = head + 8 * nvec;
-  if (tid < head) adam_scalar<LOWP>(tid, p, m, v, g, lowp, coef, s);
-  if (tid < n - body_end) adam_scalar<LOWP>(body_end + tid, p, m, v, g, lowp, coef, s);
+  if (tid < head) adam_scalar<LOWP>(tid, n, p, m, v, g, lowp, coef, s);
+  if (tid < n - body_end) adam_scalar<LOWP>(body_end + tid, n, p, m, v, g, lowp, coef, s);
 
   for (int64_t i = tid; i < nvec; i += stride) {
     const int64_t k = head + 8 * i;
+    if (!ZS_CHECK(k >= 0 && k + 8 <= n && aligned(p + k, 32) && aligned(m + k, 32) && aligned(v + k, 32) &&
+                      aligned(g + k, 32) && (LOWP == 0 || aligned(static_cast<char*>(lowp) + 2 * k, LW)),
+                  2, k))
+      continue;
     float gr[8], pr[8], mr[8], vr[8];
     ld8_ro(g + k, gr);
     ld8_rw(p + k, pr);
@@ -108,7 +113,7 @@ __global__ void __launch_bounds__(256) adamw_scalar_kernel(float* __restrict__ p
   }
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n; k += stride)
-    adam_scalar<LOWP>(k, p, m, v, g, lowp, coef, s);
+    adam_scalar<LOWP>(k, n, p, m, v, g, lowp, coef, s);
 }
 
 template <int LOWP, int LW>
@@ -149,6 +154,8 @@ static zero_status launch_lowp(float* p, float* m, float* v, const float* g, voi
   if (la % 4 == 0) return launch_v8<LOWP, 4>(p, m, v, g, lowp, head, nvec, n, s, ds, clip, st);
   return launch_v8<LOWP, 2>(p, m, v, g, lowp, head, nvec, n, s, ds, clip, st);
 }
+
+ZS_DEBUG_UNIT(adamw)
 
 zero_status launch_adamw(float* p, float* m, float* v, const float* g, void* lowp, int lowp_dtype, int64_t n,
                          const AdamScalars& s, const zero_adamw_device_state* ds, const zero_norm_result* clip,

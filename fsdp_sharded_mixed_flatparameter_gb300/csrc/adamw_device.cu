@@ -46,6 +46,19 @@ __global__ void adamw_prepare_kernel(const zero_adamw_hparams* __restrict__ hp,
   state->apply = 1;
 }
 
+// One thread that records a violation on purpose without touching memory: the
+// debug build's self-test of its own reporting (release builds: a no-op).
+__global__ void debug_selftest_kernel(long long index) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) (void)ZS_CHECK(false, 999, index);
+}
+
+zero_status launch_debug_selftest(long long index, cudaStream_t st) {
+  debug_selftest_kernel<<<1, 32, 0, st>>>(index);
+  return check_launch("debug_selftest_kernel");
+}
+
+ZS_DEBUG_UNIT(adamw_device)
+
 zero_status launch_adamw_prepare(const zero_adamw_hparams* hp, const zero_norm_result* clip,
                                  zero_adamw_device_state* state, cudaStream_t st) {
   adamw_prepare_kernel<<<1, 32, 0, st>>>(hp, clip, state);

@@ -50,6 +50,11 @@ __global__ void __launch_bounds__(256) adamw_table_kernel(float* __restrict__ p,
                         f0 + kAtBlock <= toff + tnum && reinterpret_cast<uintptr_t>(tsrc) % vb == 0;
     if (direct) {
       const int64_t k = k0 + 8 * threadIdx.x;
+      if (!ZS_CHECK(k + 8 <= n && f0 - toff + 8 * threadIdx.x + 8 <= tnum && aligned(p + k, 32) &&
+                        aligned(m + k, 32) && aligned(v + k, 32) && aligned(tsrc + es * 8 * threadIdx.x, vb) &&
+                        (LOWP == 0 || aligned(static_cast<char*>(lowp) + 2 * k, LW)),
+                    10, k))
+        continue;
       float gr[8], pr[8], mr[8], vr[8];
       load8_src<DT>(tsrc + es * 8 * threadIdx.x, gr);
       ld8_rw(p + k, pr);
@@ -86,6 +91,7 @@ __global__ void __launch_bounds__(256) adamw_table_kernel(float* __restrict__ p,
       __syncthreads();
       for (int q = threadIdx.x; q < blen; q += blockDim.x) {
         const int64_t k = k0 + q;
+        if (!ZS_CHECK(k < n && q < kAtBlock, 11, k)) continue;
         float pk = p[k], mk = m[k], vk = v[k];
         adam_update(pk, mk, vk, stage[stage_idx(q)], coef, s);
         p[k] = pk;
@@ -97,6 +103,8 @@ __global__ void __launch_bounds__(256) adamw_table_kernel(float* __restrict__ p,
     }
   }
 }
+
+ZS_DEBUG_UNIT(adamw_table)
 
 template <int DT, int LOWP, int LW>
 static zero_status launch_table_t(float* p, float* m, float* v, const zero_tensor* table, int n_tensors,

@@ -268,6 +268,46 @@ zero_status zero_adamw_step_tensors(float* d_master, float* d_exp_avg, float* d_
                                 grad_scale, d_param_lowp, lowp_dtype, n, s, nullptr, d_clip, zs::as_stream(stream));
 }
 
+// ------------------------------------------------------------- debug builds
+zero_status zero_debug_errors(uint64_t* out, int32_t reset) {
+  if (out == nullptr) return fail(ZERO_EINVAL, "zero_debug_errors: NULL out");
+#ifdef ZERO_DEBUG
+  zero_status (*const readers[])(unsigned long long*, bool) = {zs::debug_read_adamw, zs::debug_read_adamw_table,
+                                                                 zs::debug_read_adamw_device, zs::debug_read_flatten,
+                                                                 zs::debug_read_sqnorm};
+  uint64_t total = 0, first[3] = {0, 0, 0};
+  for (auto rd : readers) {
+    unsigned long long r[4];
+    const zero_status st = rd(r, reset != 0);
+    if (st != ZERO_OK) return st;
+    if (r[0] != 0 && total == 0) {
+      first[0] = r[1];
+      first[1] = r[2];
+      first[2] = r[3];
+    }
+    total += r[0];
+  }
+  out[0] = total;
+  out[1] = first[0];
+  out[2] = first[1];
+  out[3] = first[2];
+  return ZERO_OK;
+#else
+  (void)reset;
+  return fail(ZERO_EINVAL, "zero_debug_errors: this library was built without ZERO_DEBUG");
+#endif
+}
+
+zero_status zero_debug_selftest(int64_t index, void* stream) {
+#ifdef ZERO_DEBUG
+  return zs::launch_debug_selftest(index, zs::as_stream(stream));
+#else
+  (void)index;
+  (void)stream;
+  return fail(ZERO_EINVAL, "zero_debug_selftest: this library was built without ZERO_DEBUG");
+#endif
+}
+
 // ------------------------------------------------------------- graph-capturable steps
 static zero_status check_state(const char* who, const void* d_state) {
   if (d_state == nullptr) return fail(ZERO_EINVAL, "%s: NULL d_state", who);

@@ -37,7 +37,47 @@ inline unsigned one_pass_blocks(int64_t units, int64_t per_block) {
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
-inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+// ----------------------------------------------------------- debug builds
+// Built with -DZERO_DEBUG (libzeroshard_debug.so), every global-memory access
+// site first checks its index against the extent it must stay in and its
+// address against the alignment its vector width needs: ZS_CHECK(cond,
+// site, index) is true when the access is valid; otherwise it counts the
+// violation, records the first one (site, index, block) and is false, and
+// the caller skips the access -- so a bad index is reported instead of
+// faulting.  This stands in for a memory checker on GPUs where none runs.
+// Device globals are per translation unit (no relocatable device code), so
+// each unit defines its record and a host reader with ZS_DEBUG_UNIT(name).
+// Release builds compile every check to `true`.
+#ifdef ZERO_DEBUG
+static __device__ unsigned long long g_zs_debug[4];  // count, first site, first index, first block
+static __device__ __noinline__ bool debug_fail(int site, long long index) {
+  if (atomicAdd(&g_zs_debug[0], 1ull) == 0ull) {
+    g_zs_debug[1] = static_cast<unsigned long long>(site);
+    g_zs_debug[2] = static_cast<unsigned long long>(index);
+    g_zs_debug[3] = blockIdx.x;
+  }
+  return false;
+}
+#define ZS_CHECK(cond, site, index) ((cond) || ::zs::debug_fail((site), static_cast<long long>(index)))
+#define ZS_DEBUG_UNIT(name)                                                                        \
+  zero_status debug_read_##name(unsigned long long* out, bool reset) {                             \
+    if (cudaMemcpyFromSymbol(out, g_zs_debug, sizeof(g_zs_debug)) != cudaSuccess)                  \
+      return check_launch("debug record of " #name);                                               \
+    if (reset) {                                                                                    \
+      const unsigned long long z[4] = {0ull, 0ull, 0ull, 0ull};                                     \
+      if (cudaMemcpyToSymbol(g_zs_debug, z, sizeof(z)) != cudaSuccess)                              \
+        return check_launch("debug record of " #name);                                             \
+    }                                                                                               \
+    return ZERO_OK;                                                                                 \
+  }
+#else
+#define ZS_CHECK(cond, site, index) true
+#define ZS_DEBUG_UNIT(name)
+#endif
+
+__host__ __device__ inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
 
 // ------------------------------------------------------ streaming loads
 // 32-byte loads/stores (8 x binary32 in one instruction, sm_100+) with

@@ -98,6 +98,10 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
 
       const bool direct = tlen == kFlTile && (dst_vec || !WRITE) && tsrc != nullptr && toff <= klo &&
                           khi <= toff + tnum && reinterpret_cast<uintptr_t>(tsrc) % vb == 0;
+      if (!ZS_CHECK(!direct || (klo - toff + kFlTile <= tnum && aligned(tsrc, vb) &&
+                                (!WRITE || aligned(dst + base, 32)) && base + kFlTile <= len),
+                    20, tile))
+        continue;
       if (EXACT && direct) {
         // 1024 groups of 8 (16 bytes of source each); thread t takes groups t + 256 r, loads first
         uint4 w[4];
@@ -148,6 +152,7 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
       for (int u = threadIdx.x; u < ngroups; u += kFlThreads) {
         float y[8];
         const int64_t d = base + 8 * u;
+        if (!ZS_CHECK(d < len && (!WRITE || !dst_vec || 8 * u + 8 > tlen || aligned(dst + d, 32)), 21, d)) continue;
         if ((dst_vec || !WRITE) && 8 * u + 8 <= tlen) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) y[i] = stage[stage_idx(8 * u + i)];
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
     }
     if (NORM) {
       const double bs = block_sum_norm<kFlThreads>(nacc, red);
-      if (threadIdx.x == 0) partials[wb] = bs;
+      if (threadIdx.x == 0 && ZS_CHECK(wb < nblocks_work, 22, wb)) partials[wb] = bs;
     }
   }
   if (EXACT) {
@@ -248,8 +253,9 @@ zero_status launch_flatten(const zero_tensor* table, int32_t n_tensors, int src_
 // acc[k] = (ACC ? acc[k] : 0-free) + fl(scale * x[k]); groups of 8 with one
 // 32-byte accumulator load/store and one 16/32-byte source load.
 template <int DT, bool ACC>
-__device__ __forceinline__ void accum_scalar(int64_t k, float* __restrict__ acc, const void* __restrict__ src,
-                                             float scale, bool& bad) {
+__device__ __forceinline__ void accum_scalar(int64_t k, int64_t n, float* __restrict__ acc,
+                                             const void* __restrict__ src, float scale, bool& bad) {
+  if (!ZS_CHECK(k >= 0 && k < n, 23, k)) return;
   const float y = __fmul_rn(scale, load_elem<DT>(src, k));
   bad |= !finite_f(y);
   acc[k] = ACC ? __fadd_rn(acc[k], y) : y;
@@ -264,11 +270,13 @@ __global__ void __launch_bounds__(256) accum_kernel(float* __restrict__ acc, con
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t body_end = head + 8 * nvec;
   bool bad = false;
-  if (tid < head) accum_scalar<DT, ACC>(tid, acc, src, scale, bad);
-  if (tid < n - body_end) accum_scalar<DT, ACC>(body_end + tid, acc, src, scale, bad);
+  if (tid < head) accum_scalar<DT, ACC>(tid, n, acc, src, scale, bad);
+  if (tid < n - body_end) accum_scalar<DT, ACC>(body_end + tid, n, acc, src, scale, bad);
   const char* s8 = static_cast<const char*>(src);
   for (int64_t i = tid; i < nvec; i += stride) {
     const int64_t k = head + 8 * i;
+    if (!ZS_CHECK(k + 8 <= n && aligned(acc + k, 32) && aligned(s8 + es * k, DT == ZERO_F32 ? 32 : 16), 24, k))
+      continue;
     float x[8], a[8];
     load8_src<DT>(s8 + es * k, x);
     if (ACC) ld8_rw(acc + k, a);
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(256) accum_scalar_kernel(float* __restrict__ a
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   bool bad = false;
   for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n; k += stride)
-    accum_scalar<DT, ACC>(k, acc, src, scale, bad);
+    accum_scalar<DT, ACC>(k, n, acc, src, scale, bad);
   if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
 }
 
@@ -318,6 +326,8 @@ __global__ void __launch_bounds__(kSqThreads) accum_norm_kernel(float* __restric
       for (int q = 0; q < 4; ++q) {
         const int64_t k = base + (static_cast<int64_t>(r0 + q) * kSqThreads + threadIdx.x) * 8;
         full[q] = vec && k + 8 <= n;
+        if (full[q] && !ZS_CHECK(aligned(acc + k, 32) && aligned(s8 + es * k, DT == ZERO_F32 ? 32 : 16), 25, k))
+          full[q] = false;  // (debug build) treated as a ragged group: element accesses only
         if (full[q]) {
           load8_src<DT>(s8 + es * k, x[q]);
           if (ACC) ld8_rw(acc + k, a[q]);
@@ -347,10 +357,12 @@ __global__ void __launch_bounds__(kSqThreads) accum_norm_kernel(float* __restric
       }
     }
     const double bs = block_sum_norm<kSqThreads>(nacc, red);
-    if (threadIdx.x == 0) partials[tile] = bs;
+    if (threadIdx.x == 0 && ZS_CHECK(tile < ntiles, 26, tile)) partials[tile] = bs;
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
 }
+
+ZS_DEBUG_UNIT(flatten)
 
 template <int DT, bool ACC>
 static zero_status launch_accum_t(float* acc, const void* src, int64_t n, float scale, int32_t* flag,

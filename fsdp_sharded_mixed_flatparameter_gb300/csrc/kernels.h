@@ -37,6 +37,15 @@ zero_status launch_adamw_table(float* p, float* m, float* v, const zero_tensor* 
                                const AdamScalars& s, const zero_adamw_device_state* ds,
                                const zero_norm_result* clip, cudaStream_t st);
 
+// Debug builds (ZERO_DEBUG): each translation unit's violation record
+// {count, first site, first index, first block}; reset clears it.
+zero_status debug_read_adamw(unsigned long long* out, bool reset);
+zero_status debug_read_adamw_table(unsigned long long* out, bool reset);
+zero_status debug_read_adamw_device(unsigned long long* out, bool reset);
+zero_status debug_read_flatten(unsigned long long* out, bool reset);
+zero_status debug_read_sqnorm(unsigned long long* out, bool reset);
+zero_status launch_debug_selftest(long long index, cudaStream_t st);
+
 // One thread: advance the device step state (see zero_adamw_prepare_device).
 zero_status launch_adamw_prepare(const zero_adamw_hparams* hp, const zero_norm_result* clip,
                                  zero_adamw_device_state* state, cudaStream_t st);

@@ -57,7 +57,12 @@ __device__ __forceinline__ NormAcc thread_tile_sum(const float* __restrict__ g, 
     for (int r = 0; r < 8; ++r) {
       const int64_t e = base + ((static_cast<int64_t>(round * 8 + r) * kSqThreads) + threadIdx.x) * 8;
       if (VEC) {
-        ld8_ro(g + e, x[r]);
+        if (ZS_CHECK(e + 8 <= n && aligned(g + e, 32), 30, e)) {
+          ld8_ro(g + e, x[r]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[r][i] = 0.0f;
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) x[r][i] = (e + i < n) ? __ldg(g + e + i) : 0.0f;
@@ -78,7 +83,7 @@ __global__ void __launch_bounds__(kSqThreads) sqnorm_tiles_kernel(const float* _
     const NormAcc ts = (vec_ok && base + kSqTile <= n) ? thread_tile_sum<true>(g, base, n)
                                                        : thread_tile_sum<false>(g, base, n);
     const double bs = block_sum_norm<kSqThreads>(ts, red);
-    if (threadIdx.x == 0) partials[tile] = bs;
+    if (threadIdx.x == 0 && ZS_CHECK(tile < ntiles, 31, tile)) partials[tile] = bs;
   }
 }
 
@@ -122,6 +127,8 @@ __global__ void sqnorm_combine_kernel(const double* __restrict__ sq, int n_parts
   r.finite = isfinite(norm) ? 1 : 0;
   *out = r;
 }
+
+ZS_DEBUG_UNIT(sqnorm)
 
 zero_status launch_sqnorm_combine(const double* sq, int n_parts, double max_norm, zero_norm_result* out,
                                   cudaStream_t st) {

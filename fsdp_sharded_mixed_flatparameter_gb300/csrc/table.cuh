@@ -56,10 +56,12 @@ __device__ __forceinline__ void load8_src(const void* p, float (&x)[8]) {
   }
 }
 
-// Write fl(scale * x) of source elements [j0, j0 + len) into stage[q0 ...).
+// Write fl(scale * x) of source elements [j0, j0 + len) into stage[q0 ...);
+// qcap: the staged tile's length (q0 + len <= qcap).
 template <int DT>
-__device__ __forceinline__ void stage_segment(const void* __restrict__ src, int64_t j0, int len, int q0,
+__device__ __forceinline__ void stage_segment(const void* __restrict__ src, int64_t j0, int len, int q0, int qcap,
                                               float scale, float* stage, bool& bad) {
+  if (!ZS_CHECK(q0 >= 0 && len >= 0 && q0 + len <= qcap && j0 >= 0, 40, q0)) return;
   if (src == nullptr) {
     const float y = __fmul_rn(scale, 0.0f);
     for (int e = threadIdx.x; e < len; e += kFlThreads) stage[stage_idx(q0 + e)] = y;
@@ -80,6 +82,7 @@ __device__ __forceinline__ void stage_segment(const void* __restrict__ src, int6
   // body: four source vectors in flight per thread (loads first), then one at a time
   int vi = threadIdx.x;
   for (; vi + 3 * kFlThreads < nv; vi += 4 * kFlThreads) {
+    if (!ZS_CHECK(aligned(sp + es * (h + 8 * vi), vb) && h + 8 * (vi + 3 * kFlThreads) + 8 <= len, 41, vi)) continue;
     float x[4][8];
 #pragma unroll
     for (int u = 0; u < 4; ++u) load8_src<DT>(sp + es * (h + 8 * (vi + u * kFlThreads)), x[u]);
@@ -95,6 +98,7 @@ __device__ __forceinline__ void stage_segment(const void* __restrict__ src, int6
     }
   }
   for (; vi < nv; vi += kFlThreads) {
+    if (!ZS_CHECK(aligned(sp + es * (h + 8 * vi), vb) && h + 8 * vi + 8 <= len, 42, vi)) continue;
     float x[8];
     load8_src<DT>(sp + es * (h + 8 * vi), x);
     const int q = q0 + h + 8 * vi;
@@ -125,8 +129,8 @@ __device__ __forceinline__ void stage_range(const zero_tensor* __restrict__ tabl
     const int64_t off = __ldg(&table[j].flat_offset), num = __ldg(&table[j].numel);
     const int64_t seg_end = (off + num < khi) ? off + num : khi;
     if (seg_end > k) {
-      stage_segment<DT>(table[j].ptr, k - off, static_cast<int>(seg_end - k), static_cast<int>(k - klo), scale,
-                        stage, bad);
+      stage_segment<DT>(table[j].ptr, k - off, static_cast<int>(seg_end - k), static_cast<int>(k - klo),
+                        static_cast<int>(khi - klo), scale, stage, bad);
       k = seg_end;
     }
     ++j;

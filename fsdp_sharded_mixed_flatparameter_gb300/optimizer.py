@@ -108,7 +108,9 @@ class FlatShardAdamW:
 
     # ---------------------------------------------------------------- grads
     def _table(self, grads: Sequence[Optional[torch.Tensor]]) -> torch.Tensor:
-        key = tuple(0 if g is None else g.data_ptr() for g in grads)
+        # keyed by address, size and contiguity, so a cached table is only reused for
+        # grads that passed the checks below when it was built
+        key = tuple(None if g is None else (g.data_ptr(), g.numel(), g.is_contiguous()) for g in grads)
         hit = self._tables.get(key)
         if hit is None:
             if len(grads) != len(self.numels):

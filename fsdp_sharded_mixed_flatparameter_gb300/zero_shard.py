@@ -57,8 +57,13 @@ TENSOR_ENTRY_BYTES = ctypes.sizeof(zero_tensor)
 _lib = None
 
 
+def debug_build_selected() -> bool:
+    """ZERO_SHARD_DEBUG=1 selects the self-checking debug library (built with -DZERO_DEBUG)."""
+    return os.environ.get("ZERO_SHARD_DEBUG", "") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.DEBUG_LIB if debug_build_selected() else _build.LIB
 
 
 def lib() -> ctypes.CDLL:
@@ -88,6 +93,8 @@ def lib() -> ctypes.CDLL:
                                           ctypes.POINTER(zero_adamw_hparams), i64, vp, vp]
     L.zero_loss_scale_update.argtypes = [ctypes.POINTER(f32), ctypes.POINTER(i32), i32, f64, f64, i32]
     L.zero_adamw_scalars.argtypes = [ctypes.POINTER(zero_adamw_hparams), i64, vp]
+    L.zero_debug_errors.argtypes = [vp, i32]
+    L.zero_debug_selftest.argtypes = [i64, vp]
     L.zero_adamw_prepare_device.argtypes = [vp, vp, vp, vp]
     L.zero_adamw_step_device.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, i64, vp, vp, vp]
     L.zero_adamw_step_tensors_device.argtypes = [vp, vp, vp, vp, i32, i64, ctypes.c_int, i64, f32, vp, ctypes.c_int,
@@ -99,7 +106,8 @@ def lib() -> ctypes.CDLL:
     for nm in ("zero_shard_range", "zero_tensor_table", "zero_flatten_cast", "zero_accum", "zero_grad_sqnorm",
                "zero_grad_sqnorm_finalize", "zero_grad_sqnorm_combine", "zero_grad_sqnorm_noalloc",
                "zero_adamw_step", "zero_adamw_step_tensors", "zero_loss_scale_update", "zero_adamw_scalars",
-               "zero_adamw_prepare_device", "zero_adamw_step_device", "zero_adamw_step_tensors_device"):
+               "zero_adamw_prepare_device", "zero_adamw_step_device", "zero_adamw_step_tensors_device",
+               "zero_debug_errors", "zero_debug_selftest"):
         getattr(L, nm).restype = ctypes.c_int
     _lib = L
     return L
@@ -412,6 +420,25 @@ def zero_adamw_step_tensors_device(master: torch.Tensor, exp_avg: torch.Tensor, 
         _dev(exp_avg_sq, "exp_avg_sq", torch.float32), _dev(d_table, "d_table", torch.uint8, allow_none=n_tensors == 0),
         n_tensors, total, _DT[grad_dtype], shard_start, grad_scale, lp, lowp_dt, n, _state_arg(state),
         _dev(clip, "clip", allow_none=True), _stream(stream)))
+
+
+# ------------------------------------------------------------ debug builds
+class DebugRecord(NamedTuple):
+    count: int
+    site: int
+    index: int
+    block: int
+
+
+def zero_debug_errors(reset: bool = False) -> DebugRecord:
+    """Access-check violations the debug library recorded (ZeroError on a release library)."""
+    out = np.zeros(4, dtype=np.uint64)
+    _check(lib().zero_debug_errors(ctypes.c_void_p(out.ctypes.data), int(bool(reset))))
+    return DebugRecord(*(int(x) for x in out))
+
+
+def zero_debug_selftest(index: int, stream=None) -> None:
+    _check(lib().zero_debug_selftest(index, _stream(stream)))
 
 
 # ------------------------------------------------------------ norm result I/O

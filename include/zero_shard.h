@@ -401,6 +401,26 @@ zero_status zero_adamw_step_tensors_device(float* d_master, float* d_exp_avg, fl
                                            const zero_adamw_device_state* d_state,
                                            const zero_norm_result* d_clip, void* stream);
 
+/* ---------------------------------------------------------------------
+ * Debug builds.  No counterpart on the source pages.  Built with
+ * -DZERO_DEBUG (libzeroshard_debug.so), every kernel checks each global-
+ * memory access site's index against the extent it must stay in and its
+ * address against the alignment of its vector width before the access; a
+ * violation is counted, the first one recorded, and the access skipped
+ * (reported instead of faulting).  Release builds compile the checks away
+ * and these two calls return ZERO_EINVAL.
+ * --------------------------------------------------------------------- */
+
+/* zero_debug_errors -- host (synchronises the device).
+ * out[0] = violations since the last reset, out[1..3] = site, index and
+ * block of the first one (0 when none); reset != 0 clears the record. */
+zero_status zero_debug_errors(uint64_t* out, int32_t reset);
+
+/* zero_debug_selftest -- device.
+ * Records one violation at site 999 with the given index, touching no
+ * memory: checks the reporting path of a debug build. */
+zero_status zero_debug_selftest(int64_t index, void* stream);
+
 /* Static text for a status code. */
 const char* zero_status_string(zero_status status);
 

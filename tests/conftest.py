@@ -26,3 +26,14 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _no_debug_violations(request):
+    """Under the self-checking debug library (ZERO_SHARD_DEBUG=1) every GPU test must
+    leave no recorded access violation (index out of its extent or misaligned vector)."""
+    yield
+    if os.environ.get("ZERO_SHARD_DEBUG") == "1" and "gpu" in request.keywords:
+        from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+        rec = zs.zero_debug_errors(reset=True)
+        assert rec.count == 0, f"debug build recorded access violations: {rec}"

@@ -208,3 +208,24 @@ def test_registered_grads_match_passed_grads():
     assert a.step_tensors(tg.tensors) == b.step_tensors()
     for name in ("master", "exp_avg", "exp_avg_sq", "lowp"):
         assert torch.equal(getattr(a, name).view(torch.uint8), getattr(b, name).view(torch.uint8))
+
+
+def test_cached_table_is_not_reused_for_other_sizes():
+    """The optimizer's device tables are cached by grad address; a later list with a
+    tensor at the same address but a different size or layout is checked again (and
+    refused) instead of hitting the cache."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
+    dev = torch.device("cuda:0")
+    numels = [1000, 3000, 24]
+    opt = FlatShardAdamW(numels, device=dev)
+    grads = [torch.randn(n, device=dev).to(torch.bfloat16) for n in numels]
+    opt.flatten(grads, accumulate=False)
+    short = list(grads)
+    short[1] = grads[1][:2999]            # same address, one element short
+    with pytest.raises(ValueError):
+        opt.flatten(short, accumulate=False)
+    square = torch.randn(40, 25, device=dev).to(torch.bfloat16)
+    opt2 = FlatShardAdamW([1000], device=dev)
+    opt2.flatten([square.view(-1)], accumulate=False)
+    with pytest.raises(ValueError):        # same address and size, not contiguous
+        opt2.flatten([square.t()], accumulate=False)
