@@ -19,13 +19,53 @@ namespace zs {
 // the state with coalesced scalar accesses.
 constexpr int kAtBlock = 2048;
 
+// Stores of one group of 8 updated parameters (thread t: elements k .. k+7):
+// the fp32 state and the packed low-precision copy.
+template <int LOWP, int LW>
+__device__ __forceinline__ void store_group(float* __restrict__ p, float* __restrict__ m, float* __restrict__ v,
+                                            void* __restrict__ lowp, int64_t k, const float (&pr)[8],
+                                            const float (&mr)[8], const float (&vr)[8]) {
+  st8(p + k, pr);
+  st8(m + k, mr);
+  st8(v + k, vr);
+  if (LOWP != 0) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = pack2_rn<LOWP>(pr[2 * j], pr[2 * j + 1]);
+    char* dst = static_cast<char*>(lowp) + 2 * k;
+    if (LW == 16) {
+      st16(dst, make_uint4(w[0], w[1], w[2], w[3]));
+    } else if (LW == 8) {
+      reinterpret_cast<uint2*>(dst)[0] = make_uint2(w[0], w[1]);
+      reinterpret_cast<uint2*>(dst)[1] = make_uint2(w[2], w[3]);
+    } else if (LW == 4) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) reinterpret_cast<uint32_t*>(dst)[j] = w[j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        reinterpret_cast<unsigned short*>(dst)[2 * j] = static_cast<unsigned short>(w[j] & 0xffffu);
+        reinterpret_cast<unsigned short*>(dst)[2 * j + 1] = static_cast<unsigned short>(w[j] >> 16);
+      }
+    }
+  }
+}
+
+// A full block (2048 elements, state 32-byte aligned): thread t owns the
+// group of elements k0 + 8t .. k0 + 8t + 7.  Its state loads do not depend
+// on the tensor table, so they are issued first and the table lookup's
+// dependent loads run while they are in flight; the grads then come straight
+// from the tensor (inside one co-aligned tensor) or from the block's staged
+// copy in shared memory.  A partial last block or unaligned state goes
+// element by element through the staged copy.
 template <int DT, int LOWP, int LW, bool DEVS>
-__global__ void __launch_bounds__(256) adamw_table_kernel(float* __restrict__ p, float* __restrict__ m,
-                                                          float* __restrict__ v, const zero_tensor* __restrict__ table,
-                                                          int n_tensors, int64_t shard_start, int64_t n, float gscale,
-                                                          void* __restrict__ lowp, bool state_vec, AdamScalars hs,
-                                                          const zero_adamw_device_state* __restrict__ ds,
-                                                          const zero_norm_result* __restrict__ clip) {
+__global__ void __launch_bounds__(256, 4) adamw_table_kernel(float* __restrict__ p, float* __restrict__ m,
+                                                             float* __restrict__ v,
+                                                             const zero_tensor* __restrict__ table, int n_tensors,
+                                                             int64_t shard_start, int64_t n, float gscale,
+                                                             void* __restrict__ lowp, bool state_vec, AdamScalars hs,
+                                                             const zero_adamw_device_state* __restrict__ ds,
+                                                             const zero_norm_result* __restrict__ clip) {
   __shared__ float stage[kAtBlock + kAtBlock / 8];
   AdamScalars s;
   if (!step_scalars<DEVS>(hs, ds, s)) return;  // the prepared step is skipped
@@ -42,62 +82,56 @@ __global__ void __launch_bounds__(256) adamw_table_kernel(float* __restrict__ p,
     const int64_t k0 = b * kAtBlock;
     const int blen = static_cast<int>((n - k0 < kAtBlock) ? (n - k0) : kAtBlock);
     const int64_t f0 = shard_start + k0;
+    const bool full = state_vec && blen == kAtBlock;  // block-uniform
+    const int64_t k = k0 + 8 * threadIdx.x;
+    float pr[8], mr[8], vr[8];
+    bool ok = full && ZS_CHECK(k + 8 <= n && aligned(p + k, 32) && aligned(m + k, 32) && aligned(v + k, 32), 10, k);
+    if (ok) {
+      ld8_rw(p + k, pr);
+      ld8_rw(m + k, mr);
+      ld8_rw(v + k, vr);
+    }
     const int ti = find_tensor(table, n_tensors, f0);
     const void* tptr = table[ti].ptr;
     const int64_t toff = __ldg(&table[ti].flat_offset), tnum = __ldg(&table[ti].numel);
     const char* tsrc = tptr ? static_cast<const char*>(tptr) + es * (f0 - toff) : nullptr;
-    const bool direct = state_vec && blen == kAtBlock && tsrc != nullptr && toff <= f0 &&
-                        f0 + kAtBlock <= toff + tnum && reinterpret_cast<uintptr_t>(tsrc) % vb == 0;
-    if (direct) {
-      const int64_t k = k0 + 8 * threadIdx.x;
-      if (!ZS_CHECK(k + 8 <= n && f0 - toff + 8 * threadIdx.x + 8 <= tnum && aligned(p + k, 32) &&
-                        aligned(m + k, 32) && aligned(v + k, 32) && aligned(tsrc + es * 8 * threadIdx.x, vb) &&
-                        (LOWP == 0 || aligned(static_cast<char*>(lowp) + 2 * k, LW)),
-                    10, k))
-        continue;
-      float gr[8], pr[8], mr[8], vr[8];
-      load8_src<DT>(tsrc + es * 8 * threadIdx.x, gr);
-      ld8_rw(p + k, pr);
-      ld8_rw(m + k, mr);
-      ld8_rw(v + k, vr);
+    const bool direct = full && tsrc != nullptr && toff <= f0 && f0 + kAtBlock <= toff + tnum &&
+                        reinterpret_cast<uintptr_t>(tsrc) % vb == 0;  // block-uniform
+    if (full) {
+      float gr[8];
+      if (direct) {
+        ok = ok && ZS_CHECK(f0 - toff + 8 * threadIdx.x + 8 <= tnum && aligned(tsrc + es * 8 * threadIdx.x, vb) &&
+                                (LOWP == 0 || aligned(static_cast<char*>(lowp) + 2 * k, LW)),
+                            11, k);
+        if (ok) {
+          load8_src<DT>(tsrc + es * 8 * threadIdx.x, gr);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) adam_update(pr[j], mr[j], vr[j], __fmul_rn(gscale, gr[j]), coef, s);
-      st8(p + k, pr);
-      st8(m + k, mr);
-      st8(v + k, vr);
-      if (LOWP != 0) {
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) w[j] = pack2_rn<LOWP>(pr[2 * j], pr[2 * j + 1]);
-        char* dst = static_cast<char*>(lowp) + 2 * k;
-        if (LW == 16) {
-          st16(dst, make_uint4(w[0], w[1], w[2], w[3]));
-        } else if (LW == 8) {
-          reinterpret_cast<uint2*>(dst)[0] = make_uint2(w[0], w[1]);
-          reinterpret_cast<uint2*>(dst)[1] = make_uint2(w[2], w[3]);
-        } else if (LW == 4) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) reinterpret_cast<uint32_t*>(dst)[j] = w[j];
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            reinterpret_cast<unsigned short*>(dst)[2 * j] = static_cast<unsigned short>(w[j] & 0xffffu);
-            reinterpret_cast<unsigned short*>(dst)[2 * j + 1] = static_cast<unsigned short>(w[j] >> 16);
-          }
+          for (int j = 0; j < 8; ++j) gr[j] = __fmul_rn(gscale, gr[j]);
         }
+      } else {
+        stage_range<DT>(table, n_tensors, ti, f0, f0 + kAtBlock, gscale, stage, bad);
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) gr[j] = stage[stage_idx(8 * threadIdx.x + j)];  // stride 9: no bank conflict
+        __syncthreads();  // the stage is refilled by the next block
+      }
+      if (ok) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) adam_update(pr[j], mr[j], vr[j], gr[j], coef, s);
+        store_group<LOWP, LW>(p, m, v, lowp, k, pr, mr, vr);
       }
     } else {
       stage_range<DT>(table, n_tensors, ti, f0, f0 + blen, gscale, stage, bad);
       __syncthreads();
       for (int q = threadIdx.x; q < blen; q += blockDim.x) {
-        const int64_t k = k0 + q;
-        if (!ZS_CHECK(k < n && q < kAtBlock, 11, k)) continue;
-        float pk = p[k], mk = m[k], vk = v[k];
+        const int64_t kq = k0 + q;
+        if (!ZS_CHECK(kq < n && q < kAtBlock, 12, kq)) continue;
+        float pk = p[kq], mk = m[kq], vk = v[kq];
         adam_update(pk, mk, vk, stage[stage_idx(q)], coef, s);
-        p[k] = pk;
-        m[k] = mk;
-        v[k] = vk;
-        if (LOWP != 0) static_cast<unsigned short*>(lowp)[k] = round1_rn<LOWP>(pk);
+        p[kq] = pk;
+        m[kq] = mk;
+        v[kq] = vk;
+        if (LOWP != 0) static_cast<unsigned short*>(lowp)[kq] = round1_rn<LOWP>(pk);
       }
       __syncthreads();
     }
