@@ -16,9 +16,9 @@
 //     block per tile (the grid loop
 //     only covers grids beyond the hardware limit), so the partial of a tile
 //     does not depend on which block computed it or how many blocks ran.
-//  2. sqnorm_finalize_kernel: one block adds the partials in a fixed order
-//     (binary64), adds the other ranks' share, takes the square root and the
-//     clip coefficient, and writes the zero_norm_result.
+//  2. sqnorm_finalize_kernel: a cluster of 8 blocks adds the partials in a
+//     fixed order (binary64), adds the other ranks' share, takes the square
+//     root and the clip coefficient, and writes the zero_norm_result.
 //
 // Accuracy: the double-float sums carry about 48 significant bits, so the
 // relative error of the sum of squares is ~1e-14 (binary64 beyond the
@@ -34,6 +34,8 @@
 // non-finite norm, |g| < 2^-75 underflows toward 0) are where the result can
 // differ from the binary64 oracle; gradients never come near either.
 // No atomics: the result is bit-identical from run to run and GPU to GPU.
+#include <cooperative_groups.h>
+
 #include <cmath>
 #include <mutex>
 
@@ -42,6 +44,8 @@
 #include "reduce.cuh"
 
 namespace zs {
+
+namespace cg = cooperative_groups;
 
 
 // Element e of a tile belongs to thread t, vector slot r, lane i where
@@ -88,26 +92,44 @@ __global__ void __launch_bounds__(kSqThreads) sqnorm_tiles_kernel(const float* _
 }
 
 constexpr int kFinThreads = 1024;
+constexpr int kFinCluster = 8;  // blocks of the finalize (a portable cluster size)
 
-__global__ void __launch_bounds__(kFinThreads) sqnorm_finalize_kernel(const double* __restrict__ partials,
-                                                                      int64_t ntiles, double extra_sqnorm,
-                                                                      double max_norm,
-                                                                      zero_norm_result* __restrict__ out) {
+// The finalize over the tile partials runs as one thread-block cluster of 8
+// blocks on 8 SMs: binary64 runs at a small fraction of the binary32 rate on
+// GB300, and one SM's binary64 pipe alone took ~66 us for Llama-7B's 205,641
+// partials.  Block r adds the contiguous chunk r of the partials (thread
+// stride, then block_sum); after the cluster barrier block 0 reads the 8
+// block totals from the other blocks' shared memory (distributed shared
+// memory) in rank order and writes the result; a second barrier keeps every
+// block's shared memory alive until then.  The order depends on ntiles only.
+__global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThreads)
+    sqnorm_finalize_kernel(const double* __restrict__ partials, int64_t ntiles, double extra_sqnorm,
+                           double max_norm, zero_norm_result* __restrict__ out) {
   __shared__ double red[kFinThreads / 32];
+  __shared__ double block_total;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int64_t r = cluster.block_rank();
+  const int64_t chunk = (ntiles + kFinCluster - 1) / kFinCluster;
+  const int64_t lo = r * chunk, hi = (lo + chunk < ntiles) ? lo + chunk : ntiles;
   double acc = 0.0;
-  for (int64_t j = threadIdx.x; j < ntiles; j += kFinThreads) acc += partials[j];
+  for (int64_t j = lo + threadIdx.x; j < hi; j += kFinThreads) acc += partials[j];
   const double local = block_sum<kFinThreads>(acc, red);
-  if (threadIdx.x == 0) {
-    const double sq = local + extra_sqnorm;
+  if (threadIdx.x == 0) block_total = local;
+  cluster.sync();
+  if (r == 0 && threadIdx.x == 0) {
+    double total = 0.0;
+    for (int i = 0; i < kFinCluster; ++i) total += *cluster.map_shared_rank(&block_total, i);
+    const double sq = total + extra_sqnorm;
     const double norm = __dsqrt_rn(sq);
     const double q = __ddiv_rn(max_norm, __dadd_rn(norm, 1e-6));
-    zero_norm_result r;
-    r.sqnorm = sq;
-    r.norm = norm;
-    r.clip_coef = (q < 1.0) ? __double2float_rn(q) : 1.0f;
-    r.finite = isfinite(norm) ? 1 : 0;
-    *out = r;
+    zero_norm_result res;
+    res.sqnorm = sq;
+    res.norm = norm;
+    res.clip_coef = (q < 1.0) ? __double2float_rn(q) : 1.0f;
+    res.finite = isfinite(norm) ? 1 : 0;
+    *out = res;
   }
+  cluster.sync();
 }
 
 // Global norm from the ranks' local sums of squares, added in rank order by
@@ -139,7 +161,7 @@ zero_status launch_sqnorm_combine(const double* sq, int n_parts, double max_norm
 zero_status launch_sqnorm_finalize(const double* partials, int64_t n, double extra_sqnorm, double max_norm,
                                    zero_norm_result* out, cudaStream_t st) {
   const int64_t ntiles = (n + kSqTile - 1) / kSqTile;
-  sqnorm_finalize_kernel<<<1, kFinThreads, 0, st>>>(partials, ntiles, extra_sqnorm, max_norm, out);
+  sqnorm_finalize_kernel<<<kFinCluster, kFinThreads, 0, st>>>(partials, ntiles, extra_sqnorm, max_norm, out);
   return check_launch("sqnorm_finalize_kernel");
 }
 
@@ -151,7 +173,7 @@ zero_status launch_sqnorm(const float* g, int64_t n, double extra_sqnorm, double
     zero_status s = check_launch("sqnorm_tiles_kernel");
     if (s != ZERO_OK) return s;
   }
-  sqnorm_finalize_kernel<<<1, kFinThreads, 0, st>>>(partials, ntiles, extra_sqnorm, max_norm, out);
+  sqnorm_finalize_kernel<<<kFinCluster, kFinThreads, 0, st>>>(partials, ntiles, extra_sqnorm, max_norm, out);
   return check_launch("sqnorm_finalize_kernel");
 }
 
