@@ -498,10 +498,23 @@ def run_gpu(args):
     return 0
 
 
-def graph_step_ms(args, wl, s, e, dev, micro, stream) -> float:
+L2_BYTES = 129 << 20
+
+
+def l2_flusher(dev, step_bytes: int):
+    """A writer of 512 MB (4x the 129 MB L2) to run between timed steps when a step's
+    working set is small enough to stay L2-resident, else None."""
+    if step_bytes >= 4 * L2_BYTES:
+        return None
+    buf = torch.empty(512 << 18, dtype=torch.float32, device=dev)
+    return lambda: buf.fill_(1.0)
+
+
+def graph_step_ms(args, wl, s, e, dev, micro, stream, flush=None):
     """ms per step of the configuration's whole step replayed from a CUDA graph: a
     capturable optimizer (device step count), all micro-batches' grad passes with the
-    fused norm on the last, finalize, prepare and AdamW captured once."""
+    fused norm on the last, finalize, prepare and AdamW captured once.  Returns (per
+    replay after an L2 flush when `flush` is given, else back to back; back to back)."""
     from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
     opt = FlatShardAdamW(wl.numels, world_size=wl.world_size, rank=wl.rank, lr=wl.lr, betas=wl.betas, eps=wl.eps,
                          weight_decay=wl.weight_decay, max_norm=wl.max_norm,
@@ -522,16 +535,27 @@ def graph_step_ms(args, wl, s, e, dev, micro, stream) -> float:
         opt.launch_step()
     for _ in range(args.warmup):
         graph.replay()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(args.steps):
+    for _ in range(args.steps):  # back to back
         graph.replay()
     b.record(stream)
     torch.cuda.synchronize(dev)
+    b2b = a.elapsed_time(b) / args.steps
+    ms = b2b
+    if flush is not None:  # each replay timed alone, after an L2 flush outside its events
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in evs:
+            flush()
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     if not opt.finish_step().finite:
         raise RuntimeError("non-finite grad norm in the benchmark")
-    return a.elapsed_time(b) / args.steps
+    return ms, b2b
 
 
 def run_config(args):
@@ -587,6 +611,9 @@ def run_config(args):
         if not opt.finish_step().finite:
             raise RuntimeError("non-finite grad norm in the benchmark")
 
+    # bytes one step touches: every grad pass and AdamW (the fp32 grad buffer is re-read by each pass)
+    step_bytes = src_bytes + 4 * opt.grad.numel() * (2 * M) + ADAMW_BYTES_PER_PARAM * n
+    flush = l2_flusher(dev, step_bytes)
     for _ in range(args.warmup):
         step()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
@@ -594,13 +621,25 @@ def run_config(args):
     torch.cuda.synchronize(dev)
     a.record(stream)
     for k in range(args.steps):
+        if flush is not None:
+            flush()
         step(evs[k])
     b.record(stream)
     torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / args.steps
+    if flush is None:
+        ms = a.elapsed_time(b) / args.steps
+        eager_b2b = ms
+    else:  # the step's own events (first grad pass to the end of AdamW), the flush outside them
+        ms = statistics.mean(ev[0].elapsed_time(ev[3]) for ev in evs)
+        a.record(stream)
+        for k in range(args.steps):  # and back to back, host read of the norm after every step
+            step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        eager_b2b = a.elapsed_time(b) / args.steps
     t_grad = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs)
     t_k4 = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in evs)
-    graph_ms = graph_step_ms(args, wl, s, e, dev, micro, stream) if n <= (1 << 31) else None
+    graph_ms = graph_step_ms(args, wl, s, e, dev, micro, stream, flush) if n <= (1 << 31) else None
     peaks, _ = measured_peaks()
     grad_elems = opt.grad.numel()
     # grad passes: every micro-batch reads its source; the first writes the fp32 grad, later ones read+write it
@@ -611,16 +650,22 @@ def run_config(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "params_per_rank": n, "tensors": wl.n_tensors, "world_size": wl.world_size,
                    "rank": wl.rank, "micro_batches": M, "grad_dtype": wl.grad_dtype, "mode": wl.mode,
-                   "grad_buffer_elems": grad_elems},
+                   "grad_buffer_elems": grad_elems,
+                   "l2": (f"step touches {step_bytes / 1e6:.0f} MB < 4x L2: 512 MB written between timed steps, "
+                          f"each step timed by its own events (first grad pass to the end of AdamW)"
+                          if flush is not None else "inputs larger than L2; no flush")},
         "kernels_ms": {"flatten_or_accum_with_norm": t_grad, "adamw": t_k4},
         "kernels_gbs": {"flatten_or_accum_with_norm": grad_bytes / (t_grad / 1e3) / 1e9,
                         "adamw": ADAMW_BYTES_PER_PARAM * n / (t_k4 / 1e3) / 1e9},
         "adamw_frac_of_measured_hbm": ADAMW_BYTES_PER_PARAM * n / (t_k4 / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
     }
+    line["back_to_back_ms_per_step"] = eager_b2b  # steps launched one after another, norm read on the host each
     if graph_ms is not None:
-        line["graph"] = {"ms_per_step": graph_ms, "value": n / (graph_ms / 1e3), "unit": UNIT,
+        line["graph"] = {"ms_per_step": graph_ms[0], "value": n / (graph_ms[0] / 1e3), "unit": UNIT,
+                         "back_to_back_ms_per_step": graph_ms[1],
                          "what": "the same step captured once in a CUDA graph (step count and skip decision on the "
-                                 "device) and replayed back to back, no host work or device-to-host read per step"}
+                                 "device), no host work or device-to-host read per step; ms_per_step timed like the "
+                                 "eager step, back_to_back_ms_per_step = replays one after another"}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_config_rates(wl)
     print(json.dumps(line))
