@@ -498,3 +498,86 @@ def test_unscale_folded_into_accumulation_is_exact():
         oracle.accum(a, x, "f16", 1.0 / (S * M), accumulate=j > 0)
         oracle.accum(b, x, "f16", 1.0 / M, accumulate=j > 0)
     assert np.array_equal(a, b * np.float32(1.0 / S))
+
+
+# ------------------------------------------- configuration-scale cross-checks
+def _close_at_scale(ours, ref):
+    scale = float(np.abs(ref).max())
+    assert np.all(np.abs(ours - ref) <= 1e-6 * np.abs(ref) + 1e-6 * scale)
+    assert float(np.median(np.abs(ours - ref) / np.maximum(np.abs(ref), 1e-30))) < 2e-7
+
+
+def test_tiny_config_vs_torch_adamw():
+    """The tiny configuration at full size (4 fp32 tensors, 1,261,891 params, its
+    hyper-parameters, 3 steps, its seeded inputs): the oracle's flatten + AdamW against
+    torch.optim.AdamW (non-foreach) on the four tensors."""
+    wl = W.tiny()
+    s, e = oracle.shard_range(wl.total, 1, 0)
+    p0 = W.master_init(wl, s, e).numpy()
+    offs = oracle.flat_offsets(wl.numels)
+    params = [torch.nn.Parameter(torch.from_numpy(p0[offs[i]:offs[i + 1]].copy())) for i in range(len(wl.numels))]
+    opt = torch.optim.AdamW(params, lr=wl.lr, betas=wl.betas, eps=wl.eps, weight_decay=wl.weight_decay,
+                            foreach=False, fused=False)
+    st = oracle.new_state(p0)
+    for t in range(1, wl.steps + 1):
+        tg = W.tensor_grads(wl, t, 0, device="cpu")
+        g = np.zeros(e - s, np.float32)
+        oracle.flatten([x.numpy() for x in tg.tensors], wl.numels, "f32", s, e, 1.0, g, accumulate=False)
+        assert np.array_equal(g, torch.cat(tg.tensors).numpy())
+        cr = oracle.step_reference(st, g, lr=wl.lr, betas=wl.betas, eps=wl.eps, wd=wl.weight_decay,
+                                   max_norm=wl.max_norm)
+        assert cr.finite and cr.coef == 1.0
+        for prm, x in zip(params, tg.tensors):
+            prm.grad = x.clone()
+        opt.step()
+    for name, ours in (("p", st.p), ("m", st.m), ("v", st.v)):
+        if name == "p":
+            ref = torch.cat([x.detach() for x in params]).numpy()
+        else:
+            ref = torch.cat([opt.state[x]["exp_avg" if name == "m" else "exp_avg_sq"] for x in params]).numpy()
+        _close_at_scale(ours, ref)
+
+
+def test_gpt2_zero1_config_vs_torch_adamw_and_clip():
+    """The GPT-2 ZeRO-1 configuration at full size (148 tensors, 124,439,808 params, rank 3
+    of 8, bf16 grads averaged over 8 micro-batches, clip 1.0 on the whole buffer's norm),
+    2 steps: the oracle's flatten/accumulate, global norm and shard update against torch --
+    the flat averaged grad summed with torch ops, clip_grad_norm_ over the whole buffer,
+    torch.optim.Adam (non-foreach) over it -- compared on rank 3's slice.
+
+    clip_grad_norm_ runs on a float64 copy of the grad: torch's float32 CPU norm of these
+    1.2e8 values is 1.3 % off (3.8929 against 3.9440), so its float32 result is no
+    reference; the float64 one agrees with the oracle to ~1e-11."""
+    wl = W.gpt2_zero1()
+    s, e = oracle.shard_range(wl.total, wl.world_size, wl.rank)
+    offs = oracle.flat_offsets(wl.numels)
+    M = wl.micro_batches
+    p_full = W.master_init(wl, 0, wl.total)
+    prm = torch.nn.Parameter(p_full.clone())
+    opt = torch.optim.Adam([prm], lr=wl.lr, betas=wl.betas, eps=wl.eps, weight_decay=0.0, foreach=False, fused=False)
+    st = oracle.new_state(p_full[s:e].numpy())
+    for t in range(1, 3):
+        acc = np.zeros(wl.total, np.float32)
+        ref = torch.zeros(wl.total)
+        for j in range(M):
+            tg = W.tensor_grads(wl, t, j, device="cpu")
+            raw16 = [x.view(torch.int16).numpy().view(np.uint16) for x in tg.tensors]
+            oracle.flatten(raw16, wl.numels, "bf16", 0, wl.total, 1.0 / M, acc, accumulate=j > 0)
+            for i, x in enumerate(tg.tensors):
+                ref[offs[i]:offs[i + 1]].add_(x.float().mul_(1.0 / M))
+            del tg, raw16
+        assert np.array_equal(acc, ref.numpy())  # power-of-two scale: the same sums bit for bit
+        cr = oracle.step_reference(st, np.ascontiguousarray(acc[s:e]), lr=wl.lr, betas=wl.betas, eps=wl.eps,
+                                   wd=wl.weight_decay, max_norm=wl.max_norm, norm_grad=acc)
+        assert cr.finite and cr.coef < 1.0  # clipping is active in this configuration
+        p64 = torch.nn.Parameter(torch.zeros(wl.total, dtype=torch.float64))
+        p64.grad = ref.double()
+        tn = torch.nn.utils.clip_grad_norm_([p64], wl.max_norm).item()
+        del p64
+        assert abs(tn - cr.norm) <= 1e-10 * cr.norm
+        assert cr.coef == np.float32(wl.max_norm / (tn + 1e-6))
+        prm.grad = ref.mul_(cr.coef)  # the clipped grad in float32, as the update applies it
+        opt.step()
+    _close_at_scale(st.p, prm.detach()[s:e].numpy())
+    _close_at_scale(st.m, opt.state[prm]["exp_avg"][s:e].numpy())
+    _close_at_scale(st.v, opt.state[prm]["exp_avg_sq"][s:e].numpy())
