@@ -168,16 +168,18 @@ def adamw(p: np.ndarray, m: np.ndarray, v: np.ndarray, g: np.ndarray, scalars: n
     lib().orc_adamw(_p(p), _p(m), _p(v), _p(g), _p(lowp), DTYPE_CODE[lowp_dtype], p.size, _p(scalars), coef)
 
 
-def bf16_rne(x: np.ndarray) -> np.ndarray:
+def bf16_rne(x: np.ndarray, out: Optional[np.ndarray] = None) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
-    y = np.empty(x.shape, dtype=np.uint16)
+    y = np.empty(x.shape, dtype=np.uint16) if out is None else _c(out, np.uint16)
+    assert y.size == x.size
     lib().orc_bf16_rne_array(_p(x), _p(y), x.size)
     return y
 
 
-def f16_rne(x: np.ndarray) -> np.ndarray:
+def f16_rne(x: np.ndarray, out: Optional[np.ndarray] = None) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
-    y = np.empty(x.shape, dtype=np.uint16)
+    y = np.empty(x.shape, dtype=np.uint16) if out is None else _c(out, np.uint16)
+    assert y.size == x.size
     lib().orc_f16_rne_array(_p(x), _p(y), x.size)
     return y
 

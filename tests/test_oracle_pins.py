@@ -147,6 +147,34 @@ def test_f16_rne_vs_numpy():
     assert np.all((ours[nan] & 0x7C00) == 0x7C00) and np.all((ours[nan] & 0x03FF) != 0)
 
 
+def test_rne_exhaustive_over_all_binary32_patterns():
+    """Both roundings over every one of the 2^32 binary32 bit patterns, in chunks, against
+    torch's conversions (.to(bfloat16), .to(float16): round to nearest even); NaN inputs
+    give a NaN of the same sign."""
+    chunk = 1 << 26
+    base = np.arange(chunk, dtype=np.uint32)
+    bits = np.empty(chunk, dtype=np.uint32)
+    x = bits.view(np.float32)
+    ours = np.empty(chunk, dtype=np.uint16)  # buffers reused across chunks
+    neq = np.empty(chunk, dtype=bool)
+    ref_t = {torch.bfloat16: torch.empty(chunk, dtype=torch.bfloat16), torch.float16: torch.empty(chunk, dtype=torch.float16)}
+    for lo in range(0, 1 << 32, chunk):
+        np.add(base, np.uint32(lo), out=bits)
+        has_nan = (lo & 0x7FFFFFFF) + chunk > 0x7F800000  # the chunks that reach the NaN patterns
+        for rne, tdt, expo, mant in ((oracle.bf16_rne, torch.bfloat16, 0x7F80, 0x007F),
+                                     (oracle.f16_rne, torch.float16, 0x7C00, 0x03FF)):
+            rne(x, out=ours)
+            ref = ref_t[tdt].copy_(torch.from_numpy(x)).view(torch.int16).numpy().view(np.uint16)
+            if not has_nan:
+                assert not np.not_equal(ours, ref, out=neq).any(), (lo, tdt)
+                continue
+            nan = np.isnan(x)
+            assert np.array_equal(ours[~nan], ref[~nan]), (lo, tdt)
+            on = ours[nan]
+            assert np.all((on & expo) == expo) and np.all((on & mant) != 0), (lo, tdt)
+            assert np.array_equal(on >> 15, (bits[nan] >> 31).astype(np.uint16)), (lo, tdt)
+
+
 # ---------------------------------------------------------- A3 flatten / cast
 def _grads(numels, dtype, seed, null=()):
     g = torch.Generator().manual_seed(seed)
