@@ -504,3 +504,35 @@ def test_flatten_reads_pinned_host_grads():
     assert bits_equal_f32(raw(dst), ref)
     with pytest.raises(ValueError):
         zs.zero_tensor_table([torch.zeros(4, dtype=torch.bfloat16)], [4])  # pageable host memory is refused
+
+
+@pytest.mark.parametrize("lowp", [torch.bfloat16, torch.float16])
+def test_lowp_writeback_exhaustive_through_adamw(lowp):
+    """The AdamW kernel's low-precision write-back over every one of the 2^32 binary32
+    patterns: with lr = 0, weight decay 0 and zero grads the update leaves p as it is
+    (p*1 - 0*0), so the kernel writes round-to-nearest-even(p) for any p; compared with
+    the oracle's rounding (NaN in, NaN out)."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    chunk = 1 << 30
+    zeros = torch.zeros(chunk, device=DEV)
+    m, v, g = zeros.clone(), zeros.clone(), zeros
+    out = torch.empty(chunk, dtype=lowp, device=DEV)
+    base = np.arange(chunk, dtype=np.uint32)
+    bits = np.empty(chunk, dtype=np.uint32)
+    ref = np.empty(chunk, dtype=np.uint16)
+    rne = oracle.bf16_rne if lowp == torch.bfloat16 else oracle.f16_rne
+    expo = 0x7F80 if lowp == torch.bfloat16 else 0x7C00
+    for lo in range(0, 1 << 32, chunk):
+        np.add(base, np.uint32(lo), out=bits)
+        p = torch.from_numpy(bits.view(np.float32)).to(DEV)
+        m.zero_()
+        v.zero_()
+        zs.zero_adamw_step(p, m, v, g, out, 0.0, 0.9, 0.999, 1e-8, 0.0, 1)
+        got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        rne(bits.view(np.float32), out=ref)
+        nan = ((bits >> 23) & 0xFF) == 0xFF
+        nan &= (bits & 0x7FFFFF) != 0
+        assert np.array_equal(got[~nan], ref[~nan]), lo
+        gn = got[nan]
+        assert np.all((gn & expo) == expo) and np.all((gn & (0x7FFF ^ expo)) != 0), lo
+        assert np.array_equal(p.view(torch.int32).cpu().numpy().view(np.uint32)[~nan], bits[~nan]), lo  # p kept
