@@ -536,3 +536,51 @@ def test_lowp_writeback_exhaustive_through_adamw(lowp):
         gn = got[nan]
         assert np.all((gn & expo) == expo) and np.all((gn & (0x7FFF ^ expo)) != 0), lo
         assert np.array_equal(p.view(torch.int32).cpu().numpy().view(np.uint32)[~nan], bits[~nan]), lo  # p kept
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_cast_and_exact_square_norm_exhaustive_over_16bit_patterns(dtype):
+    """Every one of the 65,536 bf16 / f16 patterns through the flatten/cast (scales 1, 1/8, 4
+    and 0.3, fresh and accumulating) and the flat accumulate, bit-exact against the oracle
+    (NaN to NaN); and the exact-square norm path (norm-only, power-of-two scales) over every
+    finite pattern below 2^40 gives the same partials as the general path's separate norm."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    tdt = W.torch_dtype(dtype)
+    allbits = np.arange(1 << 16, dtype=np.uint16)
+    x = torch.from_numpy(allbits.view(np.int16).copy()).view(tdt)
+    xd = x.to(DEV)
+    numels = [1 << 16]
+    table, total = zs.zero_tensor_table([xd], numels)
+    d_table = zs.device_table(table, 1, DEV)
+    for scale in (1.0, 0.125, 4.0, 0.3):
+        for acc_first in (False, True):
+            ref = np.full(total, 0.5, np.float32)
+            dst = torch.full((total,), 0.5, device=DEV)
+            oracle.flatten([allbits], numels, dtype, 0, total, scale, ref, accumulate=acc_first)
+            zs.zero_flatten_cast(d_table, 1, total, tdt, 0, total, scale, acc_first, dst)
+            acc = torch.full((total,), 0.5, device=DEV)
+            ref2 = np.full(total, 0.5, np.float32)
+            oracle.accum(ref2, allbits, dtype, scale, accumulate=acc_first)
+            zs.zero_accum(acc, xd, scale, acc_first)
+            for got, want in ((raw(dst), ref), (raw(acc), ref2)):
+                nan = np.isnan(want)
+                assert np.array_equal(np.isnan(got), nan), (scale, acc_first)
+                assert bits_equal_f32(got[~nan], want[~nan]), (scale, acc_first)
+    # every finite pattern whose scaled square sums stay in binary32 range (|x| < 2^40:
+    # all f16 values; bf16 below 2^40, the subnormals and both zeros included)
+    expo = (allbits >> (7 if dtype == "bf16" else 10)) & (0xFF if dtype == "bf16" else 0x1F)
+    finite = allbits[expo < (127 + 40 if dtype == "bf16" else 0x1F)]
+    reps = np.tile(finite, 4)  # several norm tiles, each element in different positions
+    fd = torch.from_numpy(reps.view(np.int16).copy()).view(tdt).to(DEV)
+    n = fd.numel()
+    table, total = zs.zero_tensor_table([fd], [n])
+    d_table = zs.device_table(table, 1, DEV)
+    nb = zs.zero_grad_sqnorm_workspace_bytes(n)
+    for scale in (1.0, 2.0 ** -12, 8.0):
+        ws_exact = torch.full((nb,), 0x3C, dtype=torch.uint8, device=DEV)
+        zs.zero_flatten_cast(d_table, 1, total, tdt, 0, total, scale, False, None, norm_ws=ws_exact)
+        flat = torch.empty(n, device=DEV)
+        zs.zero_flatten_cast(d_table, 1, total, tdt, 0, total, scale, False, flat)
+        ws_s, r_s, r_e = _norm_pair(zs, flat, n, fused_ws=ws_exact)
+        assert torch.equal(ws_exact, ws_s[:nb]), scale
+        assert r_s == r_e
