@@ -59,7 +59,7 @@ __device__ __forceinline__ void store_group(float* __restrict__ p, float* __rest
 // copy in shared memory.  A partial last block or unaligned state goes
 // element by element through the staged copy.
 template <int DT, int LOWP, int LW, bool DEVS>
-__global__ void __launch_bounds__(256, 4) adamw_table_kernel(float* __restrict__ p, float* __restrict__ m,
+__global__ void __launch_bounds__(256, DT == ZERO_F32 ? 3 : 4) adamw_table_kernel(float* __restrict__ p, float* __restrict__ m,
                                                              float* __restrict__ v,
                                                              const zero_tensor* __restrict__ table, int n_tensors,
                                                              int64_t shard_start, int64_t n, float gscale,
@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(256, 4) adamw_table_kernel(float* __restrict__
       ld8_rw(m + k, mr);
       ld8_rw(v + k, vr);
     }
-    const int ti = find_tensor(table, n_tensors, f0);
+    const int ti = find_tensor_warp(table, n_tensors, f0);
     const void* tptr = table[ti].ptr;
     const int64_t toff = __ldg(&table[ti].flat_offset), tnum = __ldg(&table[ti].numel);
     const char* tsrc = tptr ? static_cast<const char*>(tptr) + es * (f0 - toff) : nullptr;
