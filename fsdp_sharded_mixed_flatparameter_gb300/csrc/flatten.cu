@@ -71,7 +71,8 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
   for (int64_t wb = blockIdx.x; wb < nblocks_work; wb += gridDim.x) {
     const int64_t t0 = wb * kPerBlock;
     const int64_t t1 = (t0 + kPerBlock < ntiles) ? t0 + kPerBlock : ntiles;
-    int ti = find_tensor(table, n_tensors, shard_start + t0 * kFlTile);
+    const int64_t k_first = shard_start + t0 * kFlTile;
+    int ti = (WRITE && NORM) ? find_tensor(table, n_tensors, k_first) : find_tensor_warp(table, n_tensors, k_first);
     NormAcc nacc;  // this thread's share of the norm tile
     if (!WRITE && threadIdx.x == 0) {
       // Norm only: the block's loads are 2-4 bytes per element, too few in
