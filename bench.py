@@ -306,7 +306,7 @@ def run_gpu(args):
                          max_norm=wl.max_norm, device=dev, master=master)
     del master
     grads = tg.tensors
-    d_table = opt._table(grads)
+    d_table, _, _ = opt.device_table(grads)
     stream = torch.cuda.current_stream(dev)
     grad_bytes = sum(t.numel() * t.element_size() for t in grads)
 
@@ -520,7 +520,7 @@ def graph_step_ms(args, wl, s, e, dev, micro, stream, flush=None):
     M = wl.micro_batches
     if wl.mode != "zero3":
         for m in micro:
-            opt._table(m)  # device tables built before capture
+            opt.device_table(m)  # device tables built before capture
     torch.cuda.synchronize(dev)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
@@ -584,7 +584,7 @@ def run_config(args):
     src_bytes = M * opt.grad.numel() * esize  # each pass reads the grad range's elements once
     stream = torch.cuda.current_stream(dev)
 
-    tables = [] if wl.mode == "zero3" else [opt._resolve(m) for m in micro]  # built once, like registered grads
+    tables = [] if wl.mode == "zero3" else [opt.device_table(m) for m in micro]  # built once, like registered grads
 
     def step(ev=None):
         if ev is not None:

@@ -126,6 +126,12 @@ class FlatShardAdamW:
             self._tables[key] = hit
         return hit[0]
 
+    def device_table(self, grads: Sequence[Optional[torch.Tensor]]) -> Tuple[torch.Tensor, int, torch.dtype]:
+        """The FlatParameter table of a grads list in device memory (built once per list of
+        grad addresses and cached), with its tensor count and grad dtype.  Calling it before
+        a CUDA graph capture keeps the table's host-to-device copy out of the graph."""
+        return self._resolve(grads)
+
     def register_grads(self, grads: Sequence[Optional[torch.Tensor]]) -> None:
         """Fix the per-tensor grads once (e.g. views into one flat grad storage, as
         FSDP's FlatParameter keeps them).  flatten() / step_tensors() called without

@@ -135,7 +135,7 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
             if captured is None:
                 if wl.mode != "zero3":
                     for tg in micro:
-                        opt._table(tg.tensors)  # device tables built before capture (no copies inside it)
+                        opt.device_table(tg.tensors)  # device tables built before capture (no copies inside it)
                 torch.cuda.synchronize()
                 captured = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(captured):
