@@ -49,7 +49,9 @@ class FlatShardAdamW:
         self.start, self.end = zs.zero_shard_range(self.total, world_size, rank)
         self.n = self.end - self.start
         self.glo, self.ghi = (0, self.total) if grad_range == "full" else (self.start, self.end)
-        self.lr, self.betas, self.eps, self.weight_decay, self.max_norm = lr, tuple(betas), eps, weight_decay, max_norm
+        self.capturable = capturable
+        self._hp = [float(lr), float(betas[0]), float(betas[1]), float(eps), float(weight_decay)]
+        self.max_norm = max_norm
         dev = self.device
         # the fp32 flat grad; not needed when every step goes through step_tensors()
         self.grad = torch.empty(self.ghi - self.glo if grad_buffer else 0, dtype=torch.float32, device=dev)
@@ -70,10 +72,9 @@ class FlatShardAdamW:
                               device=dev)
         self.norm_buf = zs.new_norm_result(dev)
         self.found_nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.capturable = capturable
         self._t = 0
         if capturable:
-            self._dev_hp = zs.device_hparams(lr, self.betas[0], self.betas[1], eps, weight_decay, dev)
+            self._dev_hp = zs.device_hparams(*self._hp, dev)
             self._dev_state = zs.new_adamw_device_state(dev)
         self._norm_ready = False  # the grad norm's tile partials are up to date in self.ws
         self._local_buf: Optional[torch.Tensor] = None
@@ -95,16 +96,54 @@ class FlatShardAdamW:
         else:
             self._t = int(value)
 
+    # -------------------------------------------------- hyper-parameters
+    # Assigning lr / betas / eps / weight_decay (e.g. from a schedule) also rewrites the
+    # device copy in place when capturable=True, so a captured graph reads the new values
+    # at its next replay.
+    def _set_hp(self, i: int, value: float) -> None:
+        self._hp[i] = float(value)
+        if self.capturable:
+            zs.device_hparams(*self._hp, self.device, out=self._dev_hp)
+
+    @property
+    def lr(self) -> float:
+        return self._hp[0]
+
+    @lr.setter
+    def lr(self, value: float) -> None:
+        self._set_hp(0, value)
+
+    @property
+    def betas(self) -> Tuple[float, float]:
+        return (self._hp[1], self._hp[2])
+
+    @betas.setter
+    def betas(self, value: Tuple[float, float]) -> None:
+        self._hp[1] = float(value[0])
+        self._set_hp(2, value[1])
+
+    @property
+    def eps(self) -> float:
+        return self._hp[3]
+
+    @eps.setter
+    def eps(self, value: float) -> None:
+        self._set_hp(3, value)
+
+    @property
+    def weight_decay(self) -> float:
+        return self._hp[4]
+
+    @weight_decay.setter
+    def weight_decay(self, value: float) -> None:
+        self._set_hp(4, value)
+
     def set_hparams(self, lr: Optional[float] = None, weight_decay: Optional[float] = None) -> None:
-        """Change lr / weight decay (e.g. a schedule).  With capturable=True the device copy
-        is rewritten in place, so a captured graph uses the new values at its next replay."""
+        """Change lr and/or weight decay (same as assigning the attributes)."""
         if lr is not None:
             self.lr = lr
         if weight_decay is not None:
             self.weight_decay = weight_decay
-        if self.capturable:
-            zs.device_hparams(self.lr, self.betas[0], self.betas[1], self.eps, self.weight_decay, self.device,
-                              out=self._dev_hp)
 
     # ---------------------------------------------------------------- grads
     def _table(self, grads: Sequence[Optional[torch.Tensor]]) -> torch.Tensor:

@@ -174,8 +174,9 @@ def test_graph_replay_skips_a_nonfinite_step():
 
 
 def test_capturable_state_dict_round_trip_and_lr_change():
-    """t lives on the device: state_dict reads it, load_state_dict writes it; set_hparams
-    rewrites the device hyper-parameters that an already captured graph reads."""
+    """t lives on the device: state_dict reads it, load_state_dict writes it; changing lr
+    (set_hparams or plain assignment) rewrites the device hyper-parameters that an already
+    captured graph reads."""
     from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
     wl = W.small_llama(layers=1, hidden=128, mlp=344, vocab=301, max_norm=math.inf)
     kw = dict(lr=1e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1, device=DEV)
@@ -190,7 +191,7 @@ def test_capturable_state_dict_round_trip_and_lr_change():
     for t in range(1, 4):
         if t == 3:
             A.set_hparams(lr=2e-4)
-            B.set_hparams(lr=2e-4)
+            B.lr = 2e-4  # plain assignment reaches the device copy the graph reads
         A.step_tensors(tg.tensors)
         graph.replay()
         B.finish_step()
