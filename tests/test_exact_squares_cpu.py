@@ -1,15 +1,15 @@
 """The grad norm's exact-square shortcut, checked exhaustively on the CPU.
 
-For 16-bit grads scaled by a power of two the norm kernels skip the
-rounding residual e = fma(y, y, -fl(y*y)) of each square and use a packed
-fma y*0 + z as the non-finite probe.  Both rest on IEEE-754 binary32 facts
-checked here over every bf16 and f16 value:
+For 16-bit grads scaled by a power of two the norm-only pass skips the
+rounding residual e = fma(y, y, -fl(y*y)) of each square and tests for
+non-finite grads only where a thread's sum went non-finite.  Both rest on
+IEEE-754 binary32 facts checked here:
 
 * the residual rounds to a zero for y = fl(s * w), s a power of two
   (the square of a significand of at most 11 bits fits in 24 bits; where the
   square underflows the residual is at most half of the smallest subnormal);
 * the same is false in general (a non-power-of-two scale), so the check can fail;
-* y*0 + (+0) is a zero for finite y and NaN for inf/NaN.
+* an inf or NaN value leaves the double-float sum of squares non-finite.
 
 The binary32 results are emulated in binary64, where the square of a binary32
 value is exact and the binary64 -> binary32 cast rounds once to nearest even.
@@ -71,9 +71,38 @@ def test_square_residual_is_not_zero_in_general():
     assert np.count_nonzero(e) > 9000
 
 
-def test_zero_probe_flags_exactly_the_nonfinite_values():
-    y = _all_bf16()
-    with np.errstate(invalid="ignore"):
-        z = y * np.float32(0.0) + np.float32(0.0)
-    assert np.array_equal(np.isnan(z), ~np.isfinite(y))
-    assert np.all(z[np.isfinite(y)] == 0)
+def _df_sum_of_squares(x):
+    """The exact-square accumulation of one lane, emulated in binary32: p = x*x,
+    s = h + p with TwoSum's error into l (numpy float32 ops round like the kernel's)."""
+    f = np.float32
+    h, l = f(0), f(0)
+    with np.errstate(over="ignore", invalid="ignore"):
+        for v in x.astype(np.float32):
+            p = f(v * v)
+            s = f(h + p)
+            bp = f(s - h)
+            t = f(f(h - f(s - bp)) + f(p - bp))
+            h, l = s, f(l + t)
+    return h, l
+
+
+def test_nonfinite_value_makes_the_sum_nonfinite():
+    """The norm-only pass decides the non-finite flag only where a thread's sum went
+    non-finite: an inf or NaN anywhere in the lane leaves h non-finite, however many
+    finite values follow; a finite value whose square overflows does the same (so the
+    flag itself comes from re-reading the values, not from the sum)."""
+    rng = np.random.default_rng(3)
+    bad_values = [np.inf, -np.inf, np.nan]
+    for trial in range(300):
+        x = (rng.standard_normal(64) * 10.0 ** rng.integers(-20, 10)).astype(np.float32)
+        i = int(rng.integers(0, 64))
+        x[i] = bad_values[trial % 3]
+        h, _ = _df_sum_of_squares(x)
+        assert not np.isfinite(h), (trial, i)
+        x[i] = np.float32(1.0)
+        h, _ = _df_sum_of_squares(x)
+        assert np.isfinite(h), trial
+    x = np.full(8, 1e-3, np.float32)
+    x[3] = np.float32(2.0 ** 70)  # finite, square beyond binary32
+    h, _ = _df_sum_of_squares(x)
+    assert not np.isfinite(h)

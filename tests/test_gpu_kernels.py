@@ -412,7 +412,7 @@ def _bits_tensors(numels, dtype, seed, elem_offsets=(0,)):
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_exact_square_norm_equals_separate_norm(dtype):
     """The norm-only pass over 16-bit grads with a power-of-two scale takes the
-    exact-square path (no residual term, packed non-finite probe).  Its partials equal
+    exact-square path (no residual term, non-finite flag from the sum).  Its partials equal
     bit for bit those of the writing pass with the fused norm and of the separate norm
     over the written buffer, over values from underflowing squares to ~2^80; a
     non-power-of-two scale takes the general path and agrees the same way."""
@@ -457,7 +457,7 @@ def test_exact_square_norm_equals_separate_norm(dtype):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_exact_square_norm_flags_nonfinite(dtype):
-    """The packed probe of the exact-square path raises the flag for inf and NaN grads,
+    """The exact-square path (flag decided from the sum, values re-read) raises the flag for inf and NaN grads,
     in in-tensor and staged tiles alike, and only for them: a finite bf16 grad whose
     square overflows binary32 makes the norm non-finite without raising the flag."""
     from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
