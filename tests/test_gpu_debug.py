@@ -57,6 +57,9 @@ def test_debug_selftest_is_reported():
 def test_kernel_suites_record_no_violation_under_the_debug_build():
     suites = ["tests/test_gpu_kernels.py", "tests/test_gpu_direct.py", "tests/test_gpu_graph.py",
               "tests/test_gpu_amp.py", "tests/test_gpu_multirank.py"]
-    p = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider"] + suites,
+    # (the 2^32-pattern write-back check runs once, under the release build: here it would only
+    # repeat the same kernel sites for a minute)
+    p = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
+                        "-k", "not exhaustive_through_adamw"] + suites,
                        cwd=ROOT, env=_env(), capture_output=True, text=True, timeout=1800)
     assert p.returncode == 0, p.stdout[-4000:] + p.stderr[-2000:]
