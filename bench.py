@@ -166,7 +166,8 @@ def oracle_step_rate(wl: W.Workload, sample_params: int, min_seconds: float, max
         stage[2] += td - tc
         passes += 1
         el = time.perf_counter() - t0
-        if el >= min_seconds or passes >= max_passes:
+        # min_seconds <= 0: exactly max_passes passes; else stop once min_seconds have passed
+        if passes >= max_passes or (min_seconds > 0.0 and el >= min_seconds):
             break
     oracle_step_rate.last_stages = {k: tot * passes / v for k, v in zip(("flatten", "sqnorm", "adamw"), stage)}
     return tot * passes / el, tot, passes, el
@@ -243,21 +244,28 @@ def oracle_config_rates(wl: W.Workload, sample_params: int = 1 << 23, min_second
             "stages_elems_per_s": {"grad_pass": r_grad, "sqnorm": r_norm, "adamw": r_adam}}
 
 
+REFERENCE_SAMPLE = 1 << 24  # params of one reference-arm step (one oracle step over this sample)
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     wl = W.llama7b()
-    sample = 1 << 24
-    # warm-up passes, then K timed passes, each one oracle step over the sample
-    oracle_step_rate(wl, sample, 0.0, max(args.warmup, 1))
+    sample = REFERENCE_SAMPLE
+    # exactly --warmup untimed passes, then exactly --steps timed passes, each one whole
+    # oracle step over the sample
+    if args.warmup > 0:
+        oracle_step_rate(wl, sample, 0.0, args.warmup)
     rate, tot, passes, el = oracle_step_rate(wl, sample, 0.0, args.steps)
+    assert passes == args.steps
     cores = 1
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / passes,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl.name, "params_per_rank": wl.total, "tensors": wl.n_tensors, "world_size": 1,
+        "config": {"workload": wl.name, "params_per_rank": tot, "sample_params": tot,
+                   "workload_params": wl.total, "tensors": wl.n_tensors, "world_size": 1,
                    "grad_dtype": "bf16", "lowp_dtype": "bf16", "max_norm": wl.max_norm},
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"each step: the oracle's whole step (flatten/cast, norm, clip, AdamW) on the "

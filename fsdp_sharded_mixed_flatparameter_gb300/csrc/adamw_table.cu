@@ -77,7 +77,10 @@ __global__ void __launch_bounds__(256, DT == ZERO_F32 ? 3 : 4) adamw_table_kerne
   constexpr int es = SrcTraits<DT>::esize;
   constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
   const int64_t nblk = (n + kAtBlock - 1) / kAtBlock;
-  bool bad = false;  // the flatten pass of this step reports non-finite grads
+  // stage_range also reports non-finite grads; here that flag is unused: the
+  // norm pass of this step (K1 without output) raises d_found_nonfinite, and a
+  // non-finite norm has already made this kernel return above
+  bool unused_flag = false;
   for (int64_t b = blockIdx.x; b < nblk; b += gridDim.x) {
     const int64_t k0 = b * kAtBlock;
     const int blen = static_cast<int>((n - k0 < kAtBlock) ? (n - k0) : kAtBlock);
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(256, DT == ZERO_F32 ? 3 : 4) adamw_table_kerne
           for (int j = 0; j < 8; ++j) gr[j] = __fmul_rn(gscale, gr[j]);
         }
       } else {
-        stage_range<DT>(table, n_tensors, ti, f0, f0 + kAtBlock, gscale, stage, bad);
+        stage_range<DT>(table, n_tensors, ti, f0, f0 + kAtBlock, gscale, stage, unused_flag);
         __syncthreads();
 #pragma unroll
         for (int j = 0; j < 8; ++j) gr[j] = stage[stage_idx(8 * threadIdx.x + j)];  // stride 9: no bank conflict
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(256, DT == ZERO_F32 ? 3 : 4) adamw_table_kerne
         store_group<LOWP, LW>(p, m, v, lowp, k, pr, mr, vr);
       }
     } else {
-      stage_range<DT>(table, n_tensors, ti, f0, f0 + blen, gscale, stage, bad);
+      stage_range<DT>(table, n_tensors, ti, f0, f0 + blen, gscale, stage, unused_flag);
       __syncthreads();
       for (int q = threadIdx.x; q < blen; q += blockDim.x) {
         const int64_t kq = k0 + q;

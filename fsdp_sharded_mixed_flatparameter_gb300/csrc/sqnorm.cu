@@ -35,6 +35,7 @@
 // differ from the binary64 oracle; gradients never come near either.
 // No atomics: the result is bit-identical from run to run and GPU to GPU.
 #include <cooperative_groups.h>
+#include <cuda.h>
 
 #include <cmath>
 #include <mutex>
@@ -184,7 +185,12 @@ zero_status launch_sqnorm(const float* g, int64_t n, double extra_sqnorm, double
 // The array is a module global: every GPU that loads the library holds its
 // 4 MiB until the process exits.  In host code `g_noalloc_partials` is only a
 // host-side stand-in for the symbol, never a device address; the device
-// address is looked up once per device with cudaGetSymbolAddress.
+// address is looked up with cudaGetSymbolAddress once per device and
+// context, with that device current.  The cache is keyed on the context's
+// process-unique ID (cuCtxGetId, reached through the runtime's driver entry
+// point, so the library does not link libcuda): after cudaDeviceReset the
+// runtime creates a new primary context, which loads the module again and
+// may place the array elsewhere, and the next call looks it up again.
 
 constexpr int64_t kNoAllocMaxTiles = int64_t(1) << 19;  // 4 MiB of binary64 partials
 
@@ -193,7 +199,40 @@ static __device__ __align__(256) double g_noalloc_partials[kNoAllocMaxTiles];
 namespace {
 constexpr int kMaxDevices = 256;
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices] = {};
+struct NoAllocSlot {
+  unsigned long long ctx_id;  // ID of the context the address belongs to (0: none yet)
+  void* addr;
+};
+NoAllocSlot g_noalloc_slot[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The current context's process-unique ID.  Before the runtime has made any
+// context current (the process's first CUDA work) the handle is null and an
+// error comes back; the caller then looks the address up without caching it,
+// which also initialises the context for the next call.
+cudaError_t current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  if (get_current == nullptr || get_id == nullptr) {
+    cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound, q2 = cudaDriverEntryPointSymbolNotFound;
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaError_t e1 = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1);
+    if (e1 != cudaSuccess) return e1;
+    cudaError_t e2 = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2);
+    if (e2 != cudaSuccess) return e2;
+    if (q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+      return cudaErrorSymbolNotFound;
+    get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+    get_id = reinterpret_cast<CtxGetIdFn>(f2);
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+  if (get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  return cudaSuccess;
+}
 }  // namespace
 
 }  // namespace zs
@@ -219,16 +258,29 @@ extern "C" zero_status zero_grad_sqnorm_noalloc(const float* d_grad, int64_t n, 
   if (dev < 0 || dev >= zs::kMaxDevices) return fail(ZERO_EINVAL, "zero_grad_sqnorm_noalloc: device %d", dev);
   void* scratch = nullptr;
   {
-    // once per device, with that device current: find the array's device address
+    // once per device and context, with that device current: find the array's device address
     std::lock_guard<std::mutex> lk(zs::g_noalloc_mu);
-    if (zs::g_noalloc_addr[dev] == nullptr) {
+    unsigned long long ctx_id = 0;
+    zs::NoAllocSlot& slot = zs::g_noalloc_slot[dev];
+    ce = zs::current_context_id(&ctx_id);
+    if (ce != cudaSuccess || ctx_id == 0) {
+      // no usable context ID: look the address up on every call (always correct, a little slower)
       void* p = nullptr;
       ce = cudaGetSymbolAddress(&p, zs::g_noalloc_partials);
       if (ce != cudaSuccess || p == nullptr)
         return fail(ZERO_ECUDA, "zero_grad_sqnorm_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(ce));
-      zs::g_noalloc_addr[dev] = p;
+      scratch = p;
+    } else {
+      if (slot.addr == nullptr || slot.ctx_id != ctx_id) {
+        void* p = nullptr;
+        ce = cudaGetSymbolAddress(&p, zs::g_noalloc_partials);
+        if (ce != cudaSuccess || p == nullptr)
+          return fail(ZERO_ECUDA, "zero_grad_sqnorm_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(ce));
+        slot.addr = p;
+        slot.ctx_id = ctx_id;
+      }
+      scratch = slot.addr;
     }
-    scratch = zs::g_noalloc_addr[dev];
   }
   return zs::launch_sqnorm(d_grad, n, extra_sqnorm, max_norm, static_cast<double*>(scratch), d_out,
                            zs::as_stream(stream));

@@ -254,26 +254,37 @@ class FlatShardAdamW:
                                self.betas[0], self.betas[1], self.eps, self.weight_decay, self._t + 1,
                                self.norm_buf, stream)
 
-    def finish_step(self) -> zs.NormResult:
-        """Read the step's grad norm (a device->host copy that waits for the step).
-        With capturable=True the device already advanced (or kept) the step count."""
-        r = zs.decode_norm_result(self.norm_buf)
+    def finish_step(self, stream=None) -> zs.NormResult:
+        """Read the step's grad norm (a device->host copy that waits for the step's
+        work on `stream`, the stream the step was enqueued on; default: the current
+        stream).  With capturable=True the device already advanced (or kept) the
+        step count."""
+        with torch.cuda.stream(torch_stream(stream, self.device)):
+            r = zs.decode_norm_result(self.norm_buf)
         if r.finite and not self.capturable:
             self._t += 1
         return r
+
+    def _global_norm(self, local: torch.Tensor, process_group, stream: torch.cuda.Stream) -> torch.Tensor:
+        """The ranks' local sums of squares in rank order, on this device, ordered
+        after `local` was written on `stream` and before later work on `stream`."""
+        with torch.cuda.stream(stream):
+            return gather_sqnorms(local, process_group)
 
     def step(self, extra_sqnorm: float = 0.0, stream=None, process_group=None) -> zs.NormResult:
         """One optimizer step.  With a torch.distributed process group of more than
         one rank and a shard-only grad buffer (ZeRO-2/3), the clip norm is global:
         the ranks exchange their 8-byte local sums of squares (all-gather, rank
         order) and every rank combines the same vector, so all ranks use the same
-        coefficient and agree on skipping a non-finite step."""
+        coefficient and agree on skipping a non-finite step.  The exchange is
+        ordered on `stream` like the kernels, whichever stream that is."""
         if process_group is not None and self.glo == self.start and _world(process_group) > 1:
-            local = self.local_sqnorm(stream)
-            self.launch_step(stream=stream, gathered_sqnorms=gather_sqnorms(local, process_group))
+            st = torch_stream(stream, self.device)
+            local = self.local_sqnorm(st)
+            self.launch_step(stream=st, gathered_sqnorms=self._global_norm(local, process_group, st))
         else:
             self.launch_step(extra_sqnorm, stream)
-        return self.finish_step()
+        return self.finish_step(stream)
 
     def step_tensors(self, grads: Optional[Sequence[Optional[torch.Tensor]]] = None, *, scale: float = 1.0,
                      stream=None, process_group=None) -> zs.NormResult:
@@ -283,7 +294,7 @@ class FlatShardAdamW:
         fp32 flat grad is written (30 instead of 36 bytes per parameter); the result
         is bit-identical to flatten(scale) + step()."""
         self.launch_step_tensors(grads, scale=scale, stream=stream, process_group=process_group)
-        return self.finish_step()
+        return self.finish_step(stream)
 
     def launch_step_tensors(self, grads: Optional[Sequence[Optional[torch.Tensor]]] = None, *, scale: float = 1.0,
                             stream=None, process_group=None) -> None:
@@ -294,9 +305,10 @@ class FlatShardAdamW:
         if process_group is not None and self.glo == self.start and _world(process_group) > 1:
             if self._local_buf is None:
                 self._local_buf = zs.new_norm_result(self.device)
-            zs.zero_grad_sqnorm_finalize(self.ws, self.ghi - self.glo, 0.0, math.inf, self._local_buf, stream)
-            gathered = gather_sqnorms(zs.sqnorm_view(self._local_buf), process_group)
-            zs.zero_grad_sqnorm_combine(gathered, self.max_norm, self.norm_buf, stream)
+            st = torch_stream(stream, self.device)
+            zs.zero_grad_sqnorm_finalize(self.ws, self.ghi - self.glo, 0.0, math.inf, self._local_buf, st)
+            gathered = self._global_norm(zs.sqnorm_view(self._local_buf), process_group, st)
+            zs.zero_grad_sqnorm_combine(gathered, self.max_norm, self.norm_buf, st)
         else:
             zs.zero_grad_sqnorm_finalize(self.ws, self.ghi - self.glo, 0.0, self.max_norm, self.norm_buf, stream)
         self._norm_ready = False
@@ -343,12 +355,36 @@ def _world(group) -> int:
     return dist.get_world_size(group)
 
 
+def torch_stream(stream, device) -> torch.cuda.Stream:
+    """A torch stream object for a stream argument of this package: None (the
+    current stream of `device`), a torch.cuda.Stream, or a raw cudaStream_t
+    handle (wrapped, not owned)."""
+    if stream is None:
+        return torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return stream
+    return torch.cuda.ExternalStream(int(stream), device=device)
+
+
+def _backend(group) -> str:
+    import torch.distributed as dist
+    return str(dist.get_backend(group)).lower()
+
+
 def gather_sqnorms(local: torch.Tensor, group) -> torch.Tensor:
     """All-gather every rank's 1-element float64 sum of squares, in rank order.
 
-    The only data exchanged by the step (8 bytes per rank).  Works with NCCL on
-    device tensors and with gloo on host tensors."""
+    The step's norm exchange (8 bytes per rank).  With NCCL the device tensor
+    is gathered directly, ordered on torch's current stream.  With a backend
+    that works on host memory (gloo) a device value is staged through the host:
+    the copy out waits for the current stream, and the gathered vector is
+    copied back to the device on it.  Run it under ``torch.cuda.stream(s)`` to
+    order it on another stream s."""
     import torch.distributed as dist
-    parts = [torch.empty_like(local) for _ in range(dist.get_world_size(group))]
-    dist.all_gather(parts, local.contiguous(), group=group)
-    return torch.cat(parts)
+    world = dist.get_world_size(group)
+    staged = local.is_cuda and _backend(group) != "nccl"
+    x = local.detach().to("cpu") if staged else local.contiguous()
+    parts = [torch.empty_like(x) for _ in range(world)]
+    dist.all_gather(parts, x, group=group)
+    out = torch.cat(parts)
+    return out.to(local.device) if staged else out

@@ -12,6 +12,8 @@ the coefficient is known (pinned by the shard-slice equivalence test).
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 from typing import List, Optional
 
@@ -23,6 +25,8 @@ import workloads as W
 from _helpers import (RTOL_NORM, assert_close_f32, assert_lowp_ulp, assert_lowp_ulp_f16, bits_equal_f32, raw)
 
 DEV = torch.device("cuda:0")
+# host threads for the oracle's chunks of the multi-billion-parameter configurations
+ORACLE_THREADS = max(1, min(16, os.cpu_count() or 1))
 
 
 @dataclass
@@ -71,7 +75,8 @@ def _host_parts(tg: W.TensorGrads, numels, offsets, a: int, b: int, nulls):
 
 
 def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk: int = 1 << 26,
-                 seed: int = 0, fused: bool = True, direct: bool = False, graph: bool = False) -> RunReport:
+                 seed: int = 0, fused: bool = True, direct: bool = False, graph: bool = False,
+                 oracle_threads: int = ORACLE_THREADS) -> RunReport:
     """fused: the last micro-batch's flatten/accumulate also computes the grad
     norm's partials (the norm is then only finalized); otherwise the norm is a
     separate pass over the flat grad.  direct: one micro-batch of per-tensor
@@ -145,10 +150,14 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
             enqueue(micro)
         res = opt.finish_step()
 
-        # ---- oracle side: accumulate every element (chunked) for the norm
-        sq_parts = []
+        # ---- oracle side: accumulate every element (chunked) for the norm.  The
+        # chunks are independent (the oracle's calls on disjoint ranges), so large
+        # configurations run them on a pool of host threads (ctypes and the
+        # device-to-host copies release the GIL); math.fsum of the chunk sums is
+        # exact whatever the order, so the result is the single-threaded one.
         g_shard = np.empty(n if idx is None else idx.size, np.float32)
-        for a in range(glo, ghi, chunk):
+
+        def oracle_chunk(a):
             b = min(a + chunk, ghi)
             acc = np.empty(b - a, np.float32)
             for j in range(M):
@@ -157,8 +166,7 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
                 else:
                     parts, pn = _host_parts(micro[j], wl.numels, offsets, a, b, nulls)
                     oracle.flatten(parts, pn, wl.grad_dtype, 0, b - a, scale, acc, accumulate=j > 0)
-            sq_parts.append(oracle.sqnorm(acc))
-            # the shard's grad values the update needs
+            # the shard's grad values the update needs (disjoint per chunk)
             lo, hi = max(a, s), min(b, e)
             if hi > lo:
                 if idx is None:
@@ -166,6 +174,14 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
                 else:
                     sel = (idx >= lo - s) & (idx < hi - s)
                     g_shard[sel] = acc[idx[sel] + s - a]
+            return oracle.sqnorm(acc)
+
+        starts = list(range(glo, ghi, chunk))
+        if len(starts) > 2 and oracle_threads > 1:
+            with ThreadPoolExecutor(max_workers=min(oracle_threads, len(starts))) as pool:
+                sq_parts = list(pool.map(oracle_chunk, starts))
+        else:
+            sq_parts = [oracle_chunk(a) for a in starts]
         sq = math.fsum(sq_parts)
         cr = oracle.clip(sq, 0.0, wl.max_norm)
         assert res.finite == cr.finite

@@ -2,9 +2,9 @@
 
 tiny, GPT-2 ZeRO-1 and the ragged stress run at full size with the whole
 shard compared after every step; Llama-7B and the Llama-13B ZeRO-3 shard run
-at full size with every grad in the norm and a seeded sample of shard
-positions compared, and their full step counts run on shape-preserving
-smaller lists with the whole shard compared.
+at full size for their full step counts (5 and 20) with every grad in the
+norm and a seeded sample of shard positions compared after every step, and
+again on shape-preserving smaller lists with the whole shard compared.
 """
 import math
 
@@ -29,6 +29,10 @@ def _summary(rep):
     exact = sum(s.exact for s in rep.steps)
     worst = max(abs(s.gpu_norm - s.ref_norm) / s.ref_norm for s in rep.steps)
     print(f"{rep.name}: n={rep.n} steps={len(rep.steps)} bit-exact steps={exact} worst norm rel err={worst:.2e}")
+    for s in rep.steps:
+        print(f"  step {s.t}: norm gpu={s.gpu_norm:.17g} oracle={s.ref_norm:.17g} "
+              f"rel err={abs(s.gpu_norm - s.ref_norm) / s.ref_norm:.2e} coef gpu={s.gpu_coef!r} "
+              f"oracle={s.ref_coef!r} bit-exact={s.exact}")
 
 
 def test_tiny_full():
@@ -57,10 +61,13 @@ def test_ragged_rank2_full():
     _summary(rep)
 
 
-def test_llama7b_full_size_sampled():
+def test_llama7b_full_size_all_steps_sampled():
+    """The configuration as stated: 6,738,415,616 params, all 5 steps, every grad in the
+    oracle's norm, a seeded sample of 1M shard positions compared after every step."""
     wl = W.llama7b()
-    rep = run_workload(wl, steps=2, sample=1_000_000)
-    assert rep.n == 6738415616
+    rep = run_workload(wl, steps=wl.steps, sample=1_000_000)
+    assert rep.n == 6738415616 and len(rep.steps) == 5
+    assert all(s.ref_coef < 1.0 for s in rep.steps), "clipping expected to trigger"
     _summary(rep)
 
 
@@ -82,11 +89,13 @@ def test_llama7b_shape_all_steps():
     _summary(rep)
 
 
-def test_llama13b_zero3_rank7_full_size_sampled():
+def test_llama13b_zero3_rank7_full_size_all_steps_sampled():
+    """The configuration as stated: rank 7's 1,626,983,040 params, 8 fp16 micro-batches per
+    step, all 20 steps, every grad in the oracle's norm, 1M shard positions compared."""
     wl = W.llama13b_zero3()
-    rep = run_workload(wl, steps=1, sample=1_000_000)
-    assert rep.n == 1626983040
-    assert rep.steps[0].ref_coef < 1.0
+    rep = run_workload(wl, steps=wl.steps, sample=1_000_000)
+    assert rep.n == 1626983040 and len(rep.steps) == 20
+    assert all(s.ref_coef < 1.0 for s in rep.steps), "clipping expected to trigger"
     _summary(rep)
 
 

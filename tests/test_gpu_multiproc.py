@@ -1,0 +1,125 @@
+"""The product's multi-rank step across real processes: two ranks on one GPU.
+
+Two processes, one rank each, both on cuda:0, exchange through a gloo
+process group (the ranks' only exchange is the 8-byte local sum of squares
+of ZeRO-2/3 global grad-norm clipping; gloo stages it through host memory).
+No kernel waits on another rank: each process runs its own kernels and the
+exchange happens on the host between them.  Each rank steps its own shard
+with ``FlatShardAdamW.step(process_group=...)`` (flatten with the fused norm
+first) or ``step_tensors(process_group=...)``, on a side stream rather than
+torch's current stream, for four steps; at step 3 a grad inside rank 1's
+shard is infinite, so both ranks must skip that step together.  Every rank's
+norm, coefficient and skip decision must be the same, and every rank's state
+must equal the oracle's global-norm step bit for bit.
+"""
+import datetime
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+pytestmark = pytest.mark.gpu
+WORLD = 2
+STEPS = 4
+BAD_STEP = 3
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _workload():
+    import workloads as W
+    return W.small_ragged(n_tensors=300, world_size=WORLD, rank=0, max_norm=0.5)
+
+
+def _grads(wl, t, dev):
+    import workloads as W
+    tg = W.tensor_grads(wl, t, 0, device=dev)
+    if t == BAD_STEP:
+        tg.tensors[-1][0] = float("inf")  # the last tensor lies in rank 1's shard
+    return tg
+
+
+def _rank_main(rank, port, mode, results):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=WORLD, timeout=datetime.timedelta(seconds=180))
+    try:
+        import workloads as W
+        from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
+        dev = torch.device("cuda:0")
+        torch.cuda.set_device(dev)
+        wl = _workload().with_(rank=rank)
+        opt = FlatShardAdamW(wl.numels, world_size=WORLD, rank=rank, lr=wl.lr, betas=wl.betas, eps=wl.eps,
+                             weight_decay=wl.weight_decay, max_norm=wl.max_norm, device=dev, master=None)
+        opt.master.copy_(W.master_init(wl, opt.start, opt.end))
+        side = torch.cuda.Stream(device=dev)
+        norms = []
+        for t in range(1, STEPS + 1):
+            tg = _grads(wl, t, dev)
+            side.wait_stream(torch.cuda.current_stream(dev))  # the grads were written on the current stream
+            if mode == "step":
+                opt.flatten(tg.tensors, accumulate=False, fuse_norm=True, stream=side)
+                r = opt.step(stream=side, process_group=dist.group.WORLD)
+            else:
+                r = opt.step_tensors(tg.tensors, stream=side, process_group=dist.group.WORLD)
+            norms.append((r.sqnorm, r.norm, r.clip_coef, r.finite, opt.t))
+        torch.cuda.synchronize(dev)
+        results[rank] = {"norms": norms, "range": (opt.start, opt.end),
+                         **{k: getattr(opt, k).cpu().view(torch.int32 if k != "lowp" else torch.int16)
+                            .numpy().tobytes() for k in ("master", "exp_avg", "exp_avg_sq", "lowp")}}
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("mode", ["step", "step_tensors"])
+def test_two_processes_global_norm_step(mode):
+    import oracle
+    from _helpers import raw
+    from fsdp_sharded_mixed_flatparameter_gb300 import build
+    import workloads as W
+    build.build()  # once, before the ranks start (they only load it)
+    ctx = mp.get_context("spawn")
+    results = ctx.Manager().dict()
+    mp.start_processes(_rank_main, args=(_free_port(), mode, results), nprocs=WORLD, start_method="spawn", join=True)
+    r0, r1 = results[0], results[1]
+    # every rank saw the same norm, coefficient and skip decision at every step
+    assert r0["norms"] == r1["norms"]
+    assert [x[3] for x in r0["norms"]] == [t != BAD_STEP for t in range(1, STEPS + 1)]
+    assert [x[4] for x in r0["norms"]] == [1, 2, 2, 3]
+
+    wl = _workload()
+    states = {}
+    for rank, res in ((0, r0), (1, r1)):
+        s, e = oracle.shard_range(wl.total, WORLD, rank)
+        assert tuple(res["range"]) == (s, e)
+        states[rank] = oracle.new_state(raw(W.master_init(wl, s, e)))
+    for t in range(1, STEPS + 1):
+        tg = _grads(wl, t, torch.device("cuda:0"))  # the ranks' draws (CPU and CUDA generators differ)
+        full = np.zeros(wl.total, np.float32)
+        oracle.flatten([raw(x) for x in tg.tensors], wl.numels, "bf16", 0, wl.total, 1.0, full, False)
+        cr = oracle.clip(oracle.sqnorm(full), 0.0, wl.max_norm)
+        sq, nv, coef, fin, _ = r0["norms"][t - 1]
+        assert fin == cr.finite
+        if not cr.finite:
+            continue
+        assert abs(nv - cr.norm) <= 1e-12 * cr.norm and coef == cr.coef
+        for rank in (0, 1):
+            st = states[rank]
+            s, e = oracle.shard_range(wl.total, WORLD, rank)
+            st.t += 1
+            sc = oracle.adamw_scalars(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay, st.t)
+            oracle.adamw(st.p, st.m, st.v, np.ascontiguousarray(full[s:e]), sc, cr.coef, st.lowp)
+    for rank, res in ((0, r0), (1, r1)):
+        st = states[rank]
+        assert st.t == 3
+        assert res["master"] == st.p.tobytes(), f"rank {rank} master"
+        assert res["exp_avg"] == st.m.tobytes(), f"rank {rank} exp_avg"
+        assert res["exp_avg_sq"] == st.v.tobytes(), f"rank {rank} exp_avg_sq"
+        assert res["lowp"] == st.lowp.tobytes(), f"rank {rank} lowp"
