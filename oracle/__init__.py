@@ -56,6 +56,7 @@ def lib() -> ctypes.CDLL:
             L.orc_flat_offsets.argtypes = [vp, i32, vp]
             L.orc_flatten.argtypes = [vp, vp, i32, ctypes.c_int, i64, i64, f32, ctypes.c_int, vp, vp]
             L.orc_accum.argtypes = [vp, vp, ctypes.c_int, i64, f32, ctypes.c_int, vp]
+            L.orc_reduce_chunks.argtypes = [vp, vp, ctypes.c_int, i32, i64, i64, f32, ctypes.c_int, vp]
             L.orc_sqnorm.argtypes = [vp, i64]
             L.orc_sqnorm.restype = f64
             L.orc_clip.argtypes = [f64, f64, f64, ctypes.POINTER(f64), ctypes.POINTER(f64),
@@ -127,6 +128,18 @@ def accum(acc: np.ndarray, src: np.ndarray, dtype: str, scale: float, accumulate
     assert src.size == acc.size
     flag = np.zeros(1, dtype=np.int32)
     lib().orc_accum(_p(acc), _p(src), DTYPE_CODE[dtype], acc.size, scale, int(bool(accumulate)), _p(flag))
+    return bool(flag[0])
+
+
+def reduce_chunks(acc: np.ndarray, chunks: np.ndarray, dtype: str, n: int, scale: float, accumulate: bool) -> bool:
+    """acc[0:n] (+)= sum over r in rank order of scale * chunks[r, 0:n] (a 2-D array of
+    n_chunks blocks); returns True if a non-finite scaled value was met."""
+    _c(acc, np.float32)
+    assert chunks.ndim == 2 and chunks.flags.c_contiguous and chunks.dtype in (np.float32, np.uint16)
+    assert acc.size >= n and chunks.shape[1] >= n
+    flag = np.zeros(1, dtype=np.int32)
+    lib().orc_reduce_chunks(_p(acc), _p(chunks), DTYPE_CODE[dtype], chunks.shape[0], chunks.shape[1], n, scale,
+                            int(bool(accumulate)), _p(flag))
     return bool(flag[0])
 
 

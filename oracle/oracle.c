@@ -183,6 +183,27 @@ void orc_accum(float* acc, const void* src, int dtype, int64_t n, float scale, i
   }
 }
 
+/* The local half of a ZeRO-2/3 reduce-scatter ([ZeRO-NPU] section "ZeRO-2:
+ * 附加切分梯度", ZeRO2Optimizer.reduce_gradients: the ranks' flat grads are
+ * summed, each rank keeps its chunk, then divides it by world_size; [Mem-FSDP]
+ * FSDP MixedPrecision: reduce_dtype fp32, because summing in bf16 loses
+ * accuracy).  `chunks` holds n_chunks blocks of `stride` elements; block r is
+ * rank r's grad values over this rank's shard, as an exchange delivers them.
+ * The first n values of every block are added into acc in rank order, each
+ * scaled first, with the orc_accum rule:
+ *   acc = (accumulate ? acc : 0-free) + scale*x_0 + scale*x_1 + ...
+ * With scale = 1/world_size (a power of two for the usual world sizes)
+ * scaling each term first is exactly dividing the sum afterwards, away from
+ * subnormals, so this is the page's sum-then-divide carried out in binary32
+ * in rank order. */
+void orc_reduce_chunks(float* acc, const void* chunks, int dtype, int32_t n_chunks, int64_t stride, int64_t n,
+                       float scale, int accumulate, int32_t* nonfinite) {
+  const size_t es = (dtype == ORC_F32) ? 4u : 2u;
+  for (int32_t r = 0; r < n_chunks; ++r)
+    orc_accum(acc, (const char*)chunks + (size_t)r * (size_t)stride * es, dtype, n, scale, accumulate || r > 0,
+              nonfinite);
+}
+
 /* ------------------------------------------------------------- grad norm */
 
 /* Sum of squares of n binary32 values (clip_grad_norm_ in [ZeRO-NPU] section

@@ -271,6 +271,85 @@ def test_accum_first_overwrites():
     assert np.array_equal(acc, src * np.float32(0.5))
 
 
+# ------------------------------------------------ ZeRO-2/3 reduce-scatter (NEXT-2)
+def _padded_rank_blocks(grads, world):
+    """Rank q's received blocks: block r = rank r's flat grad over q's chunk (padded to world*chunk)."""
+    total = grads[0].size
+    chunk = -(-total // world)
+    padded = [np.concatenate([g, np.zeros(world * chunk - total, g.dtype)]) for g in grads]
+    return chunk, [np.ascontiguousarray(np.stack([p[q * chunk:(q + 1) * chunk] for p in padded])) for q in range(world)]
+
+
+@pytest.mark.parametrize("world", [2, 4, 8])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_reduce_chunks_is_reduce_scatter_then_divide(world, dtype):
+    """The ZeRO page's ZeRO-2 reduce_gradients: reduce_scatter_tensor(SUM) of the ranks'
+    flat grads, then /= world_size.  Concatenating every rank's reduced chunk equals the
+    ranks' grads summed in rank order by torch in float32, divided by world_size, bit for
+    bit (scaling each term by the power of two 1/world first is exact)."""
+    rng = np.random.default_rng(40 + world)
+    total = 10_007  # not a multiple of any world size: a short last chunk
+    g32 = [(rng.standard_normal(total) * 1e-3).astype(np.float32) for _ in range(world)]
+    conv = {"f32": lambda x: x, "bf16": oracle.bf16_rne, "f16": oracle.f16_rne}[dtype]
+    raws = [conv(g) for g in g32]
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+    as_t = (lambda r: torch.from_numpy(r)) if dtype == "f32" else \
+        (lambda r: torch.from_numpy(r.view(np.int16)).view(tdt))
+    ref = as_t(raws[0]).float()
+    for r in raws[1:]:
+        ref = ref + as_t(r).float()  # one binary32 add per rank, rank order
+    ref = (ref / world).numpy()
+    chunk, blocks = _padded_rank_blocks(raws, world)
+    got = []
+    for q in range(world):
+        s, e = oracle.shard_range(total, world, q)
+        assert s == min(q * chunk, total)
+        acc = np.full(max(e - s, 1), np.nan, np.float32)
+        assert not oracle.reduce_chunks(acc, blocks[q], dtype, e - s, 1.0 / world, accumulate=False)
+        got.append(acc[:e - s])
+    assert np.array_equal(np.concatenate(got), ref)
+
+
+def test_reduce_chunks_accumulate_and_rank_order():
+    """accumulate adds every rank's scaled value to the existing accumulator in rank order
+    (micro-batches reduced one after another); checked against torch float32 adds in that
+    order, with values whose sums depend on the order."""
+    rng = np.random.default_rng(5)
+    n, world = 513, 3
+    acc0 = (rng.standard_normal(n) * 1e3).astype(np.float32)
+    blocks = np.ascontiguousarray(np.stack([(rng.standard_normal(n + 7) * 10.0 ** k).astype(np.float32)
+                                            for k in (3, -4, 1)]))
+    scale = 0.3  # not a power of two: every product rounds
+    acc = acc0.copy()
+    oracle.reduce_chunks(acc, blocks, "f32", n, scale, accumulate=True)
+    ref = torch.from_numpy(acc0.copy())
+    sc = torch.tensor(scale, dtype=torch.float32)
+    for r in range(world):
+        ref = ref + sc * torch.from_numpy(blocks[r, :n].copy())
+    assert np.array_equal(acc, ref.numpy())
+    rev = acc0.copy()
+    oracle.reduce_chunks(rev, np.ascontiguousarray(blocks[::-1]), "f32", n, scale, accumulate=True)
+    assert not np.array_equal(rev, acc), "a different rank order must give different bits here"
+
+
+def test_reduce_chunks_vs_exact_fraction_and_padding():
+    """Every value is within world rounding errors of the exact rational sum; the padding
+    beyond n in every block (NaN here) is never read; an inf inside the range raises the flag."""
+    rng = np.random.default_rng(6)
+    n, world, stride = 48, 5, 53
+    blocks = np.full((world, stride), np.nan, np.float32)
+    blocks[:, :n] = (rng.standard_normal((world, n)) * 10.0 ** rng.uniform(-5, 2, (world, 1))).astype(np.float32)
+    scale = np.float32(1.0 / 3.0)
+    acc = np.zeros(n, np.float32)
+    assert not oracle.reduce_chunks(acc, blocks, "f32", n, float(scale), accumulate=False)
+    for k in range(n):
+        terms = [Fraction(float(scale)) * Fraction(float(blocks[r, k])) for r in range(world)]
+        err = abs(Fraction(float(acc[k])) - sum(terms))
+        assert err <= sum(abs(t) for t in terms) * Fraction(2 * world, 2**24), k
+    blocks[3, 7] = np.inf
+    assert oracle.reduce_chunks(acc, blocks, "f32", n, float(scale), accumulate=False)
+
+
 # ----------------------------------------------------------- A5 grad norm + clip
 def test_sqnorm_closed_form_all_equal():
     """sum of n copies of c^2 is n*c^2 exactly when that is representable."""
