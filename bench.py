@@ -9,7 +9,14 @@ One step = the whole hot path over one batch of synthetic grads:
 Inputs are resident in HBM (135 GB, far larger than the 129 MB L2, so no
 flush is needed between steps).  Prints one JSON line.
 
+With N > 1 ranks (torchrun, one per GPU) the step is the ZeRO-2 data plane
+over Llama-7B (strong scaling): all-to-all of the flat bf16 grads, rank-order
+fp32 reduction with the fused norm, global norm, AdamW on the shard, all-gather
+of the bf16 parameters.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py --workload NAME         another configuration's step
+  python bench.py --dataplane-ranks N     one rank of an N-rank ZeRO-2 job
 
 --impl reference times the CPU oracle (plain single-threaded C) on a bounded
 sample of the same workload on the host cores.
@@ -278,30 +285,21 @@ def run_reference(args):
 
 # ------------------------------------------------------------------------ GPU
 def run_gpu(args):
-    from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW, gather_sqnorms
+    """The headline line: Llama-7B as one rank (N = 1)."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
     from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
+    world, rank = 1, 0
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world != args.gpus:
-        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-        pg = dist
 
     base = W.llama7b()
     if args.small:
         # profiling case: same tensor shapes per layer, 1 layer, smaller vocab (268M params,
         # ~5 GB on the device, still far larger than L2)
         base = base.with_(name="llama7b_1layer_v8000", numels=tuple(W.llama_numels(1, 4096, 11008, 8000)))
-    # weak scaling: the flat parameter list is `world` copies of the Llama-7B
-    # list, so every rank's ZeRO shard is exactly one Llama-7B-shaped buffer
-    wl = base.with_(numels=base.numels * world, world_size=world, rank=rank)
+    wl = base
     s, e = zs.zero_shard_range(wl.total, world, rank)
     n = e - s
     shard_numels = list(base.numels)
@@ -318,18 +316,9 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     grad_bytes = sum(t.numel() * t.element_size() for t in grads)
 
-    local_buf = zs.new_norm_result(dev)
-
     def norm_stage():
-        """Norm + clip coefficient from the fused partials.  With several ranks the
-        norm is global: the ranks all-gather their 8-byte local sums of squares and
-        every rank combines them in rank order (the step's only exchange)."""
-        if pg is None:
-            zs.zero_grad_sqnorm_finalize(opt.ws, n, 0.0, opt.max_norm, opt.norm_buf, stream)
-        else:
-            zs.zero_grad_sqnorm_finalize(opt.ws, n, 0.0, math.inf, local_buf, stream)
-            gathered = gather_sqnorms(zs.sqnorm_view(local_buf), None)
-            zs.zero_grad_sqnorm_combine(gathered, opt.max_norm, opt.norm_buf, stream)
+        """Norm + clip coefficient from the partials the flatten pass fused in."""
+        zs.zero_grad_sqnorm_finalize(opt.ws, n, 0.0, opt.max_norm, opt.norm_buf, stream)
 
     def one_step(ev=None):
         if ev is not None:
@@ -352,8 +341,6 @@ def run_gpu(args):
 
     def barrier():
         torch.cuda.synchronize(dev)
-        if pg is not None:
-            pg.barrier()
 
     for _ in range(args.warmup):
         one_step()
@@ -420,7 +407,7 @@ def run_gpu(args):
     def user_step(step_grads):
         """The calls a user makes: FlatShardAdamW.flatten (fused norm) + step()."""
         opt.flatten(step_grads, accumulate=False, fuse_norm=True, stream=stream)
-        r = opt.step(stream=stream, process_group=None if pg is None else pg.group.WORLD)
+        r = opt.step(stream=stream)
         if not r.finite:
             raise RuntimeError("non-finite grad norm in the benchmark")
 
@@ -445,15 +432,6 @@ def run_gpu(args):
 
     e2e_ms = timed(one_step_host)
     e2e_copy_ms = timed(one_step_copy_engine)
-
-    if pg is not None:
-        t = torch.tensor([elapsed_ms, e2e_ms, e2e_copy_ms, direct_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_ms, e2e_ms, e2e_copy_ms, direct_ms = t.tolist()
-    if rank != 0:
-        if pg is not None:
-            pg.destroy_process_group()
-        return 0
 
     peaks, peak_src = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
@@ -484,22 +462,200 @@ def run_gpu(args):
                                         "adamw_tensors": 28 * n / (statistics.mean(dk4) / 1e3) / 1e9},
                         "what": "no micro-batch accumulation: norm and AdamW read the bf16 grads through the "
                                 "tensor table, the fp32 flat grad is never written; bit-identical results"},
-        "gpu_launches": (3 if world == 1 else 4) * args.steps,
+        "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
         "e2e": {"value": n * world * args.steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": grad_bytes,
                 "d2h_bytes_per_step": zs.NORM_RESULT_BYTES, "ms_per_step": e2e_ms / args.steps,
                 "how": "bf16 grads in pinned host memory read by the flatten kernel over the host link",
                 "copy_engine_ms_per_step": e2e_copy_ms / args.steps},
     }
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline:
         rate, tot, passes, el = oracle_step_rate(base, 1 << 25, 10.0, 50)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"first {tot} params of the Llama-7B flat list, {passes} whole-step "
                                           f"passes in {el:.1f} s",
                                 "stages_elems_per_s": oracle_step_rate.last_stages}
     print(json.dumps(line))
-    if pg is not None:
-        pg.destroy_process_group()
+    return 0
+
+
+# ------------------------------------------------------- ZeRO-2/3 data plane
+def run_dataplane(args):
+    """Llama-7B trained by N ranks with the ZeRO-2 data plane (strong scaling: the
+    model is fixed and each rank owns 1/N of it, the ZeRO page's Llama-7B-on-8-cards
+    setting).  One step per rank:
+      exchange   all-to-all of the padded flat bf16 grad (NCCL): each rank receives
+                 every rank's chunk of its shard
+      reduce     zero_reduce_chunks: rank-order fp32 sum, x 1/N, fused norm partials
+      norm       local finalize, 8-byte all-gather of the ranks' sums, combine
+      adamw      fused AdamW on the shard, bf16 write-back into the rank's slice
+      all-gather the ranks' bf16 slices into every rank's full FlatParameter
+      read       the 24-byte norm result (skip decision)
+    With one process and --dataplane-ranks N it times one rank of an N-rank job on
+    this GPU: the received blocks are synthetic (every rank's grads as they would
+    arrive), the exchange and both all-gathers are left out (nothing to exchange
+    with) and the other ranks' sums of squares are stood in by copies of this
+    rank's; the line says so.  When ranks share GPUs (fewer devices than ranks)
+    they exchange through gloo on host memory: a check of the code path, marked
+    as such, not a bench number."""
+    import torch.distributed as dist
+    from fsdp_sharded_mixed_flatparameter_gb300 import (ZeroDataPlane, exchange_chunks, gather_shards,
+                                                        gather_sqnorms, zero_shard as zs)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    ndev = torch.cuda.device_count()
+    shared = world > 1 and ndev < world
+    dev = torch.device("cuda", local % ndev)
+    torch.cuda.set_device(dev)
+    group = None
+    if world > 1:
+        if shared:
+            dist.init_process_group("gloo")
+        else:
+            dist.init_process_group("nccl", device_id=dev)
+        group = dist.group.WORLD
+    N = world if world > 1 else args.dataplane_ranks
+    r = rank if world > 1 else 0
+    wl = W.llama7b()
+    if args.small:
+        wl = wl.with_(name="llama7b_1layer_v8000", numels=tuple(W.llama_numels(1, 4096, 11008, 8000)))
+    total = wl.total
+    s, e = zs.zero_shard_range(total, N, r)
+    n = e - s
+    stream = torch.cuda.current_stream(dev)
+    master = W.master_init(wl, s, e, device=dev)
+    if world > 1:
+        dp = ZeroDataPlane(wl.numels, group=group, device=dev, lr=wl.lr, betas=wl.betas, eps=wl.eps,
+                           weight_decay=wl.weight_decay, max_norm=wl.max_norm, master=master)
+        opt, chunk = dp.opt, dp.chunk
+        dp.flat_grad[:total] = W.flat_grads(wl.with_(seed=wl.seed + rank), 1, 0, 0, total, device=dev)
+        recv2d = dp.recv.view(N, chunk)
+    else:
+        from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW, chunk_layout
+        dp = None
+        chunk, _ = chunk_layout(total, N)
+        opt = FlatShardAdamW(wl.numels, world_size=N, rank=r, lr=wl.lr, betas=wl.betas, eps=wl.eps,
+                             weight_decay=wl.weight_decay, max_norm=wl.max_norm, device=dev, master=master)
+        recv2d = torch.zeros(N, chunk, dtype=torch.bfloat16, device=dev)
+        for j in range(N):  # rank j's values of this rank's shard
+            recv2d[j, :n] = W.flat_grads(wl.with_(seed=wl.seed + j), 1, 0, s, e, device=dev)
+    del master
+    local_buf = zs.new_norm_result(dev)
+    NEV = 6
+
+    def one_step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        if dp is not None:
+            exchange_chunks(dp.flat_grad, dp.recv, group)
+        mark(1)
+        zs.zero_reduce_chunks(opt.grad, recv2d, n, 1.0 / N, False, None, opt.ws, stream)
+        mark(2)
+        zs.zero_grad_sqnorm_finalize(opt.ws, n, 0.0, math.inf, local_buf, stream)
+        local_sq = zs.sqnorm_view(local_buf)
+        gathered = gather_sqnorms(local_sq, group) if dp is not None else local_sq.repeat(N)
+        zs.zero_grad_sqnorm_combine(gathered, opt.max_norm, opt.norm_buf, stream)
+        mark(3)
+        zs.zero_adamw_step(opt.master, opt.exp_avg, opt.exp_avg_sq, opt.grad, opt.lowp, opt.lr, opt.betas[0],
+                           opt.betas[1], opt.eps, opt.weight_decay, opt.t + 1, opt.norm_buf, stream)
+        mark(4)
+        if dp is not None:
+            gather_shards(dp.flat_param, group)
+        mark(5)
+        res = opt.finish_step(stream)
+        if not res.finite:
+            raise RuntimeError("non-finite grad norm in the benchmark")
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if group is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        one_step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(NEV)] for _ in range(args.steps)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(dev.index) as clk:
+        a.record(stream)
+        for k in range(args.steps):
+            one_step(evs[k])
+        b.record(stream)
+        barrier()
+    elapsed_ms = a.elapsed_time(b)
+    parts = {name: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in evs)
+             for i, name in enumerate(("exchange", "reduce", "norm", "adamw", "all_gather"))}
+
+    e2e_ms, h2d = None, 0
+    if dp is not None:
+        # end to end through the public API: the step's grads come from pinned host memory
+        host = torch.empty(dp.flat_grad.numel(), dtype=dp.flat_grad.dtype, pin_memory=True)
+        host.copy_(dp.flat_grad)
+        h2d = host.numel() * host.element_size()
+
+        def user_step():
+            dp.flat_grad.copy_(host, non_blocking=True)
+            dp.reduce_scatter_grads()
+            if not dp.step().finite:
+                raise RuntimeError("non-finite grad norm in the benchmark")
+        user_step()
+        barrier()
+        a.record(stream)
+        for _ in range(args.steps):
+            user_step()
+        b.record(stream)
+        barrier()
+        e2e_ms = a.elapsed_time(b)
+    if group is not None:
+        t = torch.tensor([elapsed_ms, e2e_ms or 0.0] + list(parts.values()), dtype=torch.float64)
+        if not shared:
+            t = t.to(dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        vals = t.tolist()
+        elapsed_ms, e2e_ms = vals[0], vals[1]
+        parts = dict(zip(parts, vals[2:]))
+        if rank != 0:
+            dist.destroy_process_group()
+            return 0
+    peaks, peak_src = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    adamw_gbs = ADAMW_BYTES_PER_PARAM * n / (parts["adamw"] / 1e3) / 1e9
+    reduce_bytes = (2 * N + 4) * n  # N bf16 blocks read, the fp32 shard grad written
+    line = {
+        "metric": METRIC, "value": total * args.steps / (elapsed_ms / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{wl.name} ZeRO-2 over {N} ranks", "params_total": total, "params_per_rank": n,
+                   "ranks": N, "grad_dtype": "bf16", "lowp_dtype": "bf16", "max_norm": wl.max_norm,
+                   "l2": "inputs larger than L2; no flush"},
+        "roofline": {"bound": "hbm", "kernel": "adamw_v8_kernel", "achieved": adamw_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": adamw_gbs / hbm, "peak_source": peak_src, "traffic": None,
+                     "algorithmic_bytes_per_launch": ADAMW_BYTES_PER_PARAM * n},
+        "kernels_ms": parts,
+        "kernels_gbs": {"reduce": reduce_bytes / (parts["reduce"] / 1e3) / 1e9, "adamw": adamw_gbs},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if dp is None:
+        line["value"] = n * args.steps / (elapsed_ms / 1e3)
+        line["emulated"] = (f"one rank of a {N}-rank job on one GPU: the {N} received blocks are synthetic, the "
+                            f"exchange and all-gathers are not run, the other ranks' sums of squares are copies of "
+                            f"this rank's; value = this rank's params/s")
+        line["scaling"] = "weak"
+    else:
+        line["e2e"] = {"value": total * args.steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": zs.NORM_RESULT_BYTES, "ms_per_step": e2e_ms / args.steps,
+                       "how": "ZeroDataPlane.reduce_scatter_grads + step, grads copied from pinned host memory"}
+        if shared:
+            line["emulated"] = "ranks share one GPU and exchange through gloo on host memory: a code-path check"
+    print(json.dumps(line))
+    if group is not None:
+        dist.destroy_process_group()
     return 0
 
 
@@ -688,6 +844,8 @@ def main():
                     help="another configuration's step (a table row, not the headline line)")
     ap.add_argument("--small", action="store_true",
                     help="profiling case for ncu (a smaller list of the same shape), not a bench line")
+    ap.add_argument("--dataplane-ranks", type=int, default=0,
+                    help="with one process: time one rank of an N-rank ZeRO-2 Llama-7B job (reduce, norm, AdamW)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         raise SystemExit("--warmup must be >= 3")
@@ -695,6 +853,8 @@ def main():
         return run_reference(args)
     if args.workload != "llama7b_flat":
         return run_config(args)
+    if args.gpus > 1 or args.dataplane_ranks > 1:
+        return run_dataplane(args)
     return run_gpu(args)
 
 

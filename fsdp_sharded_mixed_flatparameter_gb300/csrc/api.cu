@@ -133,6 +133,29 @@ zero_status zero_accum(float* d_acc, const void* d_src, zero_dtype src_dtype, in
                           static_cast<double*>(d_norm_ws), zs::as_stream(stream));
 }
 
+zero_status zero_reduce_chunks(float* d_acc, const void* d_chunks, zero_dtype src_dtype, int32_t n_chunks,
+                               int64_t chunk_stride, int64_t n, float scale, int32_t accumulate,
+                               int32_t* d_found_nonfinite, void* d_norm_ws, size_t norm_ws_bytes, void* stream) {
+  if (n < 0) return fail(ZERO_EINVAL, "zero_reduce_chunks: n %lld < 0", (long long)n);
+  if (n_chunks < 1) return fail(ZERO_EINVAL, "zero_reduce_chunks: n_chunks %d < 1", (int)n_chunks);
+  if (chunk_stride < n)
+    return fail(ZERO_EINVAL, "zero_reduce_chunks: chunk_stride %lld < n %lld", (long long)chunk_stride,
+                (long long)n);
+  if (!zs::valid_dtype(src_dtype)) return fail(ZERO_EINVAL, "zero_reduce_chunks: bad src_dtype %d", (int)src_dtype);
+  if (accumulate != 0 && accumulate != 1) return fail(ZERO_EINVAL, "zero_reduce_chunks: accumulate must be 0 or 1");
+  if (!std::isfinite(scale)) return fail(ZERO_EINVAL, "zero_reduce_chunks: non-finite scale");
+  if (n > 0 && (d_acc == nullptr || d_chunks == nullptr)) return fail(ZERO_EINVAL, "zero_reduce_chunks: NULL buffer");
+  const int64_t es = (src_dtype == ZERO_F32) ? 4 : 2;
+  if (chunk_stride > (int64_t(1) << 62) / es / n_chunks)
+    return fail(ZERO_EINVAL, "zero_reduce_chunks: %d chunks of %lld elements exceed 2^62 bytes", (int)n_chunks,
+                (long long)chunk_stride);
+  const zero_status w = check_norm_ws("zero_reduce_chunks", d_norm_ws, norm_ws_bytes, n);
+  if (w != ZERO_OK) return w;
+  if (n == 0) return ZERO_OK;
+  return zs::launch_reduce_chunks(d_acc, d_chunks, src_dtype, n_chunks, chunk_stride, n, scale, accumulate,
+                                  d_found_nonfinite, static_cast<double*>(d_norm_ws), zs::as_stream(stream));
+}
+
 size_t zero_grad_sqnorm_workspace_bytes(int64_t n) {
   if (n <= 0) return 0;
   return static_cast<size_t>((n + zs::kSqTile - 1) / zs::kSqTile) * sizeof(double);

@@ -1,5 +1,6 @@
-// flatten.cu -- gradient flatten/cast into the FlatParameter layout (K1) and
-// flat micro-batch accumulation (K2).
+// flatten.cu -- gradient flatten/cast into the FlatParameter layout (K1),
+// flat micro-batch accumulation (K2) and the local reduction of a ZeRO-2/3
+// reduce-scatter (K2r).
 //
 // K1 implements the ZeRO page's _flatten_gradients (grad.view(-1).float(),
 // zeros for a tensor without grad, concatenated in list order) restricted to
@@ -386,6 +387,129 @@ __global__ void __launch_bounds__(kSqThreads) accum_norm_kernel(float* __restric
   if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
 }
 
+// ------------------------------------------------------------------- K2r
+// The local half of a ZeRO-2/3 reduce-scatter (the ZeRO page's ZeRO-2
+// reduce_gradients: the ranks' flat grads summed, each rank keeping its
+// chunk, divided by world_size; the memory-ledger page: reduce in fp32).
+// An all-to-all exchange has brought every rank's values of this rank's
+// shard here as n_chunks blocks `stride_bytes` apart (block r = rank r's);
+// they are added into the fp32 accumulator in rank order, each scaled
+// first (scale = 1/world_size, times 1/accum_steps when micro-batches are
+// reduced one by one):
+//     acc = (ACC ? acc : first term) + s*x_0 + s*x_1 + ...
+// exactly the rule of n_chunks accumulate passes, but in one pass: every
+// block is read once (2 bytes per element and rank for 16-bit grads) and
+// the accumulator is read (ACC) and written once.  The exchange moves the
+// grads in their own 16-bit type; only the sum is binary32.
+// Work split and fused norm as accum_norm_kernel: one block per 32768-
+// element norm tile; in a tile that is whole and vector-aligned, thread t
+// takes its groups r*256 + t two at a time and loads up to four ranks'
+// blocks of them together (eight 16/32-byte loads in flight per thread)
+// before adding them in rank order; the ragged last tile goes element by
+// element.  NORM adds the squares of the final values in the norm tile
+// contract's order (add8 and add1 give the same bits).
+constexpr int kRcGroups = 2;  // groups of 8 elements a thread carries at a time
+
+template <int DT, int B>
+__device__ __forceinline__ void reduce_batch(float (&a)[kRcGroups][8], const char* __restrict__ src,
+                                             int64_t stride_bytes, const int64_t (&k)[kRcGroups], float scale,
+                                             bool first_is_set, bool& bad) {
+  constexpr int es = SrcTraits<DT>::esize;
+  float x[B][kRcGroups][8];
+#pragma unroll
+  for (int u = 0; u < B; ++u)
+#pragma unroll
+    for (int q = 0; q < kRcGroups; ++q) load8_src<DT>(src + u * stride_bytes + es * k[q], x[u][q]);
+#pragma unroll
+  for (int u = 0; u < B; ++u) {
+    const bool set = first_is_set && u == 0;  // the first rank's value starts the sum (no add: -0 stays -0)
+#pragma unroll
+    for (int q = 0; q < kRcGroups; ++q) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float y = __fmul_rn(scale, x[u][q][i]);
+        bad |= !finite_f(y);
+        a[q][i] = set ? y : __fadd_rn(a[q][i], y);
+      }
+    }
+  }
+}
+
+template <int DT, bool ACC, bool NORM>
+__global__ void __launch_bounds__(kSqThreads) reduce_chunks_kernel(float* __restrict__ acc,
+                                                                   const char* __restrict__ src, int n_chunks,
+                                                                   int64_t stride_bytes, int64_t n, int64_t ntiles,
+                                                                   bool vec, float scale,
+                                                                   int32_t* __restrict__ flag,
+                                                                   double* __restrict__ partials) {
+  __shared__ float2 red[kSqThreads / 32];
+  constexpr int es = SrcTraits<DT>::esize;
+  constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
+  bool bad = false;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    NormAcc nacc;
+    const int64_t base = tile * kSqTile;
+    if (vec && base + kSqTile <= n) {  // block-uniform: every group of the tile is a full vector group
+#pragma unroll 1
+      for (int r0 = 0; r0 < kSqVecPerThread; r0 += kRcGroups) {
+        float a[kRcGroups][8];
+        int64_t k[kRcGroups];
+        bool ok = true;
+#pragma unroll
+        for (int q = 0; q < kRcGroups; ++q) {
+          k[q] = base + (static_cast<int64_t>(r0 + q) * kSqThreads + threadIdx.x) * 8;
+          ok = ok && ZS_CHECK(k[q] + 8 <= n && aligned(acc + k[q], 32) && aligned(src + es * k[q], vb), 27, k[q]);
+        }
+        if (!ok) continue;  // (debug build only)
+#pragma unroll
+        for (int q = 0; q < kRcGroups; ++q) {
+          if (ACC) {
+            ld8_rw(acc + k[q], a[q]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[q][i] = 0.0f;
+          }
+        }
+        int c = 0;
+#pragma unroll 1
+        for (; c + 4 <= n_chunks; c += 4)
+          reduce_batch<DT, 4>(a, src + c * stride_bytes, stride_bytes, k, scale, !ACC && c == 0, bad);
+        if (c + 2 <= n_chunks) {
+          reduce_batch<DT, 2>(a, src + c * stride_bytes, stride_bytes, k, scale, !ACC && c == 0, bad);
+          c += 2;
+        }
+        if (c < n_chunks) reduce_batch<DT, 1>(a, src + c * stride_bytes, stride_bytes, k, scale, !ACC && c == 0, bad);
+#pragma unroll
+        for (int q = 0; q < kRcGroups; ++q) {
+          if (NORM) nacc.add8(a[q]);
+          st8(acc + k[q], a[q]);
+        }
+      }
+    } else {  // the ragged last tile, or buffers without the vector alignment: element by element
+      for (int r = 0; r < kSqVecPerThread; ++r) {
+        const int64_t k = base + (static_cast<int64_t>(r) * kSqThreads + threadIdx.x) * 8;
+        for (int i = 0; i < 8 && k + i < n; ++i) {
+          const int64_t j = k + i;
+          if (!ZS_CHECK(j >= 0 && j < n, 28, j)) continue;
+          float o = ACC ? acc[j] : 0.0f;
+          for (int c = 0; c < n_chunks; ++c) {
+            const float y = __fmul_rn(scale, load_elem<DT>(src + c * stride_bytes, j));
+            bad |= !finite_f(y);
+            o = (!ACC && c == 0) ? y : __fadd_rn(o, y);
+          }
+          if (NORM) nacc.add1(i, o);
+          acc[j] = o;
+        }
+      }
+    }
+    if (NORM) {
+      const double bs = block_sum_norm<kSqThreads>(nacc, red);
+      if (threadIdx.x == 0 && ZS_CHECK(tile < ntiles, 29, tile)) partials[tile] = bs;
+    }
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
+}
+
 ZS_DEBUG_UNIT(flatten)
 
 template <int DT, bool ACC>
@@ -429,6 +553,46 @@ zero_status launch_accum(float* acc, const void* src, int src_dtype, int64_t n, 
     case ZERO_BF16 * 2 + 1: return launch_accum_n<ZERO_BF16, true>(acc, src, n, scale, flag, partials, st);
     case ZERO_F16 * 2: return launch_accum_n<ZERO_F16, false>(acc, src, n, scale, flag, partials, st);
     default: return launch_accum_n<ZERO_F16, true>(acc, src, n, scale, flag, partials, st);
+  }
+}
+
+template <int DT, bool ACC, bool NORM>
+static zero_status launch_reduce_chunks_t(float* acc, const void* src, int n_chunks, int64_t stride, int64_t n,
+                                          float scale, int32_t* flag, double* partials, cudaStream_t st) {
+  constexpr int64_t es = SrcTraits<DT>::esize;
+  constexpr uintptr_t vb = (DT == ZERO_F32) ? 32 : 16;
+  const int64_t stride_bytes = stride * es;
+  const bool vec = aligned(acc, 32) && aligned(src, vb) && stride_bytes % static_cast<int64_t>(vb) == 0;
+  const int64_t ntiles = (n + kSqTile - 1) / kSqTile;
+  reduce_chunks_kernel<DT, ACC, NORM><<<one_pass_blocks(ntiles, 1), kSqThreads, 0, st>>>(
+      acc, static_cast<const char*>(src), n_chunks, stride_bytes, n, ntiles, vec, scale, flag, partials);
+  return check_launch("reduce_chunks_kernel");
+}
+
+template <int DT, bool ACC>
+static zero_status launch_reduce_chunks_n(float* acc, const void* src, int n_chunks, int64_t stride, int64_t n,
+                                          float scale, int32_t* flag, double* partials, cudaStream_t st) {
+  if (partials != nullptr)
+    return launch_reduce_chunks_t<DT, ACC, true>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
+  return launch_reduce_chunks_t<DT, ACC, false>(acc, src, n_chunks, stride, n, scale, flag, nullptr, st);
+}
+
+zero_status launch_reduce_chunks(float* acc, const void* src, int src_dtype, int n_chunks, int64_t stride, int64_t n,
+                                 float scale, int accumulate, int32_t* flag, double* partials, cudaStream_t st) {
+  if (n <= 0) return ZERO_OK;
+  switch (src_dtype * 2 + (accumulate ? 1 : 0)) {
+    case ZERO_F32 * 2:
+      return launch_reduce_chunks_n<ZERO_F32, false>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
+    case ZERO_F32 * 2 + 1:
+      return launch_reduce_chunks_n<ZERO_F32, true>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
+    case ZERO_BF16 * 2:
+      return launch_reduce_chunks_n<ZERO_BF16, false>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
+    case ZERO_BF16 * 2 + 1:
+      return launch_reduce_chunks_n<ZERO_BF16, true>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
+    case ZERO_F16 * 2:
+      return launch_reduce_chunks_n<ZERO_F16, false>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
+    default:
+      return launch_reduce_chunks_n<ZERO_F16, true>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
   }
 }
 

@@ -59,6 +59,11 @@ zero_status launch_flatten(const zero_tensor* table, int32_t n_tensors, int src_
 zero_status launch_accum(float* acc, const void* src, int src_dtype, int64_t n, float scale, int accumulate,
                          int32_t* flag, double* partials, cudaStream_t st);
 
+// The ranks' received blocks of this rank's shard (n_chunks blocks, `stride`
+// elements apart) added into acc in rank order, each scaled first.
+zero_status launch_reduce_chunks(float* acc, const void* src, int src_dtype, int n_chunks, int64_t stride, int64_t n,
+                                 float scale, int accumulate, int32_t* flag, double* partials, cudaStream_t st);
+
 zero_status launch_sqnorm(const float* g, int64_t n, double extra_sqnorm, double max_norm, double* partials,
                           zero_norm_result* out, cudaStream_t st);
 

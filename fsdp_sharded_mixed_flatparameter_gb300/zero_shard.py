@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
     sz = ctypes.c_size_t
     L.zero_flatten_cast.argtypes = [vp, i32, i64, ctypes.c_int, i64, i64, f32, i32, vp, vp, vp, sz, vp]
     L.zero_accum.argtypes = [vp, vp, ctypes.c_int, i64, f32, i32, vp, vp, sz, vp]
+    L.zero_reduce_chunks.argtypes = [vp, vp, ctypes.c_int, i32, i64, i64, f32, i32, vp, vp, sz, vp]
     L.zero_grad_sqnorm_finalize.argtypes = [vp, i64, f64, f64, vp, vp]
     L.zero_grad_sqnorm_combine.argtypes = [vp, i32, f64, vp, vp]
     L.zero_grad_sqnorm_workspace_bytes.argtypes = [i64]
@@ -103,7 +104,8 @@ def lib() -> ctypes.CDLL:
     L.zero_status_string.restype = ctypes.c_char_p
     L.zero_last_error.argtypes = []
     L.zero_last_error.restype = ctypes.c_char_p
-    for nm in ("zero_shard_range", "zero_tensor_table", "zero_flatten_cast", "zero_accum", "zero_grad_sqnorm",
+    for nm in ("zero_shard_range", "zero_tensor_table", "zero_flatten_cast", "zero_accum", "zero_reduce_chunks",
+               "zero_grad_sqnorm",
                "zero_grad_sqnorm_finalize", "zero_grad_sqnorm_combine", "zero_grad_sqnorm_noalloc",
                "zero_adamw_step", "zero_adamw_step_tensors", "zero_loss_scale_update", "zero_adamw_scalars",
                "zero_adamw_prepare_device", "zero_adamw_step_device", "zero_adamw_step_tensors_device",
@@ -224,6 +226,23 @@ def zero_accum(acc: torch.Tensor, src: torch.Tensor, scale: float, accumulate: b
                             int(bool(accumulate)),
                             _dev(found_nonfinite, "found_nonfinite", torch.int32, allow_none=True),
                             _dev(norm_ws, "norm_ws", allow_none=True), _ws_bytes(norm_ws), _stream(stream)))
+
+
+def zero_reduce_chunks(acc: torch.Tensor, chunks: torch.Tensor, n: int, scale: float, accumulate: bool,
+                       found_nonfinite: Optional[torch.Tensor] = None, norm_ws: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    """acc[0:n] (+)= the rank-order sum of scale * chunks[r, 0:n] (chunks: a 2-D
+    [n_chunks, chunk_stride] CUDA tensor of the received blocks, rank r's in row r)."""
+    if chunks.dim() != 2:
+        raise ValueError("chunks must be 2-D: [n_chunks, chunk_stride]")
+    if chunks.dtype not in _DT:
+        raise ValueError(f"chunks dtype {chunks.dtype} is not f32/bf16/f16")
+    if acc.numel() < n or chunks.shape[1] < n:
+        raise ValueError("acc or a chunk is shorter than n")
+    _check(lib().zero_reduce_chunks(_dev(acc, "acc", torch.float32), _dev(chunks, "chunks"), _DT[chunks.dtype],
+                                    chunks.shape[0], chunks.shape[1], n, scale, int(bool(accumulate)),
+                                    _dev(found_nonfinite, "found_nonfinite", torch.int32, allow_none=True),
+                                    _dev(norm_ws, "norm_ws", allow_none=True), _ws_bytes(norm_ws), _stream(stream)))
 
 
 def zero_grad_sqnorm_finalize(ws: Optional[torch.Tensor], n: int, extra_sqnorm: float, max_norm: float,

@@ -170,6 +170,41 @@ zero_status zero_accum(float* d_acc, const void* d_src, zero_dtype src_dtype, in
                        int32_t accumulate, int32_t* d_found_nonfinite, void* d_norm_ws,
                        size_t norm_ws_bytes, void* stream);
 
+/* zero_reduce_chunks -- device.
+ * The local half of a ZeRO-2/3 reduce-scatter (the ZeRO page, section
+ * "ZeRO-2: 附加切分梯度", ZeRO2Optimizer.reduce_gradients: the ranks' flat
+ * grads are summed, each rank keeps its chunk, which is then divided by
+ * world_size; the memory-ledger page, FSDP MixedPrecision: the reduction is
+ * done in fp32 because summing in bf16 loses accuracy).  An all-to-all
+ * exchange of the ranks' flat low-precision grads (padded to world_size
+ * equal chunks) has placed, for this rank's shard, n_chunks blocks in
+ * d_chunks, block r holding rank r's values; block r starts at element
+ * r * chunk_stride.  For k in [0, n), in rank order r = 0 .. n_chunks-1:
+ *   d_acc[k] = fl(d_acc[k] + fl(scale * x_r[k]))
+ * where, for r == 0 and accumulate == 0, d_acc[k] = fl(scale * x_0[k])
+ * instead (the accumulator's old contents are not read).  x_r is block r in
+ * src_dtype cast exactly to fp32.  This is the rule of n_chunks successive
+ * zero_accum calls, in one pass.  scale = 1 / world_size (times
+ * 1 / accum_steps when each micro-batch is reduced and accumulated): for a
+ * power-of-two world size scaling each term first is exactly the page's
+ * sum-then-divide, summed in rank order in binary32.  Elements n ..
+ * chunk_stride-1 of every block (the padding of a short last shard) are
+ * never read.  d_found_nonfinite and d_norm_ws (zero_grad_sqnorm_workspace_
+ * bytes(n)) as for zero_flatten_cast: the norm partials are those of the
+ * final d_acc values.
+ * Layout: d_acc fp32 [n]; d_chunks [n_chunks][chunk_stride] of src_dtype.
+ * Fast path: d_acc 32-byte aligned, d_chunks and chunk_stride * element
+ * size 16-byte (16-bit) or 32-byte (fp32) aligned; otherwise a slower,
+ * equally exact element path.
+ * Errors: ZERO_EINVAL for n < 0, n_chunks < 1, chunk_stride < n, NULL
+ * buffers with n > 0, a bad dtype, accumulate not 0/1, a non-finite scale,
+ * a chunk array larger than 2^62 bytes, or a too-small / misaligned norm
+ * workspace. */
+zero_status zero_reduce_chunks(float* d_acc, const void* d_chunks, zero_dtype src_dtype, int32_t n_chunks,
+                               int64_t chunk_stride, int64_t n, float scale, int32_t accumulate,
+                               int32_t* d_found_nonfinite, void* d_norm_ws, size_t norm_ws_bytes,
+                               void* stream);
+
 /* zero_grad_sqnorm_workspace_bytes -- host only.
  * Device scratch that zero_grad_sqnorm needs for n elements: one binary64
  * partial per fixed tile of the grad buffer (8 bytes per 32768 elements).

@@ -90,7 +90,8 @@ def test_two_processes_global_norm_step(mode):
     mp.start_processes(_rank_main, args=(_free_port(), mode, results), nprocs=WORLD, start_method="spawn", join=True)
     r0, r1 = results[0], results[1]
     # every rank saw the same norm, coefficient and skip decision at every step
-    assert r0["norms"] == r1["norms"]
+    # (repr: a skipped step's norm is NaN on both ranks, and NaN != NaN)
+    assert repr(r0["norms"]) == repr(r1["norms"])
     assert [x[3] for x in r0["norms"]] == [t != BAD_STEP for t in range(1, STEPS + 1)]
     assert [x[4] for x in r0["norms"]] == [1, 2, 2, 3]
 
@@ -123,3 +124,106 @@ def test_two_processes_global_norm_step(mode):
         assert res["exp_avg"] == st.m.tobytes(), f"rank {rank} exp_avg"
         assert res["exp_avg_sq"] == st.v.tobytes(), f"rank {rank} exp_avg_sq"
         assert res["lowp"] == st.lowp.tobytes(), f"rank {rank} lowp"
+
+
+# ------------------------------------------------------------------ ZeRO-2 data plane
+M_DP = 2  # micro-batches, each reduced as it comes
+
+
+def _dp_grads(wl, rank, t, j, dev):
+    """Rank `rank`'s full flat bf16 grad of micro-batch j (rank 1's holds an inf at step BAD_STEP,
+    inside rank 0's chunk: the exchange carries it to rank 0)."""
+    import workloads as W
+    g = W.flat_grads(wl.with_(seed=100 + rank), t, j, 0, wl.total, device=dev)
+    if t == BAD_STEP and rank == 1 and j == 0:
+        g[5] = float("inf")
+    return g
+
+
+def _dp_rank_main(rank, port, results):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=WORLD, timeout=datetime.timedelta(seconds=180))
+    try:
+        import workloads as W
+        from fsdp_sharded_mixed_flatparameter_gb300 import ZeroDataPlane, zero_shard_range
+        dev = torch.device("cuda:0")
+        torch.cuda.set_device(dev)
+        wl = _workload()
+        s, e = zero_shard_range(wl.total, WORLD, rank)
+        dp = ZeroDataPlane(wl.numels, group=dist.group.WORLD, device=dev, lr=wl.lr, betas=wl.betas, eps=wl.eps,
+                           weight_decay=wl.weight_decay, max_norm=wl.max_norm, master=W.master_init(wl, s, e).to(dev))
+        side = torch.cuda.Stream(device=dev)
+        norms = []
+        for t in range(1, STEPS + 1):
+            for j in range(M_DP):
+                dp.flat_grad[:wl.total] = _dp_grads(wl, rank, t, j, dev)  # what backward leaves
+                side.wait_stream(torch.cuda.current_stream(dev))
+                dp.reduce_scatter_grads(accumulate=j > 0, scale=1.0 / (WORLD * M_DP), fuse_norm=j == M_DP - 1,
+                                        stream=side)
+                torch.cuda.current_stream(dev).wait_stream(side)  # flat_grad is rewritten next
+            r = dp.step(stream=side)
+            norms.append((r.sqnorm, r.norm, r.clip_coef, r.finite, dp.opt.t))
+        torch.cuda.synchronize(dev)
+        results[rank] = {"norms": norms, "range": (s, e), "flat_param": dp.flat_param.cpu().view(torch.int16)
+                         .numpy().tobytes(), "padded": dp.padded,
+                         **{k: getattr(dp.opt, k).cpu().view(torch.int32).numpy().tobytes()
+                            for k in ("master", "exp_avg", "exp_avg_sq")}}
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_processes_zero2_data_plane():
+    """ZeroDataPlane across two processes: all-to-all of the padded flat bf16 grads, fp32
+    rank-order reduction with the fused norm over two micro-batches, global norm, AdamW
+    into the shard's slice of the bf16 FlatParameter, in-place all-gather -- on a side
+    stream, with a non-finite grad exchanged into the other rank's shard at step 3."""
+    import oracle
+    from _helpers import raw
+    from fsdp_sharded_mixed_flatparameter_gb300 import build
+    import workloads as W
+    build.build()
+    ctx = mp.get_context("spawn")
+    results = ctx.Manager().dict()
+    mp.start_processes(_dp_rank_main, args=(_free_port(), results), nprocs=WORLD, start_method="spawn", join=True)
+    r0, r1 = results[0], results[1]
+    assert repr(r0["norms"]) == repr(r1["norms"])  # NaN-aware: a skipped step's norm is NaN
+    assert [x[3] for x in r0["norms"]] == [t != BAD_STEP for t in range(1, STEPS + 1)]
+    assert [x[4] for x in r0["norms"]] == [1, 2, 2, 3]
+    assert r0["flat_param"] == r1["flat_param"], "ranks hold different parameters after the all-gather"
+
+    wl = _workload()
+    total = wl.total
+    chunk = -(-total // WORLD)
+    dev = torch.device("cuda:0")
+    states = {}
+    for rank in range(WORLD):
+        s, e = oracle.shard_range(total, WORLD, rank)
+        states[rank] = oracle.new_state(raw(W.master_init(wl, s, e)))
+    for t in range(1, STEPS + 1):
+        acc = {q: np.zeros(max(states[q].p.size, 1), np.float32) for q in range(WORLD)}
+        for j in range(M_DP):
+            full = [np.concatenate([raw(_dp_grads(wl, r, t, j, dev)), np.zeros(WORLD * chunk - total, np.uint16)])
+                    for r in range(WORLD)]
+            for q in range(WORLD):
+                blocks = np.ascontiguousarray(np.stack([f[q * chunk:(q + 1) * chunk] for f in full]))
+                oracle.reduce_chunks(acc[q], blocks, "bf16", states[q].p.size, 1.0 / (WORLD * M_DP), j > 0)
+        grad = np.concatenate([acc[q][:states[q].p.size] for q in range(WORLD)])
+        cr = oracle.clip(oracle.sqnorm(grad), 0.0, wl.max_norm)
+        _, nv, coef, fin, _ = r0["norms"][t - 1]
+        assert fin == cr.finite
+        if not cr.finite:
+            continue
+        assert abs(nv - cr.norm) <= 1e-12 * cr.norm and coef == cr.coef
+        for q in range(WORLD):
+            st = states[q]
+            st.t += 1
+            sc = oracle.adamw_scalars(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay, st.t)
+            oracle.adamw(st.p, st.m, st.v, np.ascontiguousarray(acc[q][:st.p.size]), sc, cr.coef, st.lowp)
+    lowp = np.frombuffer(r0["flat_param"], np.uint16)
+    assert np.array_equal(lowp[:total], np.concatenate([states[q].lowp for q in range(WORLD)]))
+    assert not lowp[total:].any()
+    for q, res in ((0, r0), (1, r1)):
+        st = states[q]
+        assert res["master"] == st.p.tobytes() and res["exp_avg"] == st.m.tobytes()
+        assert res["exp_avg_sq"] == st.v.tobytes()
