@@ -180,6 +180,54 @@ def oracle_step_rate(wl: W.Workload, sample_params: int, min_seconds: float, max
     return tot * passes / el, tot, passes, el
 
 
+def oracle_step_rate_threads(wl: W.Workload, sample_params: int, threads: int, passes: int):
+    """The oracle's whole step on the same sample as oracle_step_rate, with the element
+    range split into `threads` contiguous parts run by that many host threads (the
+    oracle's C functions release the GIL): flatten/cast of each part, each part's sum
+    of squares (added exactly with math.fsum, so the norm is the single-threaded one's
+    to the last bit or two), clip, AdamW of each part.  A second CPU baseline using all
+    the host's cores; the single-threaded oracle stays the parity reference."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    numels, tot = [], 0
+    for n in wl.numels:
+        take = min(n, sample_params - tot)
+        if take <= 0:
+            break
+        numels.append(take)
+        tot += take
+    g = torch.Generator().manual_seed(wl.seed)
+    grads = [(torch.randn(n, generator=g) * wl.grad_std).to(torch.bfloat16).view(torch.int16).numpy()
+             .view(np.uint16) for n in numels]
+    p = (torch.randn(tot, generator=g) * wl.init_std).numpy()
+    st = oracle.new_state(p)
+    flat = np.empty(tot, np.float32)
+    bounds = [tot * i // threads for i in range(threads + 1)]
+    parts = [(a, b) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+
+    def flatten_part(ab):
+        a, b = ab
+        oracle.flatten(grads, numels, "bf16", a, b, 1.0, flat[a:b], accumulate=False)
+
+    def sq_part(ab):
+        return oracle.sqnorm(flat[ab[0]:ab[1]])
+
+    with ThreadPoolExecutor(max_workers=len(parts)) as pool:
+        def one_pass():
+            list(pool.map(flatten_part, parts))
+            cr = oracle.clip(math.fsum(pool.map(sq_part, parts)), 0.0, wl.max_norm)
+            st.t += 1
+            sc = oracle.adamw_scalars(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay, st.t)
+            list(pool.map(lambda ab: oracle.adamw(st.p[ab[0]:ab[1]], st.m[ab[0]:ab[1]], st.v[ab[0]:ab[1]],
+                                                  flat[ab[0]:ab[1]], sc, cr.coef, st.lowp[ab[0]:ab[1]]), parts))
+        one_pass()  # warm-up: page in the buffers
+        t0 = time.perf_counter()
+        for _ in range(passes):
+            one_pass()
+        el = time.perf_counter() - t0
+    return tot * passes / el, tot, passes, el
+
+
 def _sample_list(numels, lo: int, count: int):
     """Sizes of the pieces of the tensor list that cover flat positions [lo, lo + count)."""
     out, pos = [], 0
@@ -475,6 +523,12 @@ def run_gpu(args):
                                 "sample": f"first {tot} params of the Llama-7B flat list, {passes} whole-step "
                                           f"passes in {el:.1f} s",
                                 "stages_elems_per_s": oracle_step_rate.last_stages}
+        threads = max(1, os.cpu_count() or 1)
+        trate, ttot, tpasses, tel = oracle_step_rate_threads(base, 1 << 25, threads, 10)
+        line["cpu_baseline_all_cores"] = {
+            "value": trate, "unit": UNIT, "cores": threads, "kind": "oracle, element ranges on host threads",
+            "sample": f"first {ttot} params of the Llama-7B flat list split into {threads} ranges, {tpasses} "
+                      f"whole-step passes in {tel:.1f} s"}
     print(json.dumps(line))
     return 0
 
@@ -680,7 +734,8 @@ def graph_step_ms(args, wl, s, e, dev, micro, stream, flush=None):
     opt = FlatShardAdamW(wl.numels, world_size=wl.world_size, rank=wl.rank, lr=wl.lr, betas=wl.betas, eps=wl.eps,
                          weight_decay=wl.weight_decay, max_norm=wl.max_norm,
                          grad_range="full" if wl.mode == "zero1" else "shard", device=dev,
-                         master=W.master_init(wl, s, e, device=dev), capturable=True)
+                         lowp_dtype=W.torch_dtype(wl.lowp_dtype), master=W.master_init(wl, s, e, device=dev),
+                         capturable=True)
     M = wl.micro_batches
     if wl.mode != "zero3":
         for m in micro:
@@ -724,7 +779,7 @@ def run_config(args):
     last one, AdamW), inputs resident; prints one JSON line with the per-kernel split."""
     from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
     from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
-    wl = W.ALL[args.workload]()
+    wl = {**W.ALL, **W.VARIANTS}[args.workload]()
     if args.small:
         # profiling case: the same distribution on ~10x fewer parameters
         if wl.name.startswith("ragged"):
@@ -738,7 +793,7 @@ def run_config(args):
     opt = FlatShardAdamW(wl.numels, world_size=wl.world_size, rank=wl.rank, lr=wl.lr, betas=wl.betas, eps=wl.eps,
                          weight_decay=wl.weight_decay, max_norm=wl.max_norm,
                          grad_range="full" if wl.mode == "zero1" else "shard", device=dev,
-                         master=W.master_init(wl, s, e, device=dev))
+                         lowp_dtype=W.torch_dtype(wl.lowp_dtype), master=W.master_init(wl, s, e, device=dev))
     M = wl.micro_batches
     esize = W.torch_dtype(wl.grad_dtype).itemsize
     if wl.mode == "zero3":
@@ -811,7 +866,7 @@ def run_config(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "params_per_rank": n, "tensors": wl.n_tensors, "world_size": wl.world_size,
                    "rank": wl.rank, "micro_batches": M, "grad_dtype": wl.grad_dtype, "mode": wl.mode,
-                   "grad_buffer_elems": grad_elems,
+                   "lowp_dtype": wl.lowp_dtype, "weight_decay": wl.weight_decay, "grad_buffer_elems": grad_elems,
                    "l2": (f"step touches {step_bytes / 1e6:.0f} MB < 4x L2: 512 MB written between timed steps, "
                           f"each step timed by its own events (first grad pass to the end of AdamW)"
                           if flush is not None else "inputs larger than L2; no flush")},
@@ -840,7 +895,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="llama7b_flat", choices=sorted(W.ALL),
+    ap.add_argument("--workload", default="llama7b_flat", choices=sorted({**W.ALL, **W.VARIANTS}),
                     help="another configuration's step (a table row, not the headline line)")
     ap.add_argument("--small", action="store_true",
                     help="profiling case for ncu (a smaller list of the same shape), not a bench line")

@@ -106,6 +106,22 @@ def test_llama13b_zero3_shape_all_steps():
     _summary(rep)
 
 
+def test_llama13b_zero3_f16_chunk_full_size_sampled():
+    """The ZeRO page's ZeRO-3 update at the 13B rank's full size: fp16 local parameter chunk,
+    Adam without weight decay (section "ZeRO-3: 切分参数"), 8 fp16 micro-batches, 2 steps."""
+    wl = W.llama13b_zero3_f16chunk()
+    assert wl.lowp_dtype == "f16" and wl.weight_decay == 0.0
+    rep = run_workload(wl, steps=2, sample=1_000_000)
+    assert rep.n == 1626983040 and all(s.ref_coef < 1.0 for s in rep.steps)
+    _summary(rep)
+
+
+def test_llama13b_zero3_f16_chunk_shape_all_steps():
+    wl = W.llama13b_zero3_f16chunk().with_(numels=tuple(W.llama_numels(5, 640, 1728, 4000)), max_norm=0.1)
+    rep = run_workload(wl, steps=W.llama13b_zero3().steps, fused=False)
+    _summary(rep)
+
+
 def test_null_grads_and_fp16_writeback():
     """Tensors without grad read as zeros; the ZeRO-3 fp16 local chunk as the low-precision copy."""
     wl = W.small_ragged(n_tensors=400, null_grads=(0, 5, 399), lowp_dtype="f16", world_size=3, rank=1)

@@ -144,7 +144,7 @@ def test_four_ranks_zero2_step_through_the_data_plane():
     from fsdp_sharded_mixed_flatparameter_gb300.dataplane import chunk_layout
     import workloads as W
     world, M, steps = 4, 2, 3
-    wl = W.small_ragged(n_tensors=700, max_log2=13, world_size=world, rank=0, max_norm=0.5)
+    wl = W.small_ragged(n_tensors=700, max_log2=13, world_size=world, rank=0, max_norm=0.2)
     total = wl.total
     chunk, padded = chunk_layout(total, world)
     assert chunk == -(-total // world) and padded % world == 0 and padded - total < world

@@ -162,6 +162,16 @@ def ragged() -> Workload:
 ALL = {w().name: w for w in (tiny, gpt2_zero1, llama7b, llama13b_zero3, ragged)}
 
 
+def llama13b_zero3_f16chunk() -> Workload:
+    """The Llama-13B ZeRO-3 rank with the ZeRO page's ZeRO-3 update (section "ZeRO-3: 切分参数"):
+    the rank's low-precision parameter chunk is fp16, and the page's Adam has no weight decay."""
+    return llama13b_zero3().with_(name="llama13b_zero3_r7of8_f16chunk", lowp_dtype="f16", weight_decay=0.0)
+
+
+# variants of the five configurations (bench lines and parity tests, not configurations of their own)
+VARIANTS = {w().name: w for w in (llama13b_zero3_f16chunk,)}
+
+
 def small_llama(layers: int = 2, hidden: int = 256, mlp: int = 688, vocab: int = 1000, **kw) -> Workload:
     """A Llama-shaped list small enough for the oracle to finish in seconds."""
     base = llama7b().with_(name=f"llama_l{layers}_h{hidden}",
