@@ -29,20 +29,8 @@
 // (reduce.cuh), so its partial equals bit for bit what the separate norm
 // kernel would compute from the written buffer -- without reading it again.
 //
-// Norm only (WRITE = false: the direct AdamW path needs the norm of the
-// grads but not the flat copy): the pass reads 2 bytes per element and is
-// bound by instruction issue and latency rather than DRAM, so (a) one bulk
-// prefetch per block pulls its source range into L2 before the loads, and
-// (b) for 16-bit grads with a power-of-two scale (EXACT = 1; 2 when the
-// scale is 1 and the multiply goes away) every value fl(scale * w) has a
-// square with no rounding residual, so the in-tensor tiles use
-// NormAcc::add2_exact (same bits, fewer FMA-pipe operations) and do no
-// per-element finiteness test: an inf or NaN value makes the thread's sum
-// non-finite, and only a thread whose sum is non-finite at the end of its
-// norm tile re-reads its in-tensor groups to decide the flag (a finite value
-// whose square overflows binary32 gives the same sum but no flag).
-// (The same shortcut in the writing pass measured ~4 % slower there, where
-// DRAM is the bound, so the writing pass keeps the general code.)
+// Norm only (K1n, normonly_kernel below): the direct AdamW path needs the
+// norm of the grads but not the flat copy; that pass has its own kernel.
 #include <string.h>
 
 #include "common.cuh"
@@ -52,7 +40,7 @@
 
 namespace zs {
 
-template <int DT, bool ACC, bool NORM, bool WRITE, int EXACT>
+template <int DT, bool ACC, bool NORM>
 __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* __restrict__ table, int n_tensors,
                                                              int64_t shard_start, int64_t len, int64_t ntiles,
                                                              float* __restrict__ dst, bool dst_vec, float scale,
@@ -64,33 +52,15 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
   constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
   constexpr int kPerBlock = NORM ? static_cast<int>(kSqTile / kFlTile) : 1;  // tiles per block
   static_assert(!NORM || kFlThreads == kSqThreads, "norm tile contract");
-  static_assert(WRITE || (NORM && !ACC), "norm-only mode reads and squares, nothing else");
-  static_assert(!EXACT || (DT != ZERO_F32 && !WRITE), "exact squares: norm-only pass over 16-bit grads");
   const int64_t nblocks_work = (ntiles + kPerBlock - 1) / kPerBlock;
   bool bad = false;
-  const unsigned long long scale2 = f2_pack(scale, scale);
 
   for (int64_t wb = blockIdx.x; wb < nblocks_work; wb += gridDim.x) {
     const int64_t t0 = wb * kPerBlock;
     const int64_t t1 = (t0 + kPerBlock < ntiles) ? t0 + kPerBlock : ntiles;
     const int64_t k_first = shard_start + t0 * kFlTile;
-    int ti = (WRITE && NORM) ? find_tensor(table, n_tensors, k_first) : find_tensor_warp(table, n_tensors, k_first);
+    int ti = NORM ? find_tensor(table, n_tensors, k_first) : find_tensor_warp(table, n_tensors, k_first);
     NormAcc nacc;  // this thread's share of the norm tile
-    const int ti_first = ti;
-    if (!WRITE && threadIdx.x == 0) {
-      // Norm only: the block's loads are 2-4 bytes per element, too few in
-      // flight to cover DRAM latency, so one bulk prefetch pulls the block's
-      // whole source range (up to 64 KB of a 16-bit tensor) into L2 first.
-      const int64_t k0 = shard_start + t0 * kFlTile;
-      const int64_t k1 = shard_start + ((t1 * kFlTile < len) ? t1 * kFlTile : len);
-      const zero_tensor tt = table[ti];
-      if (tt.ptr != nullptr && tt.flat_offset <= k0 && k1 <= tt.flat_offset + tt.numel) {
-        const uintptr_t a = reinterpret_cast<uintptr_t>(tt.ptr) + es * (k0 - tt.flat_offset);
-        const uintptr_t a0 = (a + 15) & ~uintptr_t(15), a1 = (a + es * (k1 - k0)) & ~uintptr_t(15);
-        if (a1 > a0) prefetch_l2_bulk(reinterpret_cast<const void*>(a0), static_cast<uint32_t>(a1 - a0));
-      }
-    }
-
     for (int64_t tile = t0; tile < t1; ++tile) {
       const int64_t base = tile * kFlTile;
       const int tlen = static_cast<int>((len - base < kFlTile) ? (len - base) : kFlTile);
@@ -100,30 +70,12 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
       const int64_t toff = __ldg(&table[ti].flat_offset), tnum = __ldg(&table[ti].numel);
       const char* tsrc = tptr ? static_cast<const char*>(tptr) + es * (klo - toff) : nullptr;
 
-      const bool direct = tlen == kFlTile && (dst_vec || !WRITE) && tsrc != nullptr && toff <= klo &&
+      const bool direct = tlen == kFlTile && dst_vec && tsrc != nullptr && toff <= klo &&
                           khi <= toff + tnum && reinterpret_cast<uintptr_t>(tsrc) % vb == 0;
       if (!ZS_CHECK(!direct || (klo - toff + kFlTile <= tnum && aligned(tsrc, vb) &&
-                                (!WRITE || aligned(dst + base, 32)) && base + kFlTile <= len),
+                                aligned(dst + base, 32) && base + kFlTile <= len),
                     20, tile))
         continue;
-      if (EXACT && direct) {
-        // 1024 groups of 8 (16 bytes of source each); thread t takes groups t + 256 r, loads first
-        uint4 w[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) w[r] = ld16_ro(tsrc + 16 * (threadIdx.x + r * kFlThreads));
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const uint32_t ws[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const unsigned long long w2 =
-                f2_pack(half_bits_to_f32<DT>(ws[j] & 0xffffu), half_bits_to_f32<DT>(ws[j] >> 16));
-            const unsigned long long v = (EXACT == 2) ? w2 : f2_mul(w2, scale2);
-            nacc.add2_exact(v);
-          }
-        }
-        continue;
-      }
       if (direct) {
         // 1024 groups of 8; thread t takes groups t + 256 r, r = 0..3, all loads first
         float x[4][8];
@@ -143,7 +95,7 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
             x[r][i] = ACC ? __fadd_rn(a[r][i], y) : y;
           }
           if (NORM) nacc.add8(x[r]);
-          if (WRITE) st8(dst + base + 8 * (threadIdx.x + r * kFlThreads), x[r]);
+          st8(dst + base + 8 * (threadIdx.x + r * kFlThreads), x[r]);
         }
         continue;
       }
@@ -155,8 +107,8 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
       for (int u = threadIdx.x; u < ngroups; u += kFlThreads) {
         float y[8];
         const int64_t d = base + 8 * u;
-        if (!ZS_CHECK(d < len && (!WRITE || !dst_vec || 8 * u + 8 > tlen || aligned(dst + d, 32)), 21, d)) continue;
-        if ((dst_vec || !WRITE) && 8 * u + 8 <= tlen) {
+        if (!ZS_CHECK(d < len && (!dst_vec || 8 * u + 8 > tlen || aligned(dst + d, 32)), 21, d)) continue;
+        if (dst_vec && 8 * u + 8 <= tlen) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) y[i] = stage[stage_idx(8 * u + i)];
           if (ACC) {
@@ -166,36 +118,120 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
             for (int i = 0; i < 8; ++i) y[i] = __fadd_rn(a[i], y[i]);
           }
           if (NORM) nacc.add8(y);
-          if (WRITE) st8(dst + d, y);
+          st8(dst + d, y);
         } else {
           for (int i = 0; i < 8 && 8 * u + i < tlen; ++i) {
             const float si = stage[stage_idx(8 * u + i)];
             const float yi = ACC ? __fadd_rn(dst[d + i], si) : si;
             if (NORM) nacc.add1(i, yi);
-            if (WRITE) dst[d + i] = yi;
+            dst[d + i] = yi;
           }
         }
       }
       __syncthreads();
     }
-    if (EXACT) {  // the flag of the in-tensor tiles, decided only where the sum went non-finite
-      float h0, h1;
-      f2_unpack(nacc.h, h0, h1);
-      if (!finite_f(h0) || !finite_f(h1)) {
-        int tj = ti_first;
-        for (int64_t tile = t0; tile < t1; ++tile) {
-          const int64_t base = tile * kFlTile;
-          const int tlen = static_cast<int>((len - base < kFlTile) ? (len - base) : kFlTile);
-          const int64_t klo = shard_start + base, khi = klo + tlen;
-          while (tj + 1 < n_tensors && __ldg(&table[tj + 1].flat_offset) <= klo) ++tj;
-          const void* tptr = table[tj].ptr;
-          const int64_t toff = __ldg(&table[tj].flat_offset), tnum = __ldg(&table[tj].numel);
-          const char* tsrc = tptr ? static_cast<const char*>(tptr) + es * (klo - toff) : nullptr;
-          const bool direct = tlen == kFlTile && tsrc != nullptr && toff <= klo && khi <= toff + tnum &&
-                              reinterpret_cast<uintptr_t>(tsrc) % vb == 0;
-          if (!direct) continue;
-          for (int r = 0; r < 4; ++r) {
-            const uint4 w = ld16_ro(tsrc + 16 * (threadIdx.x + r * kFlThreads));
+    if (NORM) {
+      const double bs = block_sum_norm<kFlThreads>(nacc, red);
+      if (threadIdx.x == 0 && ZS_CHECK(wb < nblocks_work, 22, wb)) partials[wb] = bs;
+    }
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
+}
+
+// ------------------------------------------------------------------- K1n
+// Norm only (the direct AdamW path needs the norm of the grads, not their
+// flat fp32 copy): reads the grads through the table and writes only the
+// norm tiles' partials, 2 bytes per element for 16-bit grads.  With so few
+// bytes per element the pass is bound by instructions, not DRAM, so it has
+// its own kernel with no staging buffer (small shared-memory footprint, so
+// more blocks per SM) and no per-8192-element tile bookkeeping:
+//  * one block per 32768-element norm tile (the tile contract of reduce.cuh);
+//  * a tile that lies inside one tensor with a 16-byte aligned (32-byte for
+//    fp32) source -- all but a few tiles per tensor boundary -- is read with
+//    16-byte loads, eight per thread in flight (no L2 bulk prefetch: measured
+//    on GB300 at 6.74B bf16 grads, a 64 KB prefetch per tile racing these
+//    loads took 2.87 ms, none 1.85 ms = 7.27 TB/s; four or sixteen loads in
+//    flight instead of eight were no better or worse);
+//  * any other tile (tensor boundaries, a tensor without grad, misaligned
+//    sources, the ragged end) goes element by element: every thread walks
+//    the table forward over its own elements in the contract's order;
+//  * for 16-bit grads with a power-of-two scale (EXACT = 1; 2 when the scale
+//    is 1 and the multiply goes away) every value fl(scale * w) has a square
+//    with no rounding residual, so NormAcc::add2_exact gives the general
+//    accumulator's bits with fewer instructions, and the non-finite flag needs
+//    no per-element test: an inf or NaN value leaves the thread's sum
+//    non-finite, and only then does the thread re-read its groups to decide
+//    (a finite value whose square overflows binary32 gives the same sum but
+//    no flag).
+// The partials equal bit for bit those of the separate norm kernel over the
+// flattened values, and those of the writing flatten pass with the fused norm.
+template <int DT, int EXACT>
+__global__ void __launch_bounds__(kSqThreads) normonly_kernel(const zero_tensor* __restrict__ table, int n_tensors,
+                                                              int64_t shard_start, int64_t len, int64_t ntiles,
+                                                              float scale, int32_t* __restrict__ flag,
+                                                              double* __restrict__ partials) {
+  __shared__ float2 red[kSqThreads / 32];
+  constexpr int es = SrcTraits<DT>::esize;
+  constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
+  static_assert(!EXACT || DT != ZERO_F32, "exact squares: 16-bit grads only");
+  const unsigned long long scale2 = f2_pack(scale, scale);
+  bool bad = false;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int64_t base = tile * kSqTile;
+    const int64_t k0 = shard_start + base;
+    const int64_t tlen = (len - base < kSqTile) ? len - base : kSqTile;
+    const int ti = find_tensor_warp(table, n_tensors, k0);
+    const void* tptr = table[ti].ptr;
+    const int64_t toff = __ldg(&table[ti].flat_offset), tnum = __ldg(&table[ti].numel);
+    const char* tsrc = tptr ? static_cast<const char*>(tptr) + es * (k0 - toff) : nullptr;
+    const bool pure = tlen == kSqTile && tsrc != nullptr && toff <= k0 && k0 + kSqTile <= toff + tnum &&
+                      reinterpret_cast<uintptr_t>(tsrc) % vb == 0;  // block-uniform
+    NormAcc nacc;
+    if (pure && ZS_CHECK(k0 - toff + kSqTile <= tnum && aligned(tsrc, vb), 50, tile)) {
+#pragma unroll
+      for (int round = 0; round < 2; ++round) {
+        if (DT == ZERO_F32) {
+          float x[8][8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) ld8_ro(reinterpret_cast<const float*>(tsrc) +
+                                                 8 * ((round * 8 + r) * kSqThreads + threadIdx.x), x[r]);
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              x[r][i] = __fmul_rn(scale, x[r][i]);
+              bad |= !finite_f(x[r][i]);
+            }
+            nacc.add8(x[r]);
+          }
+        } else {
+          uint4 w[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) w[r] = ld16_ro(tsrc + 16 * ((round * 8 + r) * kSqThreads + threadIdx.x));
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const uint32_t ws[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float lo = half_bits_to_f32<DT>(ws[j] & 0xffffu), hi = half_bits_to_f32<DT>(ws[j] >> 16);
+              if (EXACT) {
+                const unsigned long long w2 = f2_pack(lo, hi);
+                nacc.add2_exact(EXACT == 2 ? w2 : f2_mul(w2, scale2));
+              } else {
+                const float y0 = __fmul_rn(scale, lo), y1 = __fmul_rn(scale, hi);
+                bad |= !finite_f(y0) || !finite_f(y1);
+                nacc.add2(y0, y1);
+              }
+            }
+          }
+        }
+      }
+      if (EXACT) {  // the flag, decided only where the thread's sum went non-finite
+        float h0, h1;
+        f2_unpack(nacc.h, h0, h1);
+        if (!finite_f(h0) || !finite_f(h1)) {
+          for (int r = 0; r < kSqVecPerThread; ++r) {
+            const uint4 w = ld16_ro(tsrc + 16 * (r * kSqThreads + threadIdx.x));
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
             for (int j = 0; j < 4; ++j) {
               bad |= !finite_f(__fmul_rn(scale, half_bits_to_f32<DT>(ws[j] & 0xffffu)));
@@ -204,11 +240,27 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
           }
         }
       }
+    } else {
+      // element by element; each thread walks the table forward over its own
+      // elements, which ascend in the contract's (r, i) order
+      int j = ti;
+      for (int r = 0; r < kSqVecPerThread; ++r) {
+        const int64_t g = base + (static_cast<int64_t>(r) * kSqThreads + threadIdx.x) * 8;
+        for (int i = 0; i < 8 && g + i < len; ++i) {
+          const int64_t kf = shard_start + g + i;
+          while (j + 1 < n_tensors && __ldg(&table[j + 1].flat_offset) <= kf) ++j;
+          const void* p = table[j].ptr;
+          const int64_t off = __ldg(&table[j].flat_offset), num = __ldg(&table[j].numel);
+          float x = 0.0f;
+          if (p != nullptr && ZS_CHECK(kf >= off && kf - off < num, 51, kf)) x = load_elem<DT>(p, kf - off);
+          const float y = __fmul_rn(scale, x);
+          bad |= !finite_f(y);
+          nacc.add1(i, y);
+        }
+      }
     }
-    if (NORM) {
-      const double bs = block_sum_norm<kFlThreads>(nacc, red);
-      if (threadIdx.x == 0 && ZS_CHECK(wb < nblocks_work, 22, wb)) partials[wb] = bs;
-    }
+    const double bs = block_sum_norm<kSqThreads>(nacc, red);
+    if (threadIdx.x == 0 && ZS_CHECK(tile < ntiles, 52, tile)) partials[tile] = bs;
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0 && flag != nullptr) atomicOr(flag, 1);
 }
@@ -222,29 +274,37 @@ static bool pow2_scale(float scale) {
   return (b & 0x7fffffu) == 0u && ex != 0u && ex != 0xffu;
 }
 
-template <int DT, bool ACC, bool NORM, bool WRITE>
+template <int DT, bool ACC, bool NORM>
 static zero_status launch_flatten_t(const zero_tensor* table, int32_t n_tensors, int64_t s, int64_t e, float scale,
                                     float* dst, int32_t* flag, double* partials, cudaStream_t st) {
   const int64_t len = e - s;
   const int64_t ntiles = (len + kFlTile - 1) / kFlTile;
   const int64_t per = NORM ? kSqTile / kFlTile : 1;
   const unsigned grid = one_pass_blocks(ntiles, per);
-  const bool dst_vec = dst != nullptr && aligned(dst, 32);
-  if constexpr (DT != ZERO_F32 && !WRITE) {
+  const bool dst_vec = aligned(dst, 32);
+  flatten_kernel<DT, ACC, NORM><<<grid, kFlThreads, 0, st>>>(table, n_tensors, s, len, ntiles, dst, dst_vec, scale,
+                                                             flag, partials);
+  return check_launch("flatten_kernel");
+}
+
+template <int DT>
+static zero_status launch_normonly(const zero_tensor* table, int32_t n_tensors, int64_t s, int64_t e, float scale,
+                                   int32_t* flag, double* partials, cudaStream_t st) {
+  const int64_t len = e - s;
+  const int64_t ntiles = (len + kSqTile - 1) / kSqTile;
+  const unsigned grid = one_pass_blocks(ntiles, 1);
+  if constexpr (DT != ZERO_F32) {
     if (scale == 1.0f) {
-      flatten_kernel<DT, ACC, NORM, WRITE, 2><<<grid, kFlThreads, 0, st>>>(table, n_tensors, s, len, ntiles, dst,
-                                                                          dst_vec, scale, flag, partials);
-      return check_launch("flatten_kernel");
+      normonly_kernel<DT, 2><<<grid, kSqThreads, 0, st>>>(table, n_tensors, s, len, ntiles, scale, flag, partials);
+      return check_launch("normonly_kernel");
     }
     if (pow2_scale(scale)) {
-      flatten_kernel<DT, ACC, NORM, WRITE, 1><<<grid, kFlThreads, 0, st>>>(table, n_tensors, s, len, ntiles, dst,
-                                                                          dst_vec, scale, flag, partials);
-      return check_launch("flatten_kernel");
+      normonly_kernel<DT, 1><<<grid, kSqThreads, 0, st>>>(table, n_tensors, s, len, ntiles, scale, flag, partials);
+      return check_launch("normonly_kernel");
     }
   }
-  flatten_kernel<DT, ACC, NORM, WRITE, 0><<<grid, kFlThreads, 0, st>>>(table, n_tensors, s, len, ntiles, dst,
-                                                                          dst_vec, scale, flag, partials);
-  return check_launch("flatten_kernel");
+  normonly_kernel<DT, 0><<<grid, kSqThreads, 0, st>>>(table, n_tensors, s, len, ntiles, scale, flag, partials);
+  return check_launch("normonly_kernel");
 }
 
 template <int DT, bool ACC>
@@ -252,11 +312,11 @@ static zero_status launch_flatten_n(const zero_tensor* table, int32_t n_tensors,
                                     float* dst, int32_t* flag, double* partials, cudaStream_t st) {
   if (dst == nullptr) {  // norm partials only: the grad is not written (ACC is rejected by the caller)
     if (ACC) return ZERO_EINVAL;
-    return launch_flatten_t<DT, false, true, false>(table, n_tensors, s, e, scale, nullptr, flag, partials, st);
+    return launch_normonly<DT>(table, n_tensors, s, e, scale, flag, partials, st);
   }
   if (partials != nullptr)
-    return launch_flatten_t<DT, ACC, true, true>(table, n_tensors, s, e, scale, dst, flag, partials, st);
-  return launch_flatten_t<DT, ACC, false, true>(table, n_tensors, s, e, scale, dst, flag, nullptr, st);
+    return launch_flatten_t<DT, ACC, true>(table, n_tensors, s, e, scale, dst, flag, partials, st);
+  return launch_flatten_t<DT, ACC, false>(table, n_tensors, s, e, scale, dst, flag, nullptr, st);
 }
 
 zero_status launch_flatten(const zero_tensor* table, int32_t n_tensors, int src_dtype, int64_t s, int64_t e,

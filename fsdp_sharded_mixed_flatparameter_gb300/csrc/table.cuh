@@ -28,12 +28,6 @@ __device__ __forceinline__ int find_tensor(const zero_tensor* __restrict__ table
   return lo;
 }
 
-// Ask the TMA unit to bring [p, p + bytes) into L2 (no data is returned;
-// p 16-byte aligned, bytes a multiple of 16, the range inside one allocation).
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // find_tensor by a warp at once: the 32 lanes test 32 evenly spaced
 // candidates per round and __ballot_sync picks the segment that holds k, so
 // n tensors take ceil(log32 n) rounds of independent loads (2 for the 291 of
