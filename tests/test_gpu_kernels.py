@@ -282,6 +282,40 @@ def test_flatten_ragged_matches_oracle_bit_exact(dtype):
             assert flag.item() == 0
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_flatten_big_misaligned_tensors(dtype):
+    """Tensors spanning many 8192-element tiles whose sources are not co-aligned with the
+    destination (every element offset 0..7): the 16-bit tiles inside a tensor are realigned
+    in registers, the rest staged; bit for bit against the oracle, and the fused norm's
+    partials equal to the separate norm kernel's over the written values."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    numels = [5, 40000, 3, 70001, 17, 30000, 9000, 1, 25000, 8208, 8217]
+    host, dev = _table_case(numels, dtype, seed=9, elem_offsets=[0, 1, 2, 3, 5, 7, 6, 4])
+    table, total = zs.zero_tensor_table(dev, numels)
+    d_table = zs.device_table(table, len(numels), DEV)
+    rawh = [raw(h) for h in host]
+    for world, rank in ((1, 0), (3, 1), (5, 4)):
+        s, e = oracle.shard_range(total, world, rank)
+        D = Guarded(e - s, torch.float32, 0)
+        ref = np.zeros(e - s, np.float32)
+        flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+        ws = torch.empty(zs.zero_grad_sqnorm_workspace_bytes(e - s), dtype=torch.uint8, device=DEV)
+        for j, scale in enumerate((0.25, 0.25, 0.5)):
+            last = j == 2
+            zs.zero_flatten_cast(d_table, len(numels), total, W.torch_dtype(dtype), s, e, scale, j > 0, D.t, flag,
+                                 ws if last else None)
+            oracle.flatten(rawh, numels, dtype, s, e, scale, ref, accumulate=j > 0)
+        torch.cuda.synchronize()
+        D.check_guards()
+        assert bits_equal_f32(raw(D.t), ref), (world, rank)
+        assert flag.item() == 0
+        out_f, out_s = zs.new_norm_result(DEV), zs.new_norm_result(DEV)
+        zs.zero_grad_sqnorm_finalize(ws, e - s, 0.0, 1.0, out_f)
+        zs.zero_grad_sqnorm(D.t.clone(), 0.0, 1.0, torch.empty_like(ws), out_s)
+        torch.cuda.synchronize()
+        assert bytes(out_f.cpu().numpy()) == bytes(out_s.cpu().numpy()), (world, rank)
+
+
 def test_flatten_big_aligned_tensors_fast_path():
     """Llama-shaped list (tensors aligned, tiles inside one tensor) vs torch.cat and the oracle."""
     from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
