@@ -314,7 +314,10 @@ zero_status zero_adamw_step(float* d_master, float* d_exp_avg, float* d_exp_avg_
  * returns ZERO_EINVAL with a message that names the limit.
  * Set-up: the first call on each device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture begins.
+ * call before any stream capture begins.  The address is kept per device and
+ * context (keyed on the context's process-unique ID): after cudaDeviceReset
+ * the runtime's new context may hold the array elsewhere, so the first call
+ * in it looks the address up again (and should also come before a capture).
  * Sharing: all calls on a device use the same array, which keeps the last
  * call's partials.  Calls whose work overlaps on the GPU (for example on two
  * streams at once) race on it; the caller must serialise them.  Nothing
