@@ -32,7 +32,6 @@ through the host); every arithmetic step runs in libzeroshard's kernels.
 """
 from __future__ import annotations
 
-import math
 from typing import List, Optional, Sequence, Tuple
 
 import torch
@@ -150,9 +149,7 @@ class ZeroDataPlane:
             chunks = self.recv.view(self.world_size, self.chunk)
         else:
             chunks = self.flat_grad.view(1, self.padded)
-        zs.zero_reduce_chunks(opt.grad, chunks, opt.n, sc, accumulate, opt.found_nonfinite,
-                              opt.ws if fuse_norm else None, st)
-        opt._norm_ready = fuse_norm
+        opt.reduce(chunks, accumulate=accumulate, scale=sc, fuse_norm=fuse_norm, stream=st)
 
     def all_gather_params(self, stream=None) -> None:
         """Every rank's updated low-precision slice into every rank's flat_param."""

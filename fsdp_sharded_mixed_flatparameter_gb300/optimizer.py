@@ -212,6 +212,17 @@ class FlatShardAdamW:
                       stream)
         self._norm_ready = fuse_norm
 
+    def reduce(self, chunks: torch.Tensor, *, accumulate: bool, scale: float, fuse_norm: bool = False,
+               stream=None) -> None:
+        """Reduce the ranks' received chunks of this shard into the fp32 shard grad (ZeRO-2/3,
+        zero_reduce_chunks): chunks is [world_size, chunk] in rank order, the first n of each
+        row are this shard's values; fuse_norm as for flatten()."""
+        if self.glo != self.start:
+            raise ValueError("reduce() needs a shard-only grad buffer (grad_range='shard')")
+        zs.zero_reduce_chunks(self.grad, chunks, self.n, scale, accumulate, self.found_nonfinite,
+                              self.ws if fuse_norm else None, stream)
+        self._norm_ready = fuse_norm
+
     # ----------------------------------------------------------------- step
     def shard_grad(self) -> torch.Tensor:
         return self.grad[self.start - self.glo:self.end - self.glo]

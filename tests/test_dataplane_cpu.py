@@ -10,7 +10,6 @@ where the all-gather sends it from).
 import os
 import socket
 
-import numpy as np
 import pytest
 import torch
 import torch.distributed as dist

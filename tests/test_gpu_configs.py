@@ -72,9 +72,10 @@ def test_llama7b_full_size_all_steps_sampled():
 
 
 def test_llama7b_full_size_direct_path_sampled():
-    """The benchmark's direct path (norm pass + AdamW through the tensor table, no fp32 grad) at full size."""
-    rep = run_workload(W.llama7b(), steps=1, sample=1_000_000, direct=True)
-    assert rep.n == 6738415616
+    """The benchmark's direct path (norm pass + AdamW through the tensor table, no fp32 grad) at
+    full size, for the configuration's 5 steps."""
+    rep = run_workload(W.llama7b(), steps=W.llama7b().steps, sample=1_000_000, direct=True)
+    assert rep.n == 6738415616 and len(rep.steps) == 5
     _summary(rep)
 
 

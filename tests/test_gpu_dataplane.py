@@ -168,12 +168,9 @@ def test_four_ranks_zero2_step_through_the_data_plane():
             for q, opt in enumerate(opts):
                 # what rank q receives from the all-to-all: block r = rank r's chunk q
                 recv = torch.stack([grads[r][j][q * chunk:(q + 1) * chunk] for r in range(world)]).contiguous()
-                zs.zero_reduce_chunks(opt.grad, recv, opt.n, 1.0 / (world * M), j > 0, opt.found_nonfinite,
-                                      opt.ws if j == M - 1 else None)
+                opt.reduce(recv, accumulate=j > 0, scale=1.0 / (world * M), fuse_norm=j == M - 1)
                 oracle.reduce_chunks(ref_acc[q], np.ascontiguousarray(raw(recv)), "bf16", opt.n, 1.0 / (world * M),
                                      j > 0)
-            for opt in opts:
-                opt._norm_ready = j == M - 1
         gathered = torch.cat([opt.local_sqnorm() for opt in opts])  # the 8-byte all-gather, rank order
         results = []
         for opt in opts:
@@ -196,3 +193,68 @@ def test_four_ranks_zero2_step_through_the_data_plane():
         lowp = raw(flat_param)
         assert np.array_equal(lowp[:total], np.concatenate([st.lowp for st in states]))
         assert not lowp[total:].any()
+
+
+def test_one_rank_of_eight_full_size_sampled():
+    """One rank of an 8-rank ZeRO-2 Llama-7B job at full size, in the launch configuration
+    `bench.py --dataplane-ranks 8` times (842,301,952 shard params, 8 received bf16 blocks,
+    the reduction with the fused norm, then AdamW), 2 steps: the oracle reduces every element
+    for the norm (host threads over disjoint chunks, exact fsum) and the state is compared at
+    1M sampled positions (element-wise, so sampling is exact)."""
+    import math
+    from concurrent.futures import ThreadPoolExecutor
+    from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW, chunk_layout, zero_shard as zs
+    import workloads as W
+    from _configs import ORACLE_THREADS
+    wl = W.llama7b()
+    N, r = 8, 3
+    total = wl.total
+    chunk, _ = chunk_layout(total, N)
+    s, e = oracle.shard_range(total, N, r)
+    n = e - s
+    assert n == chunk == 842301952
+    master = W.master_init(wl, s, e, device=DEV)
+    opt = FlatShardAdamW(wl.numels, world_size=N, rank=r, lr=wl.lr, betas=wl.betas, eps=wl.eps,
+                         weight_decay=wl.weight_decay, max_norm=wl.max_norm, device=DEV, master=master)
+    rng = np.random.default_rng(7)
+    idx = np.unique(np.concatenate([rng.integers(0, n, size=1_000_000), [0, n - 1]])).astype(np.int64)
+    d_idx = torch.from_numpy(idx).to(DEV)
+    st = oracle.new_state(raw(master.index_select(0, d_idx)))
+    del master
+    recv = torch.zeros(N, chunk, dtype=torch.bfloat16, device=DEV)
+    step_chunk = 1 << 25
+    for t in (1, 2):
+        for j in range(N):  # rank j's values of this rank's shard, as the exchange delivers them
+            recv[j, :n] = W.flat_grads(wl.with_(seed=wl.seed + j), t, 0, s, e, device=DEV)
+        opt.reduce(recv, accumulate=False, scale=1.0 / N, fuse_norm=True)
+        opt.launch_step()
+        res = opt.finish_step()
+        g_sample = np.empty(idx.size, np.float32)
+
+        def oracle_chunk(a):
+            b = min(a + step_chunk, n)
+            blocks = np.ascontiguousarray(raw(recv[:, a:b]))
+            acc = np.empty(b - a, np.float32)
+            oracle.reduce_chunks(acc, blocks, "bf16", b - a, 1.0 / N, False)
+            sel = (idx >= a) & (idx < b)
+            g_sample[sel] = acc[idx[sel] - a]
+            return oracle.sqnorm(acc)
+
+        with ThreadPoolExecutor(max_workers=ORACLE_THREADS) as pool:
+            sq = math.fsum(pool.map(oracle_chunk, range(0, n, step_chunk)))
+        cr = oracle.clip(sq, 0.0, wl.max_norm)
+        assert res.finite and cr.finite and cr.coef < 1.0
+        assert abs(res.norm - cr.norm) <= RTOL_NORM * cr.norm, (res.norm, cr.norm)
+        st.t += 1
+        sc = oracle.adamw_scalars(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay, st.t)
+        oracle.adamw(st.p, st.m, st.v, g_sample, sc, cr.coef, st.lowp)
+        assert opt.t == st.t
+        for got, ref in ((opt.master, st.p), (opt.exp_avg, st.m), (opt.exp_avg_sq, st.v)):
+            g = raw(got.index_select(0, d_idx))
+            assert_close_f32(g, ref)
+            if res.clip_coef == cr.coef:
+                assert bits_equal_f32(g, ref)
+        if res.clip_coef == cr.coef:
+            assert np.array_equal(raw(opt.lowp.index_select(0, d_idx)), st.lowp)
+        print(f"rank {r} of {N}, step {t}: norm gpu={res.norm:.17g} oracle={cr.norm:.17g} "
+              f"coef equal={res.clip_coef == cr.coef}")

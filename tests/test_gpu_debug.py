@@ -4,8 +4,8 @@ Each kernel checks every global-memory access site's index against its
 extent and its address against its vector alignment, recording violations
 instead of faulting.  Its reporting path is exercised by a self-test that
 records a violation without touching memory, and the kernel, direct-path,
-graph, AMP and multi-rank suites run under it with a check after every test
-that nothing was recorded.
+graph, AMP, multi-rank and data-plane suites run under it with a check after
+every test that nothing was recorded.
 """
 import os
 import subprocess
@@ -56,10 +56,10 @@ def test_debug_selftest_is_reported():
 
 def test_kernel_suites_record_no_violation_under_the_debug_build():
     suites = ["tests/test_gpu_kernels.py", "tests/test_gpu_direct.py", "tests/test_gpu_graph.py",
-              "tests/test_gpu_amp.py", "tests/test_gpu_multirank.py"]
-    # (the 2^32-pattern write-back check runs once, under the release build: here it would only
-    # repeat the same kernel sites for a minute)
+              "tests/test_gpu_amp.py", "tests/test_gpu_multirank.py", "tests/test_gpu_dataplane.py"]
+    # (the 2^32-pattern write-back check and the full-size data-plane rank run once, under the
+    # release build: here they would only repeat the same kernel sites for a minute)
     p = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
-                        "-k", "not exhaustive_through_adamw"] + suites,
+                        "-k", "not exhaustive_through_adamw and not full_size"] + suites,
                        cwd=ROOT, env=_env(), capture_output=True, text=True, timeout=1800)
     assert p.returncode == 0, p.stdout[-4000:] + p.stderr[-2000:]
