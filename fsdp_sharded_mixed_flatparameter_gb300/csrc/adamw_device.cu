@@ -10,7 +10,8 @@
 // (adam_scalars.cuh), so the AdamW kernel that follows reads them and the
 // result is bit-identical to a host-driven step.  With both the count and the
 // decision on the device, a whole step needs no host work and no
-// device-to-host read, and can be replayed from a graph.
+// device-to-host read, and can be replayed from a graph.  The dynamic loss
+// scale of mixed-precision steps can live on the device as well.
 #include "adam_scalars.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -46,6 +47,33 @@ __global__ void adamw_prepare_kernel(const zero_adamw_hparams* __restrict__ hp,
   state->apply = 1;
 }
 
+// The dynamic loss scale on the device (zero_loss_scale_update_device): the
+// host update's rule and roundings -- binary64 products rounded to binary32,
+// a grown scale kept only if finite -- then the grad passes' next unscale
+// factor 1 / (scale * accum_steps), rounded once, and the overflow flag cleared.
+__global__ void loss_scale_update_kernel(zero_loss_scale_state* __restrict__ st, int32_t accum_steps,
+                                         double growth, double backoff, int32_t interval,
+                                         const zero_norm_result* __restrict__ norm) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  const bool found = st->found_inf != 0 || (norm != nullptr && !norm->finite);
+  if (found) {
+    st->scale = __double2float_rn(__dmul_rn(static_cast<double>(st->scale), backoff));
+    st->growth_tracker = 0;
+  } else {
+    const int32_t good = st->growth_tracker + 1;
+    if (good >= interval) {
+      const float grown = __double2float_rn(__dmul_rn(static_cast<double>(st->scale), growth));
+      if (isfinite(grown)) st->scale = grown;
+      st->growth_tracker = 0;
+    } else {
+      st->growth_tracker = good;
+    }
+  }
+  st->unscale = __double2float_rn(__ddiv_rn(1.0, __dmul_rn(static_cast<double>(st->scale),
+                                                            static_cast<double>(accum_steps))));
+  st->found_inf = 0;
+}
+
 // One thread that records a violation on purpose without touching memory: the
 // debug build's self-test of its own reporting (release builds: a no-op).
 __global__ void debug_selftest_kernel(long long index) {
@@ -58,6 +86,13 @@ zero_status launch_debug_selftest(long long index, cudaStream_t st) {
 }
 
 ZS_DEBUG_UNIT(adamw_device)
+
+zero_status launch_loss_scale_update(zero_loss_scale_state* state, int32_t accum_steps, double growth,
+                                     double backoff, int32_t interval, const zero_norm_result* norm,
+                                     cudaStream_t st) {
+  loss_scale_update_kernel<<<1, 32, 0, st>>>(state, accum_steps, growth, backoff, interval, norm);
+  return check_launch("loss_scale_update_kernel");
+}
 
 zero_status launch_adamw_prepare(const zero_adamw_hparams* hp, const zero_norm_result* clip,
                                  zero_adamw_device_state* state, cudaStream_t st) {

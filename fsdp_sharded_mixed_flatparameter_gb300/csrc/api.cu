@@ -96,9 +96,9 @@ static zero_status check_norm_ws(const char* who, const void* ws, size_t ws_byte
 }
 
 zero_status zero_flatten_cast(const zero_tensor* d_table, int32_t n_tensors, int64_t total, zero_dtype src_dtype,
-                              int64_t shard_start, int64_t shard_end, float scale, int32_t accumulate,
-                              float* d_dst, int32_t* d_found_nonfinite, void* d_norm_ws, size_t norm_ws_bytes,
-                              void* stream) {
+                              int64_t shard_start, int64_t shard_end, float scale, const float* d_scale,
+                              int32_t accumulate, float* d_dst, int32_t* d_found_nonfinite, void* d_norm_ws,
+                              size_t norm_ws_bytes, void* stream) {
   if (n_tensors < 0) return fail(ZERO_EINVAL, "zero_flatten_cast: n_tensors %d < 0", n_tensors);
   if (n_tensors > 0 && d_table == nullptr) return fail(ZERO_EINVAL, "zero_flatten_cast: NULL d_table");
   if (total < 0 || (n_tensors == 0 && total != 0))
@@ -114,13 +114,13 @@ zero_status zero_flatten_cast(const zero_tensor* d_table, int32_t n_tensors, int
   const zero_status w = check_norm_ws("zero_flatten_cast", d_norm_ws, norm_ws_bytes, shard_end - shard_start);
   if (w != ZERO_OK) return w;
   if (shard_end == shard_start) return ZERO_OK;
-  return zs::launch_flatten(d_table, n_tensors, src_dtype, shard_start, shard_end, scale, accumulate, d_dst,
-                            d_found_nonfinite, static_cast<double*>(d_norm_ws), zs::as_stream(stream));
+  return zs::launch_flatten(d_table, n_tensors, src_dtype, shard_start, shard_end, scale, d_scale, accumulate,
+                            d_dst, d_found_nonfinite, static_cast<double*>(d_norm_ws), zs::as_stream(stream));
 }
 
 zero_status zero_accum(float* d_acc, const void* d_src, zero_dtype src_dtype, int64_t n, float scale,
-                       int32_t accumulate, int32_t* d_found_nonfinite, void* d_norm_ws, size_t norm_ws_bytes,
-                       void* stream) {
+                       const float* d_scale, int32_t accumulate, int32_t* d_found_nonfinite, void* d_norm_ws,
+                       size_t norm_ws_bytes, void* stream) {
   if (n < 0) return fail(ZERO_EINVAL, "zero_accum: n %lld < 0", (long long)n);
   if (!zs::valid_dtype(src_dtype)) return fail(ZERO_EINVAL, "zero_accum: bad src_dtype %d", (int)src_dtype);
   if (accumulate != 0 && accumulate != 1) return fail(ZERO_EINVAL, "zero_accum: accumulate must be 0 or 1");
@@ -129,13 +129,14 @@ zero_status zero_accum(float* d_acc, const void* d_src, zero_dtype src_dtype, in
   const zero_status w = check_norm_ws("zero_accum", d_norm_ws, norm_ws_bytes, n);
   if (w != ZERO_OK) return w;
   if (n == 0) return ZERO_OK;
-  return zs::launch_accum(d_acc, d_src, src_dtype, n, scale, accumulate, d_found_nonfinite,
+  return zs::launch_accum(d_acc, d_src, src_dtype, n, scale, d_scale, accumulate, d_found_nonfinite,
                           static_cast<double*>(d_norm_ws), zs::as_stream(stream));
 }
 
 zero_status zero_reduce_chunks(float* d_acc, const void* d_chunks, zero_dtype src_dtype, int32_t n_chunks,
-                               int64_t chunk_stride, int64_t n, float scale, int32_t accumulate,
-                               int32_t* d_found_nonfinite, void* d_norm_ws, size_t norm_ws_bytes, void* stream) {
+                               int64_t chunk_stride, int64_t n, float scale, const float* d_scale,
+                               int32_t accumulate, int32_t* d_found_nonfinite, void* d_norm_ws,
+                               size_t norm_ws_bytes, void* stream) {
   if (n < 0) return fail(ZERO_EINVAL, "zero_reduce_chunks: n %lld < 0", (long long)n);
   if (n_chunks < 1) return fail(ZERO_EINVAL, "zero_reduce_chunks: n_chunks %d < 1", (int)n_chunks);
   if (chunk_stride < n)
@@ -152,8 +153,9 @@ zero_status zero_reduce_chunks(float* d_acc, const void* d_chunks, zero_dtype sr
   const zero_status w = check_norm_ws("zero_reduce_chunks", d_norm_ws, norm_ws_bytes, n);
   if (w != ZERO_OK) return w;
   if (n == 0) return ZERO_OK;
-  return zs::launch_reduce_chunks(d_acc, d_chunks, src_dtype, n_chunks, chunk_stride, n, scale, accumulate,
-                                  d_found_nonfinite, static_cast<double*>(d_norm_ws), zs::as_stream(stream));
+  return zs::launch_reduce_chunks(d_acc, d_chunks, src_dtype, n_chunks, chunk_stride, n, scale, d_scale,
+                                  accumulate, d_found_nonfinite, static_cast<double*>(d_norm_ws),
+                                  zs::as_stream(stream));
 }
 
 size_t zero_grad_sqnorm_workspace_bytes(int64_t n) {
@@ -199,15 +201,23 @@ zero_status zero_grad_sqnorm_combine(const double* d_sqnorms, int32_t n_parts, d
   return zs::launch_sqnorm_combine(d_sqnorms, n_parts, max_norm, d_out, zs::as_stream(stream));
 }
 
+static zero_status check_loss_scale_policy(const char* who, double growth_factor, double backoff_factor,
+                                           int32_t growth_interval) {
+  if (!(growth_factor > 1.0) || !std::isfinite(growth_factor))
+    return fail(ZERO_EINVAL, "%s: growth_factor must be > 1 and finite", who);
+  if (!(backoff_factor > 0.0 && backoff_factor < 1.0))
+    return fail(ZERO_EINVAL, "%s: backoff_factor must be in (0, 1)", who);
+  if (growth_interval < 1) return fail(ZERO_EINVAL, "%s: growth_interval < 1", who);
+  return ZERO_OK;
+}
+
 zero_status zero_loss_scale_update(float* scale, int32_t* growth_tracker, int32_t found_inf, double growth_factor,
                                    double backoff_factor, int32_t growth_interval) {
   if (scale == nullptr || growth_tracker == nullptr)
     return fail(ZERO_EINVAL, "zero_loss_scale_update: NULL scale or growth_tracker");
-  if (!(growth_factor > 1.0) || !std::isfinite(growth_factor))
-    return fail(ZERO_EINVAL, "zero_loss_scale_update: growth_factor must be > 1 and finite");
-  if (!(backoff_factor > 0.0 && backoff_factor < 1.0))
-    return fail(ZERO_EINVAL, "zero_loss_scale_update: backoff_factor must be in (0, 1)");
-  if (growth_interval < 1) return fail(ZERO_EINVAL, "zero_loss_scale_update: growth_interval < 1");
+  const zero_status c = check_loss_scale_policy("zero_loss_scale_update", growth_factor, backoff_factor,
+                                                growth_interval);
+  if (c != ZERO_OK) return c;
   if (found_inf) {
     *scale = static_cast<float>(static_cast<double>(*scale) * backoff_factor);
     *growth_tracker = 0;
@@ -222,6 +232,18 @@ zero_status zero_loss_scale_update(float* scale, int32_t* growth_tracker, int32_
     *growth_tracker = good;
   }
   return ZERO_OK;
+}
+
+zero_status zero_loss_scale_update_device(zero_loss_scale_state* d_state, int32_t accum_steps, double growth_factor,
+                                          double backoff_factor, int32_t growth_interval,
+                                          const zero_norm_result* d_norm, void* stream) {
+  if (d_state == nullptr) return fail(ZERO_EINVAL, "zero_loss_scale_update_device: NULL d_state");
+  if (accum_steps < 1) return fail(ZERO_EINVAL, "zero_loss_scale_update_device: accum_steps < 1");
+  const zero_status c = check_loss_scale_policy("zero_loss_scale_update_device", growth_factor, backoff_factor,
+                                                growth_interval);
+  if (c != ZERO_OK) return c;
+  return zs::launch_loss_scale_update(d_state, accum_steps, growth_factor, backoff_factor, growth_interval, d_norm,
+                                      zs::as_stream(stream));
 }
 
 static zero_status adamw_scalars(const char* who, const zero_adamw_hparams* hp, int64_t step, zs::AdamScalars* s) {

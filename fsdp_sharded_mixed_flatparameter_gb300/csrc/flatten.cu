@@ -100,9 +100,11 @@ template <int DT, bool ACC, bool NORM>
 __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* __restrict__ table, int n_tensors,
                                                              int64_t shard_start, int64_t len, int64_t ntiles,
                                                              float* __restrict__ dst, bool dst_vec, float scale,
+                                                             const float* __restrict__ dscale,
                                                              int32_t* __restrict__ flag,
                                                              double* __restrict__ partials) {
   __shared__ float stage[kFlStage];
+  if (dscale != nullptr) scale = *dscale;  // a scale kept on the device (graph-captured mixed precision)
   __shared__ float2 red[kFlThreads / 32];
   constexpr int es = SrcTraits<DT>::esize;
   constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
@@ -239,12 +241,14 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
 template <int DT, int EXACT>
 __global__ void __launch_bounds__(kSqThreads) normonly_kernel(const zero_tensor* __restrict__ table, int n_tensors,
                                                               int64_t shard_start, int64_t len, int64_t ntiles,
-                                                              float scale, int32_t* __restrict__ flag,
+                                                              float scale, const float* __restrict__ dscale,
+                                                              int32_t* __restrict__ flag,
                                                               double* __restrict__ partials) {
   __shared__ float2 red[kSqThreads / 32];
   constexpr int es = SrcTraits<DT>::esize;
   constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
   static_assert(!EXACT || DT != ZERO_F32, "exact squares: 16-bit grads only");
+  if (dscale != nullptr) scale = *dscale;  // (EXACT is 0 then: the host cannot check the value)
   const unsigned long long scale2 = f2_pack(scale, scale);
   bool bad = false;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
@@ -347,61 +351,66 @@ static bool pow2_scale(float scale) {
 
 template <int DT, bool ACC, bool NORM>
 static zero_status launch_flatten_t(const zero_tensor* table, int32_t n_tensors, int64_t s, int64_t e, float scale,
-                                    float* dst, int32_t* flag, double* partials, cudaStream_t st) {
+                                    const float* dscale, float* dst, int32_t* flag, double* partials,
+                                    cudaStream_t st) {
   const int64_t len = e - s;
   const int64_t ntiles = (len + kFlTile - 1) / kFlTile;
   const int64_t per = NORM ? kSqTile / kFlTile : 1;
   const unsigned grid = one_pass_blocks(ntiles, per);
   const bool dst_vec = aligned(dst, 32);
   flatten_kernel<DT, ACC, NORM><<<grid, kFlThreads, 0, st>>>(table, n_tensors, s, len, ntiles, dst, dst_vec, scale,
-                                                             flag, partials);
+                                                             dscale, flag, partials);
   return check_launch("flatten_kernel");
 }
 
 template <int DT>
 static zero_status launch_normonly(const zero_tensor* table, int32_t n_tensors, int64_t s, int64_t e, float scale,
-                                   int32_t* flag, double* partials, cudaStream_t st) {
+                                   const float* dscale, int32_t* flag, double* partials, cudaStream_t st) {
   const int64_t len = e - s;
   const int64_t ntiles = (len + kSqTile - 1) / kSqTile;
   const unsigned grid = one_pass_blocks(ntiles, 1);
   if constexpr (DT != ZERO_F32) {
-    if (scale == 1.0f) {
-      normonly_kernel<DT, 2><<<grid, kSqThreads, 0, st>>>(table, n_tensors, s, len, ntiles, scale, flag, partials);
+    if (dscale == nullptr && scale == 1.0f) {
+      normonly_kernel<DT, 2><<<grid, kSqThreads, 0, st>>>(table, n_tensors, s, len, ntiles, scale, nullptr, flag,
+                                                           partials);
       return check_launch("normonly_kernel");
     }
-    if (pow2_scale(scale)) {
-      normonly_kernel<DT, 1><<<grid, kSqThreads, 0, st>>>(table, n_tensors, s, len, ntiles, scale, flag, partials);
+    if (dscale == nullptr && pow2_scale(scale)) {
+      normonly_kernel<DT, 1><<<grid, kSqThreads, 0, st>>>(table, n_tensors, s, len, ntiles, scale, nullptr, flag,
+                                                           partials);
       return check_launch("normonly_kernel");
     }
   }
-  normonly_kernel<DT, 0><<<grid, kSqThreads, 0, st>>>(table, n_tensors, s, len, ntiles, scale, flag, partials);
+  normonly_kernel<DT, 0><<<grid, kSqThreads, 0, st>>>(table, n_tensors, s, len, ntiles, scale, dscale, flag,
+                                                       partials);
   return check_launch("normonly_kernel");
 }
 
 template <int DT, bool ACC>
 static zero_status launch_flatten_n(const zero_tensor* table, int32_t n_tensors, int64_t s, int64_t e, float scale,
-                                    float* dst, int32_t* flag, double* partials, cudaStream_t st) {
+                                    const float* dscale, float* dst, int32_t* flag, double* partials,
+                                    cudaStream_t st) {
   if (dst == nullptr) {  // norm partials only: the grad is not written (ACC is rejected by the caller)
     if (ACC) return ZERO_EINVAL;
-    return launch_normonly<DT>(table, n_tensors, s, e, scale, flag, partials, st);
+    return launch_normonly<DT>(table, n_tensors, s, e, scale, dscale, flag, partials, st);
   }
   if (partials != nullptr)
-    return launch_flatten_t<DT, ACC, true>(table, n_tensors, s, e, scale, dst, flag, partials, st);
-  return launch_flatten_t<DT, ACC, false>(table, n_tensors, s, e, scale, dst, flag, nullptr, st);
+    return launch_flatten_t<DT, ACC, true>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
+  return launch_flatten_t<DT, ACC, false>(table, n_tensors, s, e, scale, dscale, dst, flag, nullptr, st);
 }
 
 zero_status launch_flatten(const zero_tensor* table, int32_t n_tensors, int src_dtype, int64_t s, int64_t e,
-                           float scale, int accumulate, float* dst, int32_t* flag, double* partials,
-                           cudaStream_t st) {
+                           float scale, const float* dscale, int accumulate, float* dst, int32_t* flag,
+                           double* partials, cudaStream_t st) {
   if (e <= s) return ZERO_OK;
   switch (src_dtype * 2 + (accumulate ? 1 : 0)) {
-    case ZERO_F32 * 2: return launch_flatten_n<ZERO_F32, false>(table, n_tensors, s, e, scale, dst, flag, partials, st);
-    case ZERO_F32 * 2 + 1: return launch_flatten_n<ZERO_F32, true>(table, n_tensors, s, e, scale, dst, flag, partials, st);
-    case ZERO_BF16 * 2: return launch_flatten_n<ZERO_BF16, false>(table, n_tensors, s, e, scale, dst, flag, partials, st);
+    case ZERO_F32 * 2: return launch_flatten_n<ZERO_F32, false>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
+    case ZERO_F32 * 2 + 1: return launch_flatten_n<ZERO_F32, true>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
+    case ZERO_BF16 * 2: return launch_flatten_n<ZERO_BF16, false>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
     case ZERO_BF16 * 2 + 1:
-      return launch_flatten_n<ZERO_BF16, true>(table, n_tensors, s, e, scale, dst, flag, partials, st);
-    case ZERO_F16 * 2: return launch_flatten_n<ZERO_F16, false>(table, n_tensors, s, e, scale, dst, flag, partials, st);
-    default: return launch_flatten_n<ZERO_F16, true>(table, n_tensors, s, e, scale, dst, flag, partials, st);
+      return launch_flatten_n<ZERO_BF16, true>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
+    case ZERO_F16 * 2: return launch_flatten_n<ZERO_F16, false>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
+    default: return launch_flatten_n<ZERO_F16, true>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
   }
 }
 
@@ -420,8 +429,9 @@ __device__ __forceinline__ void accum_scalar(int64_t k, int64_t n, float* __rest
 template <int DT, bool ACC>
 __global__ void __launch_bounds__(256) accum_kernel(float* __restrict__ acc, const void* __restrict__ src,
                                                     int64_t head, int64_t nvec, int64_t n, float scale,
-                                                    int32_t* __restrict__ flag) {
+                                                    const float* __restrict__ dscale, int32_t* __restrict__ flag) {
   constexpr int es = SrcTraits<DT>::esize;
+  if (dscale != nullptr) scale = *dscale;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t body_end = head + 8 * nvec;
@@ -449,7 +459,9 @@ __global__ void __launch_bounds__(256) accum_kernel(float* __restrict__ acc, con
 
 template <int DT, bool ACC>
 __global__ void __launch_bounds__(256) accum_scalar_kernel(float* __restrict__ acc, const void* __restrict__ src,
-                                                           int64_t n, float scale, int32_t* __restrict__ flag) {
+                                                           int64_t n, float scale, const float* __restrict__ dscale,
+                                                           int32_t* __restrict__ flag) {
+  if (dscale != nullptr) scale = *dscale;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   bool bad = false;
   for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n; k += stride)
@@ -465,10 +477,12 @@ __global__ void __launch_bounds__(256) accum_scalar_kernel(float* __restrict__ a
 template <int DT, bool ACC>
 __global__ void __launch_bounds__(kSqThreads) accum_norm_kernel(float* __restrict__ acc, const void* __restrict__ src,
                                                                 int64_t n, int64_t ntiles, bool vec, float scale,
+                                                                const float* __restrict__ dscale,
                                                                 int32_t* __restrict__ flag,
                                                                 double* __restrict__ partials) {
   __shared__ float2 red[kSqThreads / 32];
   constexpr int es = SrcTraits<DT>::esize;
+  if (dscale != nullptr) scale = *dscale;
   const char* s8 = static_cast<const char*>(src);
   bool bad = false;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
@@ -571,11 +585,13 @@ __global__ void __launch_bounds__(kSqThreads) reduce_chunks_kernel(float* __rest
                                                                    const char* __restrict__ src, int n_chunks,
                                                                    int64_t stride_bytes, int64_t n, int64_t ntiles,
                                                                    bool vec, float scale,
+                                                                   const float* __restrict__ dscale,
                                                                    int32_t* __restrict__ flag,
                                                                    double* __restrict__ partials) {
   __shared__ float2 red[kSqThreads / 32];
   constexpr int es = SrcTraits<DT>::esize;
   constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
+  if (dscale != nullptr) scale = *dscale;
   bool bad = false;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     NormAcc nacc;
@@ -644,8 +660,8 @@ __global__ void __launch_bounds__(kSqThreads) reduce_chunks_kernel(float* __rest
 ZS_DEBUG_UNIT(flatten)
 
 template <int DT, bool ACC>
-static zero_status launch_accum_t(float* acc, const void* src, int64_t n, float scale, int32_t* flag,
-                                  cudaStream_t st) {
+static zero_status launch_accum_t(float* acc, const void* src, int64_t n, float scale, const float* dscale,
+                                  int32_t* flag, cudaStream_t st) {
   constexpr int es = SrcTraits<DT>::esize;
   constexpr uintptr_t vb = (DT == ZERO_F32) ? 32 : 16;
   const uintptr_t aa = reinterpret_cast<uintptr_t>(acc) % 32;
@@ -654,76 +670,80 @@ static zero_status launch_accum_t(float* acc, const void* src, int64_t n, float 
   const bool vec = head >= 0 && reinterpret_cast<uintptr_t>(src) % es == 0 &&
                    (reinterpret_cast<uintptr_t>(src) + es * static_cast<uintptr_t>(head)) % vb == 0;
   if (!vec) {
-    accum_scalar_kernel<DT, ACC><<<one_pass_blocks(n, 256), 256, 0, st>>>(acc, src, n, scale, flag);
+    accum_scalar_kernel<DT, ACC><<<one_pass_blocks(n, 256), 256, 0, st>>>(acc, src, n, scale, dscale, flag);
     return check_launch("accum_scalar_kernel");
   }
   const int64_t nvec = (n - head) / 8;
-  accum_kernel<DT, ACC><<<one_pass_blocks(nvec, 256), 256, 0, st>>>(acc, src, head, nvec, n, scale, flag);
+  accum_kernel<DT, ACC><<<one_pass_blocks(nvec, 256), 256, 0, st>>>(acc, src, head, nvec, n, scale, dscale,
+                                                                                      flag);
   return check_launch("accum_kernel");
 }
 
 template <int DT, bool ACC>
-static zero_status launch_accum_n(float* acc, const void* src, int64_t n, float scale, int32_t* flag,
-                                  double* partials, cudaStream_t st) {
-  if (partials == nullptr) return launch_accum_t<DT, ACC>(acc, src, n, scale, flag, st);
+static zero_status launch_accum_n(float* acc, const void* src, int64_t n, float scale, const float* dscale,
+                                  int32_t* flag, double* partials, cudaStream_t st) {
+  if (partials == nullptr) return launch_accum_t<DT, ACC>(acc, src, n, scale, dscale, flag, st);
   constexpr uintptr_t vb = (DT == ZERO_F32) ? 32 : 16;
   const bool vec = aligned(acc, 32) && aligned(src, vb);
   const int64_t ntiles = (n + kSqTile - 1) / kSqTile;
-  accum_norm_kernel<DT, ACC><<<one_pass_blocks(ntiles, 1), kSqThreads, 0, st>>>(acc, src, n, ntiles, vec, scale, flag,
-                                                                               partials);
+  accum_norm_kernel<DT, ACC><<<one_pass_blocks(ntiles, 1), kSqThreads, 0, st>>>(acc, src, n, ntiles, vec, scale, dscale,
+                                                                               flag, partials);
   return check_launch("accum_norm_kernel");
 }
 
-zero_status launch_accum(float* acc, const void* src, int src_dtype, int64_t n, float scale, int accumulate,
-                         int32_t* flag, double* partials, cudaStream_t st) {
+zero_status launch_accum(float* acc, const void* src, int src_dtype, int64_t n, float scale, const float* dscale,
+                         int accumulate, int32_t* flag, double* partials, cudaStream_t st) {
   if (n <= 0) return ZERO_OK;
   switch (src_dtype * 2 + (accumulate ? 1 : 0)) {
-    case ZERO_F32 * 2: return launch_accum_n<ZERO_F32, false>(acc, src, n, scale, flag, partials, st);
-    case ZERO_F32 * 2 + 1: return launch_accum_n<ZERO_F32, true>(acc, src, n, scale, flag, partials, st);
-    case ZERO_BF16 * 2: return launch_accum_n<ZERO_BF16, false>(acc, src, n, scale, flag, partials, st);
-    case ZERO_BF16 * 2 + 1: return launch_accum_n<ZERO_BF16, true>(acc, src, n, scale, flag, partials, st);
-    case ZERO_F16 * 2: return launch_accum_n<ZERO_F16, false>(acc, src, n, scale, flag, partials, st);
-    default: return launch_accum_n<ZERO_F16, true>(acc, src, n, scale, flag, partials, st);
+    case ZERO_F32 * 2: return launch_accum_n<ZERO_F32, false>(acc, src, n, scale, dscale, flag, partials, st);
+    case ZERO_F32 * 2 + 1: return launch_accum_n<ZERO_F32, true>(acc, src, n, scale, dscale, flag, partials, st);
+    case ZERO_BF16 * 2: return launch_accum_n<ZERO_BF16, false>(acc, src, n, scale, dscale, flag, partials, st);
+    case ZERO_BF16 * 2 + 1: return launch_accum_n<ZERO_BF16, true>(acc, src, n, scale, dscale, flag, partials, st);
+    case ZERO_F16 * 2: return launch_accum_n<ZERO_F16, false>(acc, src, n, scale, dscale, flag, partials, st);
+    default: return launch_accum_n<ZERO_F16, true>(acc, src, n, scale, dscale, flag, partials, st);
   }
 }
 
 template <int DT, bool ACC, bool NORM>
 static zero_status launch_reduce_chunks_t(float* acc, const void* src, int n_chunks, int64_t stride, int64_t n,
-                                          float scale, int32_t* flag, double* partials, cudaStream_t st) {
+                                          float scale, const float* dscale, int32_t* flag, double* partials,
+                                          cudaStream_t st) {
   constexpr int64_t es = SrcTraits<DT>::esize;
   constexpr uintptr_t vb = (DT == ZERO_F32) ? 32 : 16;
   const int64_t stride_bytes = stride * es;
   const bool vec = aligned(acc, 32) && aligned(src, vb) && stride_bytes % static_cast<int64_t>(vb) == 0;
   const int64_t ntiles = (n + kSqTile - 1) / kSqTile;
   reduce_chunks_kernel<DT, ACC, NORM><<<one_pass_blocks(ntiles, 1), kSqThreads, 0, st>>>(
-      acc, static_cast<const char*>(src), n_chunks, stride_bytes, n, ntiles, vec, scale, flag, partials);
+      acc, static_cast<const char*>(src), n_chunks, stride_bytes, n, ntiles, vec, scale, dscale, flag, partials);
   return check_launch("reduce_chunks_kernel");
 }
 
 template <int DT, bool ACC>
 static zero_status launch_reduce_chunks_n(float* acc, const void* src, int n_chunks, int64_t stride, int64_t n,
-                                          float scale, int32_t* flag, double* partials, cudaStream_t st) {
+                                          float scale, const float* dscale, int32_t* flag, double* partials,
+                                          cudaStream_t st) {
   if (partials != nullptr)
-    return launch_reduce_chunks_t<DT, ACC, true>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
-  return launch_reduce_chunks_t<DT, ACC, false>(acc, src, n_chunks, stride, n, scale, flag, nullptr, st);
+    return launch_reduce_chunks_t<DT, ACC, true>(acc, src, n_chunks, stride, n, scale, dscale, flag, partials, st);
+  return launch_reduce_chunks_t<DT, ACC, false>(acc, src, n_chunks, stride, n, scale, dscale, flag, nullptr, st);
 }
 
 zero_status launch_reduce_chunks(float* acc, const void* src, int src_dtype, int n_chunks, int64_t stride, int64_t n,
-                                 float scale, int accumulate, int32_t* flag, double* partials, cudaStream_t st) {
+                                 float scale, const float* dscale, int accumulate, int32_t* flag, double* partials,
+                                 cudaStream_t st) {
   if (n <= 0) return ZERO_OK;
   switch (src_dtype * 2 + (accumulate ? 1 : 0)) {
     case ZERO_F32 * 2:
-      return launch_reduce_chunks_n<ZERO_F32, false>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
+      return launch_reduce_chunks_n<ZERO_F32, false>(acc, src, n_chunks, stride, n, scale, dscale, flag, partials, st);
     case ZERO_F32 * 2 + 1:
-      return launch_reduce_chunks_n<ZERO_F32, true>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
+      return launch_reduce_chunks_n<ZERO_F32, true>(acc, src, n_chunks, stride, n, scale, dscale, flag, partials, st);
     case ZERO_BF16 * 2:
-      return launch_reduce_chunks_n<ZERO_BF16, false>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
+      return launch_reduce_chunks_n<ZERO_BF16, false>(acc, src, n_chunks, stride, n, scale, dscale, flag, partials, st);
     case ZERO_BF16 * 2 + 1:
-      return launch_reduce_chunks_n<ZERO_BF16, true>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
+      return launch_reduce_chunks_n<ZERO_BF16, true>(acc, src, n_chunks, stride, n, scale, dscale, flag, partials, st);
     case ZERO_F16 * 2:
-      return launch_reduce_chunks_n<ZERO_F16, false>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
+      return launch_reduce_chunks_n<ZERO_F16, false>(acc, src, n_chunks, stride, n, scale, dscale, flag, partials, st);
     default:
-      return launch_reduce_chunks_n<ZERO_F16, true>(acc, src, n_chunks, stride, n, scale, flag, partials, st);
+      return launch_reduce_chunks_n<ZERO_F16, true>(acc, src, n_chunks, stride, n, scale, dscale, flag, partials, st);
   }
 }
 

@@ -46,23 +46,30 @@ zero_status debug_read_flatten(unsigned long long* out, bool reset);
 zero_status debug_read_sqnorm(unsigned long long* out, bool reset);
 zero_status launch_debug_selftest(long long index, cudaStream_t st);
 
+// One thread: the dynamic loss scale update on the device state.
+zero_status launch_loss_scale_update(zero_loss_scale_state* state, int32_t accum_steps, double growth,
+                                     double backoff, int32_t interval, const zero_norm_result* norm,
+                                     cudaStream_t st);
+
 // One thread: advance the device step state (see zero_adamw_prepare_device).
 zero_status launch_adamw_prepare(const zero_adamw_hparams* hp, const zero_norm_result* clip,
                                  zero_adamw_device_state* state, cudaStream_t st);
 
 // `partials` (nullable): also write the norm tiles' partial sums of squares
 // of the values written (one binary64 per 32768 elements of dst / acc).
+// `dscale` (nullable): read the scale from device memory when the kernel runs.
 zero_status launch_flatten(const zero_tensor* table, int32_t n_tensors, int src_dtype, int64_t shard_start,
-                           int64_t shard_end, float scale, int accumulate, float* dst, int32_t* flag,
-                           double* partials, cudaStream_t st);
+                           int64_t shard_end, float scale, const float* dscale, int accumulate, float* dst,
+                           int32_t* flag, double* partials, cudaStream_t st);
 
-zero_status launch_accum(float* acc, const void* src, int src_dtype, int64_t n, float scale, int accumulate,
-                         int32_t* flag, double* partials, cudaStream_t st);
+zero_status launch_accum(float* acc, const void* src, int src_dtype, int64_t n, float scale, const float* dscale,
+                         int accumulate, int32_t* flag, double* partials, cudaStream_t st);
 
 // The ranks' received blocks of this rank's shard (n_chunks blocks, `stride`
 // elements apart) added into acc in rank order, each scaled first.
 zero_status launch_reduce_chunks(float* acc, const void* src, int src_dtype, int n_chunks, int64_t stride, int64_t n,
-                                 float scale, int accumulate, int32_t* flag, double* partials, cudaStream_t st);
+                                 float scale, const float* dscale, int accumulate, int32_t* flag, double* partials,
+                                 cudaStream_t st);
 
 zero_status launch_sqnorm(const float* g, int64_t n, double extra_sqnorm, double max_norm, double* partials,
                           zero_norm_result* out, cudaStream_t st);

@@ -192,35 +192,48 @@ class FlatShardAdamW:
             return self._registered
         return self._table(grads), len(grads), self._grad_dtype(grads)
 
+    def _scale_args(self, scale, loss_scale):
+        """(host scale, device scale or None, non-finite flag) of a grad pass: with a
+        DeviceLossScale the kernels read its unscale factor and raise its flag."""
+        if loss_scale is None:
+            return float(scale), None, self.found_nonfinite
+        return 1.0, loss_scale.unscale, loss_scale.found_inf
+
     def flatten(self, grads: Optional[Sequence[Optional[torch.Tensor]]] = None, *, accumulate: bool,
-                scale: float = 1.0, fuse_norm: bool = False, stream=None) -> None:
+                scale: float = 1.0, fuse_norm: bool = False, stream=None, loss_scale=None) -> None:
         """Flatten/cast per-tensor grads (or the registered ones) into the rank's flat
         fp32 grad (K1).
 
         fuse_norm: this is the last micro-batch; the same pass also computes the
         grad norm's tile partials, so step() only has to finalize them.
+        loss_scale: a DeviceLossScale; the pass then multiplies by its unscale
+        factor, read on the device when the kernel runs (so a captured graph
+        follows the scale), and raises its overflow flag; `scale` is ignored.
         """
         table, count, dt = self._resolve(grads)
-        zs.zero_flatten_cast(table, count, self.total, dt, self.glo, self.ghi, scale, accumulate,
-                             self.grad, self.found_nonfinite, self.ws if fuse_norm else None, stream)
+        sc, dsc, flag = self._scale_args(scale, loss_scale)
+        zs.zero_flatten_cast(table, count, self.total, dt, self.glo, self.ghi, sc, accumulate,
+                             self.grad, flag, self.ws if fuse_norm else None, stream, d_scale=dsc)
         self._norm_ready = fuse_norm
 
     def accum(self, flat_src: torch.Tensor, *, accumulate: bool, scale: float = 1.0, fuse_norm: bool = False,
-              stream=None) -> None:
-        """Accumulate a flat low-precision grad covering the grad range (K2); fuse_norm as for flatten()."""
-        zs.zero_accum(self.grad, flat_src, scale, accumulate, self.found_nonfinite, self.ws if fuse_norm else None,
-                      stream)
+              stream=None, loss_scale=None) -> None:
+        """Accumulate a flat low-precision grad covering the grad range (K2); fuse_norm and
+        loss_scale as for flatten()."""
+        sc, dsc, flag = self._scale_args(scale, loss_scale)
+        zs.zero_accum(self.grad, flat_src, sc, accumulate, flag, self.ws if fuse_norm else None, stream, d_scale=dsc)
         self._norm_ready = fuse_norm
 
     def reduce(self, chunks: torch.Tensor, *, accumulate: bool, scale: float, fuse_norm: bool = False,
-               stream=None) -> None:
+               stream=None, loss_scale=None) -> None:
         """Reduce the ranks' received chunks of this shard into the fp32 shard grad (ZeRO-2/3,
         zero_reduce_chunks): chunks is [world_size, chunk] in rank order, the first n of each
         row are this shard's values; fuse_norm as for flatten()."""
         if self.glo != self.start:
             raise ValueError("reduce() needs a shard-only grad buffer (grad_range='shard')")
-        zs.zero_reduce_chunks(self.grad, chunks, self.n, scale, accumulate, self.found_nonfinite,
-                              self.ws if fuse_norm else None, stream)
+        sc, dsc, flag = self._scale_args(scale, loss_scale)
+        zs.zero_reduce_chunks(self.grad, chunks, self.n, sc, accumulate, flag, self.ws if fuse_norm else None, stream,
+                              d_scale=dsc)
         self._norm_ready = fuse_norm
 
     # ----------------------------------------------------------------- step

@@ -44,6 +44,11 @@ class zero_adamw_hparams(ctypes.Structure):
                 ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double)]
 
 
+class zero_loss_scale_state(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_float), ("growth_tracker", ctypes.c_int32), ("unscale", ctypes.c_float),
+                ("found_inf", ctypes.c_int32)]
+
+
 class zero_adamw_device_state(ctypes.Structure):
     _fields_ = [("step", ctypes.c_int64), ("apply", ctypes.c_int32), ("status", ctypes.c_int32),
                 ("scalars", ctypes.c_float * 8)]
@@ -53,6 +58,7 @@ NORM_RESULT_BYTES = ctypes.sizeof(zero_norm_result)
 HPARAMS_BYTES = ctypes.sizeof(zero_adamw_hparams)
 DEVICE_STATE_BYTES = ctypes.sizeof(zero_adamw_device_state)
 TENSOR_ENTRY_BYTES = ctypes.sizeof(zero_tensor)
+LOSS_SCALE_STATE_BYTES = ctypes.sizeof(zero_loss_scale_state)
 
 _lib = None
 
@@ -79,9 +85,9 @@ def lib() -> ctypes.CDLL:
     L.zero_shard_range.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     L.zero_tensor_table.argtypes = [vp, vp, i32, vp, ctypes.POINTER(i64)]
     sz = ctypes.c_size_t
-    L.zero_flatten_cast.argtypes = [vp, i32, i64, ctypes.c_int, i64, i64, f32, i32, vp, vp, vp, sz, vp]
-    L.zero_accum.argtypes = [vp, vp, ctypes.c_int, i64, f32, i32, vp, vp, sz, vp]
-    L.zero_reduce_chunks.argtypes = [vp, vp, ctypes.c_int, i32, i64, i64, f32, i32, vp, vp, sz, vp]
+    L.zero_flatten_cast.argtypes = [vp, i32, i64, ctypes.c_int, i64, i64, f32, vp, i32, vp, vp, vp, sz, vp]
+    L.zero_accum.argtypes = [vp, vp, ctypes.c_int, i64, f32, vp, i32, vp, vp, sz, vp]
+    L.zero_reduce_chunks.argtypes = [vp, vp, ctypes.c_int, i32, i64, i64, f32, vp, i32, vp, vp, sz, vp]
     L.zero_grad_sqnorm_finalize.argtypes = [vp, i64, f64, f64, vp, vp]
     L.zero_grad_sqnorm_combine.argtypes = [vp, i32, f64, vp, vp]
     L.zero_grad_sqnorm_workspace_bytes.argtypes = [i64]
@@ -93,6 +99,7 @@ def lib() -> ctypes.CDLL:
     L.zero_adamw_step_tensors.argtypes = [vp, vp, vp, vp, i32, i64, ctypes.c_int, i64, f32, vp, ctypes.c_int, i64,
                                           ctypes.POINTER(zero_adamw_hparams), i64, vp, vp]
     L.zero_loss_scale_update.argtypes = [ctypes.POINTER(f32), ctypes.POINTER(i32), i32, f64, f64, i32]
+    L.zero_loss_scale_update_device.argtypes = [vp, i32, f64, f64, i32, vp, vp]
     L.zero_adamw_scalars.argtypes = [ctypes.POINTER(zero_adamw_hparams), i64, vp]
     L.zero_debug_errors.argtypes = [vp, i32]
     L.zero_debug_selftest.argtypes = [i64, vp]
@@ -107,7 +114,8 @@ def lib() -> ctypes.CDLL:
     for nm in ("zero_shard_range", "zero_tensor_table", "zero_flatten_cast", "zero_accum", "zero_reduce_chunks",
                "zero_grad_sqnorm",
                "zero_grad_sqnorm_finalize", "zero_grad_sqnorm_combine", "zero_grad_sqnorm_noalloc",
-               "zero_adamw_step", "zero_adamw_step_tensors", "zero_loss_scale_update", "zero_adamw_scalars",
+               "zero_adamw_step", "zero_adamw_step_tensors", "zero_loss_scale_update", "zero_loss_scale_update_device",
+               "zero_adamw_scalars",
                "zero_adamw_prepare_device", "zero_adamw_step_device", "zero_adamw_step_tensors_device",
                "zero_debug_errors", "zero_debug_selftest"):
         getattr(L, nm).restype = ctypes.c_int
@@ -202,35 +210,44 @@ def _ws_bytes(ws: Optional[torch.Tensor]) -> int:
     return 0 if ws is None else ws.numel() * ws.element_size()
 
 
+def _dscale(d_scale: Optional[torch.Tensor]):
+    """A device float the kernels read their scale from (e.g. DeviceLossScale.unscale), or None."""
+    if d_scale is None:
+        return None
+    if d_scale.dtype != torch.float32 or d_scale.numel() < 1:
+        raise ValueError("d_scale must be a float32 device tensor")
+    return _dev(d_scale, "d_scale")
+
+
 def zero_flatten_cast(d_table: torch.Tensor, n_tensors: int, total: int, src_dtype: torch.dtype, shard_start: int,
                       shard_end: int, scale: float, accumulate: bool, dst: torch.Tensor,
                       found_nonfinite: Optional[torch.Tensor] = None, norm_ws: Optional[torch.Tensor] = None,
-                      stream=None) -> None:
+                      stream=None, d_scale: Optional[torch.Tensor] = None) -> None:
     if dst is not None and shard_end > shard_start and dst.numel() < shard_end - shard_start:
         raise ValueError("dst is smaller than the shard")
     tab = _dev(d_table, "d_table", torch.uint8, allow_none=n_tensors == 0)
     if n_tensors > 0 and d_table.numel() < n_tensors * TENSOR_ENTRY_BYTES:
         raise ValueError("d_table holds fewer entries than n_tensors")
     _check(lib().zero_flatten_cast(tab, n_tensors, total, _DT[src_dtype], shard_start, shard_end, scale,
-                                   int(bool(accumulate)), _dev(dst, "dst", torch.float32, allow_none=norm_ws is not None),
+                                   _dscale(d_scale), int(bool(accumulate)), _dev(dst, "dst", torch.float32, allow_none=norm_ws is not None),
                                    _dev(found_nonfinite, "found_nonfinite", torch.int32, allow_none=True),
                                    _dev(norm_ws, "norm_ws", allow_none=True), _ws_bytes(norm_ws), _stream(stream)))
 
 
 def zero_accum(acc: torch.Tensor, src: torch.Tensor, scale: float, accumulate: bool,
                found_nonfinite: Optional[torch.Tensor] = None, norm_ws: Optional[torch.Tensor] = None,
-               stream=None) -> None:
+               stream=None, d_scale: Optional[torch.Tensor] = None) -> None:
     if src.numel() != acc.numel():
         raise ValueError("acc and src differ in size")
     _check(lib().zero_accum(_dev(acc, "acc", torch.float32), _dev(src, "src"), _DT[src.dtype], acc.numel(), scale,
-                            int(bool(accumulate)),
+                            _dscale(d_scale), int(bool(accumulate)),
                             _dev(found_nonfinite, "found_nonfinite", torch.int32, allow_none=True),
                             _dev(norm_ws, "norm_ws", allow_none=True), _ws_bytes(norm_ws), _stream(stream)))
 
 
 def zero_reduce_chunks(acc: torch.Tensor, chunks: torch.Tensor, n: int, scale: float, accumulate: bool,
                        found_nonfinite: Optional[torch.Tensor] = None, norm_ws: Optional[torch.Tensor] = None,
-                       stream=None) -> None:
+                       stream=None, d_scale: Optional[torch.Tensor] = None) -> None:
     """acc[0:n] (+)= the rank-order sum of scale * chunks[r, 0:n] (chunks: a 2-D
     [n_chunks, chunk_stride] CUDA tensor of the received blocks, rank r's in row r)."""
     if chunks.dim() != 2:
@@ -240,7 +257,8 @@ def zero_reduce_chunks(acc: torch.Tensor, chunks: torch.Tensor, n: int, scale: f
     if acc.numel() < n or chunks.shape[1] < n:
         raise ValueError("acc or a chunk is shorter than n")
     _check(lib().zero_reduce_chunks(_dev(acc, "acc", torch.float32), _dev(chunks, "chunks"), _DT[chunks.dtype],
-                                    chunks.shape[0], chunks.shape[1], n, scale, int(bool(accumulate)),
+                                    chunks.shape[0], chunks.shape[1], n, scale, _dscale(d_scale),
+                                    int(bool(accumulate)),
                                     _dev(found_nonfinite, "found_nonfinite", torch.int32, allow_none=True),
                                     _dev(norm_ws, "norm_ws", allow_none=True), _ws_bytes(norm_ws), _stream(stream)))
 
@@ -510,3 +528,50 @@ class DynamicLossScale:
     def update(self, found_inf: bool) -> None:
         _check(lib().zero_loss_scale_update(ctypes.byref(self._scale), ctypes.byref(self._good), int(bool(found_inf)),
                                             self.growth_factor, self.backoff_factor, self.growth_interval))
+
+
+class DeviceLossScale:
+    """The GradScaler-style dynamic loss scale kept in device memory (a
+    zero_loss_scale_state), for mixed-precision steps captured in a CUDA graph.
+
+    The grad passes read ``unscale`` (= 1/(scale * accum_steps)) from device
+    memory when they run (``d_scale``) and raise ``found_inf``
+    (``found_nonfinite``); ``launch_update()`` (one thread, capturable) backs
+    the scale off or grows it on the device, recomputes ``unscale`` and clears
+    the flag.  The same rule and roundings as DynamicLossScale.update, so both
+    follow the same scale bit for bit.  ``scale``, ``growth_tracker`` and
+    ``read()`` copy the state to the host (a synchronisation)."""
+
+    def __init__(self, device, init_scale: float = 2.0 ** 16, growth_factor: float = 2.0,
+                 backoff_factor: float = 0.5, growth_interval: int = 2000, accum_steps: int = 1):
+        if accum_steps < 1:
+            raise ValueError("accum_steps must be >= 1")
+        self.growth_factor, self.backoff_factor, self.growth_interval = growth_factor, backoff_factor, growth_interval
+        self.accum_steps = int(accum_steps)
+        sc = ctypes.c_float(init_scale).value
+        st = zero_loss_scale_state(sc, 0, ctypes.c_float(1.0 / (float(sc) * self.accum_steps)).value, 0)
+        self.state = torch.frombuffer(bytearray(bytes(memoryview(st))), dtype=torch.uint8).to(device)
+        self.unscale = self.state[8:12].view(torch.float32)     # the grad passes' d_scale
+        self.found_inf = self.state[12:16].view(torch.int32)    # the grad passes' found_nonfinite
+
+    def launch_update(self, norm_result: Optional[torch.Tensor] = None, stream=None) -> None:
+        """Enqueue the update after a step (norm_result: the step's zero_norm_result, whose
+        non-finite norm also counts as an overflow)."""
+        if norm_result is not None and norm_result.numel() * norm_result.element_size() < NORM_RESULT_BYTES:
+            raise ValueError("norm_result is smaller than zero_norm_result")
+        _check(lib().zero_loss_scale_update_device(_dev(self.state, "state"), self.accum_steps, self.growth_factor,
+                                                   self.backoff_factor, self.growth_interval,
+                                                   _dev(norm_result, "norm_result", allow_none=True),
+                                                   _stream(stream)))
+
+    def read(self) -> zero_loss_scale_state:
+        raw = bytes(self.state.detach().cpu().numpy().tobytes()[:LOSS_SCALE_STATE_BYTES])
+        return zero_loss_scale_state.from_buffer_copy(raw)
+
+    @property
+    def scale(self) -> float:
+        return self.read().scale
+
+    @property
+    def growth_tracker(self) -> int:
+        return self.read().growth_tracker

@@ -131,6 +131,10 @@ zero_status zero_tensor_table(const void* const* ptrs, const int64_t* numels, in
  *   values are written (the grad is not materialized -- for a step without
  *   micro-batch accumulation whose update reads the grads through the table,
  *   see zero_adamw_step_tensors).
+ * d_scale: NULL, or a device float read when the kernel runs and used in
+ *   place of `scale` (the unscale factor of a loss scale kept on the device,
+ *   zero_loss_scale_state.unscale, so that a step captured in a CUDA graph
+ *   follows the scale's changes; `scale` must still be finite).
  * d_found_nonfinite: NULL, or a device int32 set to 1 when any
  *   fl(scale * x) is inf or NaN (never cleared by the call: zero it first).
  * d_norm_ws: NULL, or a device workspace of at least
@@ -149,7 +153,7 @@ zero_status zero_tensor_table(const void* const* ptrs, const int64_t* numels, in
  * bounds. */
 zero_status zero_flatten_cast(const zero_tensor* d_table, int32_t n_tensors, int64_t total,
                               zero_dtype src_dtype, int64_t shard_start, int64_t shard_end,
-                              float scale, int32_t accumulate, float* d_dst,
+                              float scale, const float* d_scale, int32_t accumulate, float* d_dst,
                               int32_t* d_found_nonfinite, void* d_norm_ws, size_t norm_ws_bytes,
                               void* stream);
 
@@ -161,13 +165,13 @@ zero_status zero_flatten_cast(const zero_tensor* d_table, int32_t n_tensors, int
  *   accumulate == 1:  d_acc[k] = fl(d_acc[k] + fl(scale * x[k]))
  * with x = d_src in src_dtype cast exactly to fp32.  This is the ZeRO-2/3
  * case, where the rank receives its shard's grads already flat.
- * d_found_nonfinite and d_norm_ws (zero_grad_sqnorm_workspace_bytes(n))
- * as for zero_flatten_cast.
+ * d_scale, d_found_nonfinite and d_norm_ws (zero_grad_sqnorm_workspace_
+ * bytes(n)) as for zero_flatten_cast.
  * Errors: ZERO_EINVAL for n < 0, NULL buffers with n > 0, a bad dtype,
  * accumulate not 0/1, a non-finite scale, or a too-small / misaligned norm
  * workspace. */
 zero_status zero_accum(float* d_acc, const void* d_src, zero_dtype src_dtype, int64_t n, float scale,
-                       int32_t accumulate, int32_t* d_found_nonfinite, void* d_norm_ws,
+                       const float* d_scale, int32_t accumulate, int32_t* d_found_nonfinite, void* d_norm_ws,
                        size_t norm_ws_bytes, void* stream);
 
 /* zero_reduce_chunks -- device.
@@ -189,9 +193,9 @@ zero_status zero_accum(float* d_acc, const void* d_src, zero_dtype src_dtype, in
  * power-of-two world size scaling each term first is exactly the page's
  * sum-then-divide, summed in rank order in binary32.  Elements n ..
  * chunk_stride-1 of every block (the padding of a short last shard) are
- * never read.  d_found_nonfinite and d_norm_ws (zero_grad_sqnorm_workspace_
- * bytes(n)) as for zero_flatten_cast: the norm partials are those of the
- * final d_acc values.
+ * never read.  d_scale, d_found_nonfinite and d_norm_ws (zero_grad_sqnorm_
+ * workspace_bytes(n)) as for zero_flatten_cast: the norm partials are those
+ * of the final d_acc values.
  * Layout: d_acc fp32 [n]; d_chunks [n_chunks][chunk_stride] of src_dtype.
  * Fast path: d_acc 32-byte aligned, d_chunks and chunk_stride * element
  * size 16-byte (16-bit) or 32-byte (fp32) aligned; otherwise a slower,
@@ -201,9 +205,9 @@ zero_status zero_accum(float* d_acc, const void* d_src, zero_dtype src_dtype, in
  * a chunk array larger than 2^62 bytes, or a too-small / misaligned norm
  * workspace. */
 zero_status zero_reduce_chunks(float* d_acc, const void* d_chunks, zero_dtype src_dtype, int32_t n_chunks,
-                               int64_t chunk_stride, int64_t n, float scale, int32_t accumulate,
-                               int32_t* d_found_nonfinite, void* d_norm_ws, size_t norm_ws_bytes,
-                               void* stream);
+                               int64_t chunk_stride, int64_t n, float scale, const float* d_scale,
+                               int32_t accumulate, int32_t* d_found_nonfinite, void* d_norm_ws,
+                               size_t norm_ws_bytes, void* stream);
 
 /* zero_grad_sqnorm_workspace_bytes -- host only.
  * Device scratch that zero_grad_sqnorm needs for n elements: one binary64
@@ -346,6 +350,32 @@ zero_status zero_grad_sqnorm_noalloc(const float* d_grad, int64_t n, double extr
 zero_status zero_loss_scale_update(float* scale, int32_t* growth_tracker, int32_t found_inf,
                                    double growth_factor, double backoff_factor,
                                    int32_t growth_interval);
+
+/* The dynamic loss scale kept in device memory (zero_loss_scale_update_device),
+ * for mixed-precision steps captured in a CUDA graph. */
+typedef struct zero_loss_scale_state {
+  float scale;             /* the loss scale S the next backward multiplies the loss by */
+  int32_t growth_tracker;  /* good steps since the scale last changed */
+  float unscale;           /* 1 / (S * accum_steps): the d_scale of the next step's grad passes */
+  int32_t found_inf;       /* the grad passes' d_found_nonfinite; cleared by the update */
+} zero_loss_scale_state;
+
+/* zero_loss_scale_update_device -- device (one thread).
+ * zero_loss_scale_update on a zero_loss_scale_state in device memory, read
+ * and written when the kernel runs: the step overflowed when found_inf is
+ * set, or when d_norm is given and its `finite` is 0 (a sum of squares that
+ * overflowed).  The same binary64 products rounded to binary32 as the host
+ * update, so host and device scales agree bit for bit.  Then unscale =
+ * 1 / (scale * accum_steps) in binary64 rounded to binary32 (the value the
+ * host path passes as `scale`) and found_inf = 0, ready for the next step.
+ * The caller fills the initial state (scale, growth_tracker 0, its unscale,
+ * found_inf 0).
+ * Errors: ZERO_EINVAL for a NULL state, accum_steps < 1, or factors and
+ * interval outside the ranges of zero_loss_scale_update. */
+zero_status zero_loss_scale_update_device(zero_loss_scale_state* d_state, int32_t accum_steps,
+                                          double growth_factor, double backoff_factor,
+                                          int32_t growth_interval, const zero_norm_result* d_norm,
+                                          void* stream);
 
 /* zero_adamw_step_tensors -- device.
  * zero_adamw_step with the grad read straight from the per-tensor grads

@@ -98,22 +98,22 @@ def test_invalid_arguments_return_einval_before_any_launch(L):
     FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: each call fails validation first
     hp = zero_adamw_hparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
     cases = [
-        L.zero_flatten_cast(None, 2, 10, 1, 0, 5, 1.0, 0, FAKE, None, None, 0, None),          # NULL table
-        L.zero_flatten_cast(FAKE, -1, 10, 1, 0, 5, 1.0, 0, FAKE, None, None, 0, None),         # n_tensors < 0
-        L.zero_flatten_cast(FAKE, 2, 10, 1, 6, 5, 1.0, 0, FAKE, None, None, 0, None),          # start > end
-        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 11, 1.0, 0, FAKE, None, None, 0, None),         # end > total
-        L.zero_flatten_cast(FAKE, 2, 10, 7, 0, 5, 1.0, 0, FAKE, None, None, 0, None),          # bad dtype
-        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, 2, FAKE, None, None, 0, None),          # accumulate 2
-        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, math.nan, 0, FAKE, None, None, 0, None),     # NaN scale
-        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, 0, None, None, None, 0, None),          # NULL dst
-        L.zero_flatten_cast(FAKE, 0, 10, 1, 0, 5, 1.0, 0, FAKE, None, None, 0, None),          # total without tensors
-        L.zero_accum(None, FAKE, 1, 10, 1.0, 0, None, None, 0, None),
-        L.zero_accum(FAKE, FAKE, 1, -1, 1.0, 0, None, None, 0, None),
-        L.zero_accum(FAKE, FAKE, 9, 10, 1.0, 0, None, None, 0, None),
-        L.zero_accum(FAKE, FAKE, 1, 10, math.inf, 0, None, None, 0, None),
-        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, 0, FAKE, None, FAKE, 0, None),   # norm ws too small
-        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, 0, FAKE, None, ctypes.c_void_p(0x1003), 8, None),  # misaligned
-        L.zero_accum(FAKE, FAKE, 1, 40000, 1.0, 0, None, FAKE, 8, None),              # norm ws too small
+        L.zero_flatten_cast(None, 2, 10, 1, 0, 5, 1.0, None, 0, FAKE, None, None, 0, None),          # NULL table
+        L.zero_flatten_cast(FAKE, -1, 10, 1, 0, 5, 1.0, None, 0, FAKE, None, None, 0, None),         # n_tensors < 0
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 6, 5, 1.0, None, 0, FAKE, None, None, 0, None),          # start > end
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 11, 1.0, None, 0, FAKE, None, None, 0, None),         # end > total
+        L.zero_flatten_cast(FAKE, 2, 10, 7, 0, 5, 1.0, None, 0, FAKE, None, None, 0, None),          # bad dtype
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, None, 2, FAKE, None, None, 0, None),          # accumulate 2
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, math.nan, None, 0, FAKE, None, None, 0, None),     # NaN scale
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, None, 0, None, None, None, 0, None),          # NULL dst
+        L.zero_flatten_cast(FAKE, 0, 10, 1, 0, 5, 1.0, None, 0, FAKE, None, None, 0, None),          # total without tensors
+        L.zero_accum(None, FAKE, 1, 10, 1.0, None, 0, None, None, 0, None),
+        L.zero_accum(FAKE, FAKE, 1, -1, 1.0, None, 0, None, None, 0, None),
+        L.zero_accum(FAKE, FAKE, 9, 10, 1.0, None, 0, None, None, 0, None),
+        L.zero_accum(FAKE, FAKE, 1, 10, math.inf, None, 0, None, None, 0, None),
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, None, 0, FAKE, None, FAKE, 0, None),   # norm ws too small
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, None, 0, FAKE, None, ctypes.c_void_p(0x1003), 8, None),  # misaligned
+        L.zero_accum(FAKE, FAKE, 1, 40000, 1.0, None, 0, None, FAKE, 8, None),              # norm ws too small
         L.zero_grad_sqnorm_finalize(None, 10, 0.0, 1.0, FAKE, None),                   # NULL ws
         L.zero_grad_sqnorm_finalize(FAKE, 10, 0.0, 1.0, None, None),                   # NULL out
         L.zero_grad_sqnorm_finalize(FAKE, -1, 0.0, 1.0, FAKE, None),                   # n < 0
@@ -148,6 +148,11 @@ def test_invalid_arguments_return_einval_before_any_launch(L):
         L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, None, 2, 10, 1, 0, 1.0, None, 1, 5, FAKE, None, None),
         L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 6, 1.0, None, 1, 5, FAKE, None, None),
         L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 0, 1.0, None, 1, 5, None, None, None),
+        L.zero_loss_scale_update_device(None, 1, 2.0, 0.5, 10, None, None),                     # NULL state
+        L.zero_loss_scale_update_device(FAKE, 0, 2.0, 0.5, 10, None, None),                     # accum_steps 0
+        L.zero_loss_scale_update_device(FAKE, 1, 1.0, 0.5, 10, None, None),                     # growth 1
+        L.zero_loss_scale_update_device(FAKE, 1, 2.0, 1.0, 10, None, None),                     # backoff 1
+        L.zero_loss_scale_update_device(FAKE, 1, 2.0, 0.5, 0, None, None),                      # interval 0
         L.zero_adamw_scalars(ctypes.byref(hp), 0, FAKE),                                       # step 0
         L.zero_adamw_scalars(None, 1, FAKE),                                                   # NULL hp
         L.zero_adamw_scalars(ctypes.byref(hp), 1, None),                                       # NULL out
@@ -159,8 +164,8 @@ def test_invalid_arguments_return_einval_before_any_launch(L):
 def test_empty_calls_are_noops_without_a_gpu(L):
     from fsdp_sharded_mixed_flatparameter_gb300.zero_shard import zero_adamw_hparams
     hp = zero_adamw_hparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
-    assert L.zero_flatten_cast(None, 0, 0, 1, 0, 0, 1.0, 0, None, None, None, 0, None) == 0
-    assert L.zero_accum(None, None, 1, 0, 1.0, 0, None, None, 0, None) == 0
+    assert L.zero_flatten_cast(None, 0, 0, 1, 0, 0, 1.0, None, 0, None, None, None, 0, None) == 0
+    assert L.zero_accum(None, None, 1, 0, 1.0, None, 0, None, None, 0, None) == 0
     assert L.zero_adamw_step(None, None, None, None, None, 1, 0, ctypes.byref(hp), 1, None, None) == 0
 
 

@@ -69,3 +69,59 @@ def test_loss_scaled_fp16_accumulation_with_overflow_skip():
         assert np.array_equal(raw(opt.lowp), st.lowp)
     # backed off once at step 3, grew at steps 2, 5, 7
     assert scaler.scale == 2.0 ** 16 * 2 * 0.5 * 2 * 2
+
+
+def test_graph_captured_loss_scaled_steps_with_device_scale():
+    """The same loss-scaled fp16 accumulation, captured once in a CUDA graph with the loss
+    scale on the device (DeviceLossScale): the accumulate passes read the unscale factor
+    from device memory, the overflow flag and the non-finite norm drive the device-side
+    update, the step count and skip decision stay on the device.  Replayed for 7 steps
+    (an overflow at step 3) and checked after every step against the oracle: the state bit
+    for bit, the step count, and the scale trajectory of the GradScaler policy."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import DeviceLossScale, FlatShardAdamW
+    wl = W.llama13b_zero3().with_(numels=tuple(W.llama_numels(2, 256, 688, 1000)), max_norm=0.05)
+    s, e = oracle.shard_range(wl.total, wl.world_size, wl.rank)
+    n, M, interval = e - s, 4, 2
+    master = W.master_init(wl, s, e)
+    opt = FlatShardAdamW(wl.numels, world_size=wl.world_size, rank=wl.rank, lr=wl.lr, betas=wl.betas, eps=wl.eps,
+                         weight_decay=wl.weight_decay, max_norm=wl.max_norm, device=DEV, master=master.to(DEV),
+                         capturable=True)
+    scaler = DeviceLossScale(DEV, 2.0 ** 16, 2.0, 0.5, interval, accum_steps=M)
+    micro = [torch.zeros(n, dtype=torch.float16, device=DEV) for _ in range(M)]
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for j in range(M):
+            opt.accum(micro[j], accumulate=j > 0, fuse_norm=j == M - 1, loss_scale=scaler)
+        opt.launch_step()
+        scaler.launch_update(opt.norm_buf)
+    st = oracle.new_state(master.numpy())
+    found_hist = []
+    ref_scale = 2.0 ** 16
+    for t in range(1, 8):
+        S = scaler.scale  # what a backward would multiply the loss by (read here only to build inputs)
+        assert S == ref_scale, (t, S, ref_scale)
+        unscale = float(np.float32(1.0 / (S * M)))
+        acc = np.zeros(n, np.float32)
+        ref_flag = False
+        for j in range(M):
+            g = W.flat_grads(wl.with_(grad_dtype="f32", grad_std=1e-5), t, j, s, e)
+            x = (g * S).to(torch.float16)
+            if t == 3 and j == 2:
+                x[n // 3] = math.inf
+            micro[j].copy_(x.to(DEV))
+            ref_flag |= oracle.accum(acc, raw(x), "f16", unscale, accumulate=j > 0)
+        graph.replay()
+        cr = oracle.step_reference(st, acc, lr=wl.lr, betas=wl.betas, eps=wl.eps, wd=wl.weight_decay,
+                                   max_norm=wl.max_norm)
+        assert ref_flag == (t == 3) and cr.finite == (t != 3)
+        found_hist.append(ref_flag or not cr.finite)
+        ref_scale = oracle.loss_scale_trajectory(found_hist, 2.0 ** 16, 2.0, 0.5, interval)[-1]
+        state = scaler.read()
+        assert state.scale == ref_scale and state.found_inf == 0, (t, state.scale, ref_scale)
+        assert state.unscale == np.float32(1.0 / (ref_scale * M))
+        assert opt.t == st.t == (t if t < 3 else t - 1)
+        for got, ref in ((opt.master, st.p), (opt.exp_avg, st.m), (opt.exp_avg_sq, st.v)):
+            assert bits_equal_f32(raw(got), ref), t
+        assert np.array_equal(raw(opt.lowp), st.lowp)
+    assert ref_scale == 2.0 ** 16 * 2 * 0.5 * 2 * 2

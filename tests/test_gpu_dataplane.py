@@ -131,10 +131,10 @@ def test_reduce_chunks_edge_cases():
     dev_chunks = host.to(DEV)  # device addresses, though none of these calls gets past the host checks
     a, c = ctypes.c_void_p(acc.data_ptr()), ctypes.c_void_p(dev_chunks.data_ptr())
     # checked on the host before any launch: no chunks, stride shorter than n, bad dtype, non-finite scale
-    assert L.zero_reduce_chunks(a, c, zs.ZERO_F16, 0, 10, 10, 1.0, 0, None, None, 0, None) == zs.ZERO_EINVAL
-    assert L.zero_reduce_chunks(a, c, zs.ZERO_F16, 2, 5, 10, 1.0, 0, None, None, 0, None) == zs.ZERO_EINVAL
-    assert L.zero_reduce_chunks(a, c, 7, 2, 10, 10, 1.0, 0, None, None, 0, None) == zs.ZERO_EINVAL
-    assert L.zero_reduce_chunks(a, c, zs.ZERO_F16, 2, 10, 10, float("nan"), 0, None, None, 0, None) == zs.ZERO_EINVAL
+    assert L.zero_reduce_chunks(a, c, zs.ZERO_F16, 0, 10, 10, 1.0, None, 0, None, None, 0, None) == zs.ZERO_EINVAL
+    assert L.zero_reduce_chunks(a, c, zs.ZERO_F16, 2, 5, 10, 1.0, None, 0, None, None, 0, None) == zs.ZERO_EINVAL
+    assert L.zero_reduce_chunks(a, c, 7, 2, 10, 10, 1.0, None, 0, None, None, 0, None) == zs.ZERO_EINVAL
+    assert L.zero_reduce_chunks(a, c, zs.ZERO_F16, 2, 10, 10, float("nan"), None, 0, None, None, 0, None) == zs.ZERO_EINVAL
 
 
 def test_four_ranks_zero2_step_through_the_data_plane():
