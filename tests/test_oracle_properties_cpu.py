@@ -96,3 +96,37 @@ def test_sqnorm_and_clip_vs_float64(seed, n, max_norm):
     cr = oracle.clip(sq, 0.0, max_norm)
     q = max_norm / (math.sqrt(ref) + 1e-6)
     assert cr.coef == (np.float32(q) if q < 1.0 else np.float32(1.0))
+
+
+@SETTINGS
+@given(data=st.data(), dtype=st.sampled_from(["f32", "bf16", "f16"]), log_world=st.integers(0, 4),
+       accumulate=st.booleans())
+def test_reduce_chunks_is_the_rank_order_sum_divided(data, dtype, log_world, accumulate):
+    """For a power-of-two world size, the rank-order sum of the scaled blocks equals torch's
+    float32 rank-order sum divided by the world size, on any block length, padding and
+    starting accumulator (values kept away from subnormals)."""
+    world = 1 << log_world
+    n = data.draw(st.integers(0, 200))
+    pad = data.draw(st.integers(0, 9))
+    seed = data.draw(st.integers(0, 2 ** 31))
+    rng = np.random.default_rng(seed)
+    vals = (rng.standard_normal((world, n + pad)) * 10.0 ** rng.uniform(-3, 3)).astype(np.float32)
+    if dtype == "f32":
+        blocks = vals
+        as_f32 = vals
+    else:
+        conv = oracle.bf16_rne if dtype == "bf16" else oracle.f16_rne
+        blocks = np.stack([conv(v) for v in vals]).reshape(world, n + pad)
+        as_f32 = np.stack([oracle.to_f32(b, dtype) for b in blocks]).reshape(world, n + pad)
+    acc0 = (rng.standard_normal(max(n, 1)) * 10.0).astype(np.float32)
+    got = acc0.copy()
+    oracle.reduce_chunks(got, np.ascontiguousarray(blocks), dtype, n, 1.0 / world, accumulate)
+    ref = torch.from_numpy(as_f32[0, :n].copy())
+    for r in range(1, world):
+        ref = ref + torch.from_numpy(as_f32[r, :n].copy())
+    ref = ref / world
+    if accumulate:  # the accumulator is added first, then each scaled block: compare that order directly
+        ref = torch.from_numpy(acc0[:n].copy())
+        for r in range(world):
+            ref = ref + torch.from_numpy(as_f32[r, :n].copy()) * torch.tensor(1.0 / world, dtype=torch.float32)
+    assert np.array_equal(got[:n], ref.numpy())
