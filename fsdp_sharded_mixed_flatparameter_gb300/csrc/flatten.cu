@@ -223,8 +223,9 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
 //    fp32) source -- all but a few tiles per tensor boundary -- is read with
 //    16-byte loads, eight per thread in flight (no L2 bulk prefetch: measured
 //    on GB300 at 6.74B bf16 grads, a 64 KB prefetch per tile racing these
-//    loads took 2.87 ms, none 1.85 ms = 7.27 TB/s; four or sixteen loads in
-//    flight instead of eight were no better or worse);
+//    loads took 2.87 ms, none 1.85 ms = 7.27 TB/s; with the prefetch, four
+//    loads in flight measured the same as eight and sixteen were slower at
+//    152 registers);
 //  * any other tile (tensor boundaries, a tensor without grad, misaligned
 //    sources, the ragged end) goes element by element: every thread walks
 //    the table forward over its own elements in the contract's order;
