@@ -258,3 +258,66 @@ def test_one_rank_of_eight_full_size_sampled():
             assert np.array_equal(raw(opt.lowp.index_select(0, d_idx)), st.lowp)
         print(f"rank {r} of {N}, step {t}: norm gpu={res.norm:.17g} oracle={cr.norm:.17g} "
               f"coef equal={res.clip_coef == cr.coef}")
+
+
+def test_emulated_ranks_captured_in_one_graph():
+    """The data plane's device work for three emulated ranks -- each rank's reduction of its
+    received blocks with the fused norm, the local sums of squares gathered in rank order,
+    the combine, the device step count and AdamW into the shared low-precision FlatParameter
+    -- captured once in a CUDA graph and replayed over new received blocks (and a NaN in one
+    rank's block at step 2): bit for bit against the oracle after every replay."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW, chunk_layout, zero_shard as zs
+    import workloads as W
+    world, steps = 3, 4
+    wl = W.small_ragged(n_tensors=400, max_log2=13, world_size=world, rank=0, max_norm=0.3, grad_dtype="f16")
+    total = wl.total
+    chunk, padded = chunk_layout(total, world)
+    flat_param = torch.zeros(padded, dtype=torch.bfloat16, device=DEV)
+    opts, states = [], []
+    for r in range(world):
+        s, e = oracle.shard_range(total, world, r)
+        master = W.master_init(wl, s, e)
+        opts.append(FlatShardAdamW(wl.numels, world_size=world, rank=r, lr=wl.lr, betas=wl.betas, eps=wl.eps,
+                                   weight_decay=wl.weight_decay, max_norm=wl.max_norm, device=DEV,
+                                   master=master.to(DEV), lowp_out=flat_param[s:e], capturable=True))
+        states.append(oracle.new_state(raw(master)))
+    recv = [torch.zeros(world, chunk, dtype=torch.float16, device=DEV) for _ in range(world)]  # rank q's inbox
+    gathered = torch.zeros(world, dtype=torch.float64, device=DEV)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for q, opt in enumerate(opts):
+            opt.reduce(recv[q], accumulate=False, scale=1.0 / world, fuse_norm=True)
+            gathered[q:q + 1].copy_(opt.local_sqnorm())
+        for opt in opts:
+            opt.launch_step(gathered_sqnorms=gathered)
+    for t in range(1, steps + 1):
+        full = [torch.zeros(padded, dtype=torch.float16, device=DEV) for _ in range(world)]
+        for r in range(world):
+            full[r][:total] = W.flat_grads(wl.with_(seed=200 + r), t, 0, 0, total, device=DEV)
+        if t == 2:
+            full[2][3] = float("nan")  # in rank 0's chunk: every rank must skip
+        for q in range(world):  # what the all-to-all delivers
+            recv[q].copy_(torch.stack([full[r][q * chunk:(q + 1) * chunk] for r in range(world)]))
+        graph.replay()
+        torch.cuda.synchronize()
+        accs = []
+        for q in range(world):
+            n = opts[q].n
+            a = np.zeros(max(n, 1), np.float32)
+            oracle.reduce_chunks(a, np.ascontiguousarray(raw(recv[q])), "f16", n, 1.0 / world, False)
+            accs.append(a[:n])
+        cr = oracle.clip(oracle.sqnorm(np.concatenate(accs)), 0.0, wl.max_norm)
+        assert cr.finite == (t != 2)
+        for q, (opt, st) in enumerate(zip(opts, states)):
+            r = opt.finish_step()
+            assert r.finite == cr.finite
+            if cr.finite:
+                st.t += 1
+                sc = oracle.adamw_scalars(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay, st.t)
+                oracle.adamw(st.p, st.m, st.v, np.ascontiguousarray(accs[q]), sc, cr.coef, st.lowp)
+        for q, (opt, st) in enumerate(zip(opts, states)):
+            assert opt.t == st.t == (t if t < 2 else t - 1)
+            for got, ref in ((opt.master, st.p), (opt.exp_avg, st.m), (opt.exp_avg_sq, st.v)):
+                assert bits_equal_f32(raw(got), ref), (t, q)
+        assert np.array_equal(raw(flat_param)[:total], np.concatenate([st.lowp for st in states]))
