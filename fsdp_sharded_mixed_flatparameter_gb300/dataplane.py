@@ -32,6 +32,7 @@ through the host); every arithmetic step runs in libzeroshard's kernels.
 """
 from __future__ import annotations
 
+import contextlib
 from typing import List, Optional, Sequence, Tuple
 
 import torch
@@ -151,10 +152,16 @@ class ZeroDataPlane:
             chunks = self.flat_grad.view(1, self.padded)
         opt.reduce(chunks, accumulate=accumulate, scale=sc, fuse_norm=fuse_norm, stream=st)
 
+    def _on(self, stream):
+        """Order host-issued collectives on `stream` (device buffers); host buffers need nothing."""
+        if self.device.type != "cuda":
+            return contextlib.nullcontext()
+        return torch.cuda.stream(torch_stream(stream, self.device))
+
     def all_gather_params(self, stream=None) -> None:
         """Every rank's updated low-precision slice into every rank's flat_param."""
         if self.world_size > 1:
-            with torch.cuda.stream(torch_stream(stream, self.device)):
+            with self._on(stream):
                 gather_shards(self.flat_param, self.group)
 
     def step(self, stream=None) -> zs.NormResult:
@@ -164,6 +171,22 @@ class ZeroDataPlane:
         if r.finite:
             self.all_gather_params(stream)
         return r
+
+    # ------------------------------------------------------------ checkpoint
+    def state_dict(self) -> dict:
+        """This rank's checkpoint: its optimizer shard (step count, fp32 master /
+        exp_avg / exp_avg_sq, its low-precision slice) and the layout it belongs to."""
+        sd = self.opt.state_dict()
+        sd.update(world_size=self.world_size, rank=self.rank, total=self.total)
+        return sd
+
+    def load_state_dict(self, sd: dict, stream=None) -> None:
+        """Restore this rank's shard, then all-gather the low-precision slices so that
+        flat_param holds every rank's parameters again (every rank must call it)."""
+        if (sd["world_size"], sd["rank"], sd["total"]) != (self.world_size, self.rank, self.total):
+            raise ValueError("checkpoint of another layout (world size, rank or parameter count)")
+        self.opt.load_state_dict(sd)
+        self.all_gather_params(stream)
 
     def resident_bytes(self) -> int:
         """Device bytes of this rank: the shard's fp32 state and grad plus the full

@@ -59,6 +59,19 @@ def _rank_main(rank, port, results):
         gather_shards(full, dist.group.WORLD)
         numels = [5, 4, 3]  # total 12: chunk 6, rank 1's shard [6, 12)
         dp = ZeroDataPlane(numels, group=dist.group.WORLD, device="cpu", lr=1e-3)
+        # checkpoint round trip: a rank restores its own shard, the all-gather restores the rest
+        dp.opt.lowp.copy_(torch.full((dp.opt.n,), float(rank + 1)))
+        dp.opt.master.copy_(torch.arange(dp.opt.n, dtype=torch.float32) + 100 * rank)
+        sd = dp.state_dict()
+        dp2 = ZeroDataPlane(numels, group=dist.group.WORLD, device="cpu", lr=1e-3)
+        dp2.load_state_dict(sd)
+        ckpt = {"flat_param": dp2.flat_param.float().tolist(), "master": dp2.opt.master.tolist()}
+        try:
+            bad = dict(sd, rank=1 - rank)
+            dp2.load_state_dict(bad)
+            ckpt["refused"] = False
+        except ValueError:
+            ckpt["refused"] = True
         results[rank] = {
             "recv": recv.tolist(), "full": full.tolist(),
             "chunk": dp.chunk, "padded": dp.padded, "range": (dp.opt.start, dp.opt.end),
@@ -66,6 +79,7 @@ def _rank_main(rank, port, results):
             "lowp_n": dp.opt.lowp.numel(), "grad_n": dp.opt.grad.numel(), "recv_n": dp.recv.numel(),
             "views": [(v.data_ptr() - dp.flat_grad.data_ptr()) // dp.flat_grad.element_size()
                       for v in dp.grad_views()],
+            "ckpt": ckpt,
         }
     finally:
         dist.destroy_process_group()
@@ -86,3 +100,6 @@ def test_two_ranks_exchange_gather_and_layout():
         assert (r["chunk"], r["padded"]) == (6, 12) and tuple(r["range"]) == (s, e)
         assert r["lowp_at"] == s and r["lowp_n"] == e - s == r["grad_n"]
         assert r["recv_n"] == 12 and r["views"] == [0, 5, 9]
+        # every rank's restored slice, gathered into every rank's full FlatParameter
+        assert r["ckpt"]["flat_param"] == [1.0] * 6 + [2.0] * 6
+        assert r["ckpt"]["master"] == [100.0 * q + k for k in range(6)] and r["ckpt"]["refused"]
