@@ -228,7 +228,7 @@ class FlatShardAdamW:
                stream=None, loss_scale=None) -> None:
         """Reduce the ranks' received chunks of this shard into the fp32 shard grad (ZeRO-2/3,
         zero_reduce_chunks): chunks is [world_size, chunk] in rank order, the first n of each
-        row are this shard's values; fuse_norm as for flatten()."""
+        row are this shard's values; fuse_norm and loss_scale as for flatten()."""
         if self.glo != self.start:
             raise ValueError("reduce() needs a shard-only grad buffer (grad_range='shard')")
         sc, dsc, flag = self._scale_args(scale, loss_scale)
@@ -316,7 +316,8 @@ class FlatShardAdamW:
         accumulation: a norm pass reads the grads through the FlatParameter table
         without writing them, then AdamW reads them again through the table.  No
         fp32 flat grad is written (30 instead of 36 bytes per parameter); the result
-        is bit-identical to flatten(scale) + step()."""
+        is bit-identical to flatten(scale) + step().  The grad scale is a host value
+        here (a DeviceLossScale needs the materialized path: flatten/accum + step)."""
         self.launch_step_tensors(grads, scale=scale, stream=stream, process_group=process_group)
         return self.finish_step(stream)
 
