@@ -74,6 +74,22 @@ def _host_parts(tg: W.TensorGrads, numels, offsets, a: int, b: int, nulls):
     return parts, pn
 
 
+def _adamw_parts(st, g, sc, coef, lowp_dtype, threads: int, part: int = 1 << 24) -> None:
+    """The oracle's AdamW over the state, in contiguous parts on host threads when it is
+    large: the update is element-wise, so the parts give the single call's values."""
+    n = st.p.size
+    if threads <= 1 or n <= 2 * part:
+        oracle.adamw(st.p, st.m, st.v, g, sc, coef, st.lowp, lowp_dtype)
+        return
+
+    def one(a):
+        b = min(a + part, n)
+        oracle.adamw(st.p[a:b], st.m[a:b], st.v[a:b], g[a:b], sc, coef, st.lowp[a:b], lowp_dtype)
+
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        list(pool.map(one, range(0, n, part)))
+
+
 def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk: int = 1 << 26,
                  seed: int = 0, fused: bool = True, direct: bool = False, graph: bool = False,
                  oracle_threads: int = ORACLE_THREADS) -> RunReport:
@@ -190,7 +206,7 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
         if cr.finite:
             st.t += 1
             sc = oracle.adamw_scalars(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay, st.t)
-            oracle.adamw(st.p, st.m, st.v, g_shard, sc, cr.coef, st.lowp, wl.lowp_dtype)
+            _adamw_parts(st, g_shard, sc, cr.coef, wl.lowp_dtype, oracle_threads)
         assert opt.t == st.t
 
         # ---- compare
