@@ -12,4 +12,4 @@ from .zero_shard import (  # noqa: F401
     AdamwDeviceState, decode_adamw_device_state, device_hparams, new_adamw_device_state, zero_adamw_prepare_device,
     zero_adamw_scalars, zero_adamw_step_device, zero_adamw_step_tensors_device)
 from .optimizer import FlatShardAdamW, gather_sqnorms, torch_stream  # noqa: F401
-from .dataplane import ZeroDataPlane, chunk_layout, exchange_chunks, gather_shards  # noqa: F401
+from .dataplane import ZeroDataPlane, ZeroUnits, chunk_layout, exchange_chunks, gather_shards  # noqa: F401

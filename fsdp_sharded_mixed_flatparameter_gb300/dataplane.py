@@ -38,7 +38,7 @@ from typing import List, Optional, Sequence, Tuple
 import torch
 
 from . import zero_shard as zs
-from .optimizer import FlatShardAdamW, torch_stream
+from .optimizer import FlatShardAdamW, gather_sqnorms, torch_stream
 
 
 def chunk_layout(total: int, world_size: int) -> Tuple[int, int]:
@@ -195,3 +195,49 @@ class ZeroDataPlane:
         for t in (self.flat_param, self.flat_grad, self.recv):
             b += t.numel() * t.element_size()
         return b
+
+
+class ZeroUnits:
+    """A model wrapped as several FSDP units, one FlatParameter each, stepped together.
+
+    The memory-ledger page (section "FSDP 的关键抽象：FlatParameter") wraps one unit per
+    transformer block: each unit's parameters are flattened into their own FlatParameter,
+    sharded and exchanged on their own (a ZeroDataPlane here), so that no all-gather ever
+    has to hold the whole model.  clip_grad_norm_ still spans every parameter of the
+    model: ``step()`` takes every unit's local sum of squares (fused into its reduction),
+    exchanges the U values of every rank in one all-gather, and every unit of every rank
+    combines the same rank-major, unit-ordered vector -- one norm, one coefficient and
+    one skip decision for the whole model.
+
+    units: the tensor sizes of each unit's FlatParameter; masters: each unit's fp32
+    shard (optional); other keyword arguments go to every ZeroDataPlane."""
+
+    def __init__(self, units: Sequence[Sequence[int]], *, group=None, masters: Optional[Sequence[torch.Tensor]] = None,
+                 **kw):
+        if masters is not None and len(masters) != len(units):
+            raise ValueError("one master shard per unit")
+        self.group = group
+        self.units = [ZeroDataPlane(numels, group=group, master=None if masters is None else masters[i], **kw)
+                      for i, numels in enumerate(units)]
+
+    def reduce_scatter_grads(self, **kw) -> None:
+        """Every unit's exchange and reduction (ZeroDataPlane.reduce_scatter_grads)."""
+        for u in self.units:
+            u.reduce_scatter_grads(**kw)
+
+    def step(self, stream=None) -> zs.NormResult:
+        """One step of every unit with the model's global norm; the units' parameters are
+        all-gathered afterwards (nothing changes, and nothing is gathered, when the norm
+        is not finite)."""
+        dev = self.units[0].device
+        st = torch_stream(stream, dev)
+        with torch.cuda.stream(st):
+            local = torch.cat([u.opt.local_sqnorm(st) for u in self.units])  # this rank's sums, unit order
+            gathered = local if self.units[0].world_size == 1 else gather_sqnorms(local, self.group)
+        for u in self.units:
+            u.opt.launch_step(stream=st, gathered_sqnorms=gathered)
+        results = [u.opt.finish_step(st) for u in self.units]
+        if results[0].finite:
+            for u in self.units:
+                u.all_gather_params(st)
+        return results[0]

@@ -321,3 +321,53 @@ def test_emulated_ranks_captured_in_one_graph():
             for got, ref in ((opt.master, st.p), (opt.exp_avg, st.m), (opt.exp_avg_sq, st.v)):
                 assert bits_equal_f32(raw(got), ref), (t, q)
         assert np.array_equal(raw(flat_param)[:total], np.concatenate([st.lowp for st in states]))
+
+
+def _llama_units(numels):
+    """Split a Llama tensor list into FSDP units: the embedding, each transformer block
+    (9 tensors), and the final norm with the output head."""
+    units = [list(numels[:1])]
+    i = 1
+    while len(numels) - i > 2:
+        units.append(list(numels[i:i + 9]))
+        i += 9
+    units.append(list(numels[i:]))
+    assert sum(map(len, units)) == len(numels)
+    return units
+
+
+def test_units_share_one_global_clip():
+    """Five FSDP units (embedding, three blocks, head), each its own FlatParameter and data
+    plane, stepped with one clip over the whole model: every unit's state bit for bit
+    against the oracle's global-norm step, three steps."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import ZeroUnits
+    import workloads as W
+    wl = W.small_llama(layers=3, hidden=256, mlp=688, vocab=1000, max_norm=0.05)
+    units = _llama_units(wl.numels)
+    offs = np.concatenate([[0], np.cumsum([sum(u) for u in units])]).astype(np.int64)
+    masters = [W.master_init(wl, int(offs[i]), int(offs[i + 1])) for i in range(len(units))]
+    zu = ZeroUnits(units, device=DEV, lr=wl.lr, betas=wl.betas, eps=wl.eps, weight_decay=wl.weight_decay,
+                   max_norm=wl.max_norm, masters=[m.to(DEV) for m in masters])
+    states = [oracle.new_state(raw(m)) for m in masters]
+    for t in range(1, 4):
+        grads = []
+        for i, u in enumerate(zu.units):
+            g = W.flat_grads(wl, t, 0, int(offs[i]), int(offs[i + 1]), device=DEV)
+            u.flat_grad[:g.numel()] = g
+            grads.append(oracle.to_f32(raw(g), "bf16"))
+        zu.reduce_scatter_grads()
+        res = zu.step()
+        cr = oracle.clip(oracle.sqnorm(np.concatenate(grads)), 0.0, wl.max_norm)
+        assert res.finite and cr.coef < 1.0
+        assert abs(res.norm - cr.norm) <= 1e-12 * cr.norm
+        for u, st, g in zip(zu.units, states, grads):
+            st.t += 1
+            sc = oracle.adamw_scalars(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay, st.t)
+            oracle.adamw(st.p, st.m, st.v, g, sc, cr.coef, st.lowp)
+            assert u.opt.t == st.t
+            if res.clip_coef == cr.coef:
+                for got, ref in ((u.opt.master, st.p), (u.opt.exp_avg, st.m), (u.opt.exp_avg_sq, st.v)):
+                    assert bits_equal_f32(raw(got), ref), t
+                assert np.array_equal(raw(u.flat_param)[:st.lowp.size], st.lowp)
+            else:
+                assert_close_f32(raw(u.opt.master), st.p)

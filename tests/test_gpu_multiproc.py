@@ -227,3 +227,99 @@ def test_two_processes_zero2_data_plane():
         st = states[q]
         assert res["master"] == st.p.tobytes() and res["exp_avg"] == st.m.tobytes()
         assert res["exp_avg_sq"] == st.v.tobytes()
+
+
+# ------------------------------------------------------------------ several FSDP units
+def _unit_workload():
+    import workloads as W
+    return W.small_llama(layers=2, hidden=256, mlp=688, vocab=1000, max_norm=0.05)
+
+
+def _units_of(numels):
+    return [list(numels[:1]), list(numels[1:10]), list(numels[10:19]), list(numels[19:])]
+
+
+def _units_rank_main(rank, port, results):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=WORLD, timeout=datetime.timedelta(seconds=180))
+    try:
+        import workloads as W
+        from fsdp_sharded_mixed_flatparameter_gb300 import ZeroUnits, zero_shard_range
+        dev = torch.device("cuda:0")
+        torch.cuda.set_device(dev)
+        wl = _unit_workload()
+        units = _units_of(wl.numels)
+        offs = np.concatenate([[0], np.cumsum([sum(u) for u in units])]).astype(np.int64)
+        masters = []
+        for i, u in enumerate(units):
+            s, e = zero_shard_range(sum(u), WORLD, rank)
+            masters.append(W.master_init(wl, int(offs[i]) + s, int(offs[i]) + e).to(dev))
+        zu = ZeroUnits(units, group=dist.group.WORLD, device=dev, lr=wl.lr, betas=wl.betas, eps=wl.eps,
+                       weight_decay=wl.weight_decay, max_norm=wl.max_norm, masters=masters)
+        norms = []
+        for t in range(1, 3):
+            for i, u in enumerate(zu.units):
+                u.flat_grad[:sum(units[i])] = W.flat_grads(wl.with_(seed=300 + rank), t, 0, int(offs[i]),
+                                                           int(offs[i + 1]), device=dev)
+            zu.reduce_scatter_grads()
+            r = zu.step()
+            norms.append((r.norm, r.clip_coef, r.finite))
+        torch.cuda.synchronize(dev)
+        results[rank] = {"norms": norms,
+                         "params": [u.flat_param.cpu().view(torch.int16).numpy().tobytes() for u in zu.units],
+                         "masters": [u.opt.master.cpu().numpy().tobytes() for u in zu.units]}
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_processes_units_with_one_global_clip():
+    """Four FSDP units across two processes (gloo): every unit exchanged and reduced on its
+    own, one global norm over every unit of both ranks, every rank's parameters after the
+    units' all-gathers equal to the oracle's, bit for bit."""
+    import oracle
+    from _helpers import raw
+    from fsdp_sharded_mixed_flatparameter_gb300 import build
+    import workloads as W
+    build.build()
+    ctx = mp.get_context("spawn")
+    results = ctx.Manager().dict()
+    mp.start_processes(_units_rank_main, args=(_free_port(), results), nprocs=WORLD, start_method="spawn",
+                       join=True)
+    r0, r1 = results[0], results[1]
+    assert repr(r0["norms"]) == repr(r1["norms"]) and r0["params"] == r1["params"]
+    wl = _unit_workload()
+    units = _units_of(wl.numels)
+    offs = np.concatenate([[0], np.cumsum([sum(u) for u in units])]).astype(np.int64)
+    dev = torch.device("cuda:0")
+    states = {}
+    for i, u in enumerate(units):
+        for rank in range(WORLD):
+            s, e = oracle.shard_range(sum(u), WORLD, rank)
+            states[i, rank] = oracle.new_state(raw(W.master_init(wl, int(offs[i]) + s, int(offs[i]) + e)))
+    for t in range(1, 3):
+        accs = {}
+        for i, u in enumerate(units):
+            total = sum(u)
+            chunk = -(-total // WORLD)
+            full = [np.concatenate([raw(W.flat_grads(wl.with_(seed=300 + r), t, 0, int(offs[i]), int(offs[i + 1]),
+                                                     device=dev)), np.zeros(WORLD * chunk - total, np.uint16)])
+                    for r in range(WORLD)]
+            for q in range(WORLD):
+                n = states[i, q].p.size
+                a = np.zeros(max(n, 1), np.float32)
+                oracle.reduce_chunks(a, np.ascontiguousarray(np.stack([f[q * chunk:(q + 1) * chunk] for f in full])),
+                                     "bf16", n, 1.0 / WORLD, False)
+                accs[i, q] = a[:n]
+        cr = oracle.clip(oracle.sqnorm(np.concatenate([accs[k] for k in sorted(accs)])), 0.0, wl.max_norm)
+        nv, coef, fin = r0["norms"][t - 1]
+        assert fin and cr.finite and abs(nv - cr.norm) <= 1e-12 * cr.norm and coef == cr.coef and cr.coef < 1.0
+        for k, st in states.items():
+            st.t += 1
+            sc = oracle.adamw_scalars(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay, st.t)
+            oracle.adamw(st.p, st.m, st.v, np.ascontiguousarray(accs[k]), sc, cr.coef, st.lowp)
+    for i, u in enumerate(units):
+        lowp = np.frombuffer(r0["params"][i], np.uint16)
+        assert np.array_equal(lowp[:sum(u)], np.concatenate([states[i, q].lowp for q in range(WORLD)]))
+        for q, res in ((0, r0), (1, r1)):
+            assert res["masters"][i] == states[i, q].p.tobytes(), (i, q)
