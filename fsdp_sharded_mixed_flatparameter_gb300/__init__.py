@@ -10,6 +10,6 @@ from .zero_shard import (  # noqa: F401
     device_table, lib, new_norm_result, zero_accum, zero_reduce_chunks, zero_adamw_step, zero_adamw_step_tensors, zero_flatten_cast, zero_grad_sqnorm,
     zero_grad_sqnorm_combine, zero_grad_sqnorm_finalize, zero_grad_sqnorm_noalloc, zero_grad_sqnorm_workspace_bytes, zero_shard_range, zero_tensor_table, sqnorm_view,
     AdamwDeviceState, decode_adamw_device_state, device_hparams, new_adamw_device_state, zero_adamw_prepare_device,
-    zero_adamw_scalars, zero_adamw_step_device, zero_adamw_step_tensors_device)
+    zero_adamw_scalars, zero_adamw_step_device, zero_adamw_step_tensors_device, zero_loss_scale_update_device)
 from .optimizer import FlatShardAdamW, gather_sqnorms, torch_stream  # noqa: F401
 from .dataplane import ZeroDataPlane, ZeroUnits, chunk_layout, exchange_chunks, gather_shards  # noqa: F401

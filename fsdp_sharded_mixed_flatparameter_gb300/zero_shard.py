@@ -530,6 +530,19 @@ class DynamicLossScale:
                                             self.growth_factor, self.backoff_factor, self.growth_interval))
 
 
+def zero_loss_scale_update_device(state: torch.Tensor, accum_steps: int, growth_factor: float,
+                                  backoff_factor: float, growth_interval: int,
+                                  norm_result: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The loss-scale update on a zero_loss_scale_state in device memory (one thread)."""
+    if state.numel() * state.element_size() < LOSS_SCALE_STATE_BYTES:
+        raise ValueError("state is smaller than zero_loss_scale_state")
+    if norm_result is not None and norm_result.numel() * norm_result.element_size() < NORM_RESULT_BYTES:
+        raise ValueError("norm_result is smaller than zero_norm_result")
+    _check(lib().zero_loss_scale_update_device(_dev(state, "state"), accum_steps, growth_factor, backoff_factor,
+                                               growth_interval, _dev(norm_result, "norm_result", allow_none=True),
+                                               _stream(stream)))
+
+
 class DeviceLossScale:
     """The GradScaler-style dynamic loss scale kept in device memory (a
     zero_loss_scale_state), for mixed-precision steps captured in a CUDA graph.
@@ -557,12 +570,8 @@ class DeviceLossScale:
     def launch_update(self, norm_result: Optional[torch.Tensor] = None, stream=None) -> None:
         """Enqueue the update after a step (norm_result: the step's zero_norm_result, whose
         non-finite norm also counts as an overflow)."""
-        if norm_result is not None and norm_result.numel() * norm_result.element_size() < NORM_RESULT_BYTES:
-            raise ValueError("norm_result is smaller than zero_norm_result")
-        _check(lib().zero_loss_scale_update_device(_dev(self.state, "state"), self.accum_steps, self.growth_factor,
-                                                   self.backoff_factor, self.growth_interval,
-                                                   _dev(norm_result, "norm_result", allow_none=True),
-                                                   _stream(stream)))
+        zero_loss_scale_update_device(self.state, self.accum_steps, self.growth_factor, self.backoff_factor,
+                                      self.growth_interval, norm_result, stream)
 
     def read(self) -> zero_loss_scale_state:
         raw = bytes(self.state.detach().cpu().numpy().tobytes()[:LOSS_SCALE_STATE_BYTES])
