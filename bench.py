@@ -713,6 +713,69 @@ def run_dataplane(args):
     return 0
 
 
+def llama_unit_numels(numels):
+    """A Llama tensor list as FSDP units: the embedding, each transformer block (9 tensors),
+    the final norm with the output head."""
+    units, i = [list(numels[:1])], 1
+    while len(numels) - i > 2:
+        units.append(list(numels[i:i + 9]))
+        i += 9
+    units.append(list(numels[i:]))
+    return units
+
+
+def run_units(args):
+    """Llama-7B wrapped as 34 FSDP units (embedding, 32 blocks, head), one FlatParameter and
+    data plane each, stepped under one global clip on one GPU (one rank): every unit's
+    reduction with the fused norm, the units' local sums combined, AdamW per unit.  The same
+    bytes as one FlatParameter; the line shows what the 34-way split costs in launches."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import ZeroUnits
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = W.llama7b()
+    units = llama_unit_numels(wl.numels)
+    offs = [0]
+    for u in units:
+        offs.append(offs[-1] + sum(u))
+    zu = ZeroUnits(units, device=dev, lr=wl.lr, betas=wl.betas, eps=wl.eps, weight_decay=wl.weight_decay,
+                   max_norm=wl.max_norm, masters=[W.master_init(wl, offs[i], offs[i + 1], device=dev)
+                                                  for i in range(len(units))])
+    for i, u in enumerate(zu.units):
+        u.flat_grad[:offs[i + 1] - offs[i]] = W.flat_grads(wl, 1, 0, offs[i], offs[i + 1], device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one_step():
+        zu.reduce_scatter_grads()
+        if not zu.step().finite:
+            raise RuntimeError("non-finite grad norm in the benchmark")
+
+    for _ in range(args.warmup):
+        one_step()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        a.record(stream)
+        for _ in range(args.steps):
+            one_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / args.steps
+    line = {
+        "metric": METRIC, "value": wl.total / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{wl.name} as {len(units)} FSDP units", "params_per_rank": wl.total,
+                   "units": len(units), "grad_dtype": "bf16", "lowp_dtype": "bf16", "max_norm": wl.max_norm,
+                   "l2": "inputs larger than L2; no flush"},
+        "bytes_per_param_step": 6 + 30,
+        "gpu_launches": 4 * len(units) * args.steps,  # per unit: reduce, finalize, combine, AdamW
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+    return 0
+
+
 L2_BYTES = 129 << 20
 
 
@@ -899,6 +962,8 @@ def main():
                     help="another configuration's step (a table row, not the headline line)")
     ap.add_argument("--small", action="store_true",
                     help="profiling case for ncu (a smaller list of the same shape), not a bench line")
+    ap.add_argument("--units", action="store_true",
+                    help="Llama-7B as 34 FSDP units (one FlatParameter each) under one clip, one GPU")
     ap.add_argument("--dataplane-ranks", type=int, default=0,
                     help="with one process: time one rank of an N-rank ZeRO-2 Llama-7B job (reduce, norm, AdamW)")
     args = ap.parse_args()
@@ -908,6 +973,8 @@ def main():
         return run_reference(args)
     if args.workload != "llama7b_flat":
         return run_config(args)
+    if args.units:
+        return run_units(args)
     if args.gpus > 1 or args.dataplane_ranks > 1:
         return run_dataplane(args)
     return run_gpu(args)

@@ -236,8 +236,11 @@ class ZeroUnits:
             gathered = local if self.units[0].world_size == 1 else gather_sqnorms(local, self.group)
         for u in self.units:
             u.opt.launch_step(stream=st, gathered_sqnorms=gathered)
-        results = [u.opt.finish_step(st) for u in self.units]
-        if results[0].finite:
+        # every unit combined the same vector: one device-to-host read serves them all
+        result = self.units[0].opt.finish_step(st)
+        for u in self.units[1:]:
+            u.opt.finish_step(st, result=result)
+        if result.finite:
             for u in self.units:
                 u.all_gather_params(st)
-        return results[0]
+        return result

@@ -278,13 +278,17 @@ class FlatShardAdamW:
                                self.betas[0], self.betas[1], self.eps, self.weight_decay, self._t + 1,
                                self.norm_buf, stream)
 
-    def finish_step(self, stream=None) -> zs.NormResult:
+    def finish_step(self, stream=None, result: Optional[zs.NormResult] = None) -> zs.NormResult:
         """Read the step's grad norm (a device->host copy that waits for the step's
         work on `stream`, the stream the step was enqueued on; default: the current
         stream).  With capturable=True the device already advanced (or kept) the
-        step count."""
-        with torch.cuda.stream(torch_stream(stream, self.device)):
-            r = zs.decode_norm_result(self.norm_buf)
+        step count.  `result`: the same step's result already read from another
+        optimizer that combined the same norm (several FSDP units): no second read."""
+        if result is not None:
+            r = result
+        else:
+            with torch.cuda.stream(torch_stream(stream, self.device)):
+                r = zs.decode_norm_result(self.norm_buf)
         if r.finite and not self.capturable:
             self._t += 1
         return r

@@ -103,3 +103,16 @@ def test_two_ranks_exchange_gather_and_layout():
         # every rank's restored slice, gathered into every rank's full FlatParameter
         assert r["ckpt"]["flat_param"] == [1.0] * 6 + [2.0] * 6
         assert r["ckpt"]["master"] == [100.0 * q + k for k in range(6)] and r["ckpt"]["refused"]
+
+
+def test_units_layout_on_the_host():
+    """ZeroUnits builds one FlatParameter per unit, each with its own shard layout, and
+    refuses a master list of the wrong length."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import ZeroUnits
+    units = [[5], [4, 3, 9], [2]]
+    zu = ZeroUnits(units, device="cpu", lr=1e-3)
+    assert [u.total for u in zu.units] == [5, 16, 2]
+    assert [u.flat_param.numel() for u in zu.units] == [5, 16, 2]  # one rank: no padding
+    assert [u.opt.n for u in zu.units] == [5, 16, 2]
+    with pytest.raises(ValueError):
+        ZeroUnits(units, device="cpu", masters=[torch.zeros(5)])
