@@ -769,7 +769,7 @@ def run_units(args):
                    "units": len(units), "grad_dtype": "bf16", "lowp_dtype": "bf16", "max_norm": wl.max_norm,
                    "l2": "inputs larger than L2; no flush"},
         "bytes_per_param_step": 6 + 30,
-        "gpu_launches": 4 * len(units) * args.steps,  # per unit: reduce, finalize, combine, AdamW
+        "gpu_launches": (2 * len(units) + 2) * args.steps,  # per unit reduce + AdamW; one finalize, one combine
         "clocks": clk.summary(),
     }
     print(json.dumps(line))

@@ -33,6 +33,7 @@ through the host); every arithmetic step runs in libzeroshard's kernels.
 from __future__ import annotations
 
 import contextlib
+import math
 from typing import List, Optional, Sequence, Tuple
 
 import torch
@@ -204,24 +205,44 @@ class ZeroUnits:
     transformer block: each unit's parameters are flattened into their own FlatParameter,
     sharded and exchanged on their own (a ZeroDataPlane here), so that no all-gather ever
     has to hold the whole model.  clip_grad_norm_ still spans every parameter of the
-    model: ``step()`` takes every unit's local sum of squares (fused into its reduction),
-    exchanges the U values of every rank in one all-gather, and every unit of every rank
-    combines the same rank-major, unit-ordered vector -- one norm, one coefficient and
-    one skip decision for the whole model.
+    model.  The units' norm partials (fused into their reductions) go to consecutive
+    slices of one shared workspace, so one finalize gives this rank's sum of squares over
+    every unit; the ranks exchange those 8-byte values once; unit 0 combines them in rank
+    order and every other unit's AdamW reads unit 0's result -- one norm, one
+    coefficient and one skip decision for the whole model, in 2 launches plus one
+    reduction and one AdamW per unit.
 
     units: the tensor sizes of each unit's FlatParameter; masters: each unit's fp32
     shard (optional); other keyword arguments go to every ZeroDataPlane."""
 
     def __init__(self, units: Sequence[Sequence[int]], *, group=None, masters: Optional[Sequence[torch.Tensor]] = None,
-                 **kw):
+                 device="cuda", **kw):
+        import torch.distributed as dist
         if masters is not None and len(masters) != len(units):
             raise ValueError("one master shard per unit")
         self.group = group
-        self.units = [ZeroDataPlane(numels, group=group, master=None if masters is None else masters[i], **kw)
+        world = dist.get_world_size(group) if group is not None else 1
+        rank = dist.get_rank(group) if group is not None else 0
+        dev = torch.device(device)
+        # every unit's norm partials in consecutive slices of one workspace (8 bytes per tile)
+        sizes = []
+        for numels in units:
+            s, e = zs.zero_shard_range(int(sum(numels)), world, rank)
+            sizes.append(zs.zero_grad_sqnorm_workspace_bytes(e - s))
+        self.ws = torch.empty(max(sum(sizes), 8), dtype=torch.uint8, device=dev)
+        self.ws_tiles = sum(sizes) // 8
+        offs = [0]
+        for b in sizes:
+            offs.append(offs[-1] + b)
+        self.units = [ZeroDataPlane(numels, group=group, device=dev,
+                                    master=None if masters is None else masters[i],
+                                    workspace=self.ws[offs[i]:offs[i + 1]] if sizes[i] else None, **kw)
                       for i, numels in enumerate(units)]
+        self._local = zs.new_norm_result(dev)
 
     def reduce_scatter_grads(self, **kw) -> None:
-        """Every unit's exchange and reduction (ZeroDataPlane.reduce_scatter_grads)."""
+        """Every unit's exchange and reduction (ZeroDataPlane.reduce_scatter_grads); the
+        norm partials are fused into the last micro-batch's reduction (fuse_norm)."""
         for u in self.units:
             u.reduce_scatter_grads(**kw)
 
@@ -229,15 +250,26 @@ class ZeroUnits:
         """One step of every unit with the model's global norm; the units' parameters are
         all-gathered afterwards (nothing changes, and nothing is gathered, when the norm
         is not finite)."""
-        dev = self.units[0].device
-        st = torch_stream(stream, dev)
-        with torch.cuda.stream(st):
-            local = torch.cat([u.opt.local_sqnorm(st) for u in self.units])  # this rank's sums, unit order
-            gathered = local if self.units[0].world_size == 1 else gather_sqnorms(local, self.group)
+        head = self.units[0]
+        st = torch_stream(stream, head.device)
+        for u in self.units:  # a unit whose last reduction did not fuse the norm: its partials now
+            if not u.opt._norm_ready and u.opt.n > 0:
+                zs.zero_grad_sqnorm(u.opt.grad, 0.0, math.inf, u.opt.ws, self._local, st)
+        # this rank's sum of squares over every unit's tiles (a tile count in elements)
+        zs.zero_grad_sqnorm_finalize(self.ws, self.ws_tiles * 32768, 0.0, math.inf, self._local, st)
+        local = zs.sqnorm_view(self._local)
+        if head.world_size > 1:
+            with torch.cuda.stream(st):
+                gathered = gather_sqnorms(local, self.group)
+        else:
+            gathered = local
+        head.opt.launch_step(stream=st, gathered_sqnorms=gathered)
+        for u in self.units[1:]:
+            u.opt.launch_step(stream=st, norm_result=head.opt.norm_buf)
         for u in self.units:
-            u.opt.launch_step(stream=st, gathered_sqnorms=gathered)
-        # every unit combined the same vector: one device-to-host read serves them all
-        result = self.units[0].opt.finish_step(st)
+            u.opt._norm_ready = False
+        # every unit used the same result: one device-to-host read serves them all
+        result = head.opt.finish_step(st)
         for u in self.units[1:]:
             u.opt.finish_step(st, result=result)
         if result.finite:

@@ -39,7 +39,8 @@ class FlatShardAdamW:
                  betas: Tuple[float, float] = (0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0,
                  max_norm: float = math.inf, lowp_dtype: Optional[torch.dtype] = torch.bfloat16,
                  grad_range: str = "shard", device="cuda", master: Optional[torch.Tensor] = None,
-                 lowp_out: Optional[torch.Tensor] = None, grad_buffer: bool = True, capturable: bool = False):
+                 lowp_out: Optional[torch.Tensor] = None, grad_buffer: bool = True, capturable: bool = False,
+                 workspace: Optional[torch.Tensor] = None):
         if grad_range not in ("shard", "full"):
             raise ValueError("grad_range must be 'shard' or 'full'")
         self.device = torch.device(device)
@@ -68,8 +69,13 @@ class FlatShardAdamW:
             self.lowp = torch.empty(self.n, dtype=lowp_dtype, device=dev)
         else:
             self.lowp = None
-        self.ws = torch.empty(max(zs.zero_grad_sqnorm_workspace_bytes(self.ghi - self.glo), 8), dtype=torch.uint8,
-                              device=dev)
+        need = zs.zero_grad_sqnorm_workspace_bytes(self.ghi - self.glo)
+        if workspace is not None:  # e.g. this optimizer's slice of a workspace shared by several FSDP units
+            if workspace.dtype != torch.uint8 or workspace.numel() < need or workspace.device != dev:
+                raise ValueError(f"workspace must be >= {need} uint8 bytes on {dev}")
+            self.ws = workspace
+        else:
+            self.ws = torch.empty(max(need, 8), dtype=torch.uint8, device=dev)
         self.norm_buf = zs.new_norm_result(dev)
         self.found_nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
         self._t = 0
@@ -256,27 +262,33 @@ class FlatShardAdamW:
         return zs.sqnorm_view(self._local_buf)
 
     def launch_step(self, extra_sqnorm: float = 0.0, stream=None,
-                    gathered_sqnorms: Optional[torch.Tensor] = None) -> None:
+                    gathered_sqnorms: Optional[torch.Tensor] = None,
+                    norm_result: Optional[torch.Tensor] = None) -> None:
         """Enqueue the grad norm and the AdamW step (K4) for t+1 without waiting.
 
         gathered_sqnorms: the ranks' local sums of squares in rank order (float64,
         on this device) for a global norm across ranks; otherwise the norm covers
-        this rank's grad buffer plus `extra_sqnorm`.  When the norm turns out
+        this rank's grad buffer plus `extra_sqnorm`.  norm_result: a zero_norm_result
+        another optimizer already computed for this step (several FSDP units share
+        one clip): used as is, nothing is computed.  When the norm turns out
         non-finite, K4 changes nothing on the device; finish_step() then leaves t
         unchanged.
         """
-        if gathered_sqnorms is not None:
+        clip = self.norm_buf if norm_result is None else norm_result
+        if norm_result is not None:
+            pass
+        elif gathered_sqnorms is not None:
             zs.zero_grad_sqnorm_combine(gathered_sqnorms, self.max_norm, self.norm_buf, stream)
         else:
             self._norm_into(self.norm_buf, extra_sqnorm, self.max_norm, stream)
         if self.capturable:
-            zs.zero_adamw_prepare_device(self._dev_hp, self.norm_buf, self._dev_state, stream)
+            zs.zero_adamw_prepare_device(self._dev_hp, clip, self._dev_state, stream)
             zs.zero_adamw_step_device(self.master, self.exp_avg, self.exp_avg_sq, self.shard_grad(), self.lowp,
-                                      self._dev_state, self.norm_buf, stream)
+                                      self._dev_state, clip, stream)
         else:
             zs.zero_adamw_step(self.master, self.exp_avg, self.exp_avg_sq, self.shard_grad(), self.lowp, self.lr,
                                self.betas[0], self.betas[1], self.eps, self.weight_decay, self._t + 1,
-                               self.norm_buf, stream)
+                               clip, stream)
 
     def finish_step(self, stream=None, result: Optional[zs.NormResult] = None) -> zs.NormResult:
         """Read the step's grad norm (a device->host copy that waits for the step's

@@ -339,7 +339,8 @@ def _llama_units(numels):
 def test_units_share_one_global_clip():
     """Five FSDP units (embedding, three blocks, head), each its own FlatParameter and data
     plane, stepped with one clip over the whole model: every unit's state bit for bit
-    against the oracle's global-norm step, three steps."""
+    against the oracle's global-norm step, three steps (the second without the norm fused
+    into the reductions)."""
     from fsdp_sharded_mixed_flatparameter_gb300 import ZeroUnits
     import workloads as W
     wl = W.small_llama(layers=3, hidden=256, mlp=688, vocab=1000, max_norm=0.05)
@@ -355,7 +356,7 @@ def test_units_share_one_global_clip():
             g = W.flat_grads(wl, t, 0, int(offs[i]), int(offs[i + 1]), device=DEV)
             u.flat_grad[:g.numel()] = g
             grads.append(oracle.to_f32(raw(g), "bf16"))
-        zu.reduce_scatter_grads()
+        zu.reduce_scatter_grads(fuse_norm=t != 2)  # step 2: the norm partials from a separate pass
         res = zu.step()
         cr = oracle.clip(oracle.sqnorm(np.concatenate(grads)), 0.0, wl.max_norm)
         assert res.finite and cr.coef < 1.0
