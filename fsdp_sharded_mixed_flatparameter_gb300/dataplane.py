@@ -246,12 +246,26 @@ class ZeroUnits:
         for u in self.units:
             u.reduce_scatter_grads(**kw)
 
-    def step(self, stream=None) -> zs.NormResult:
-        """One step of every unit with the model's global norm; the units' parameters are
-        all-gathered afterwards (nothing changes, and nothing is gathered, when the norm
-        is not finite)."""
+    def launch_step(self, stream=None) -> None:
+        """Enqueue the model's norm and every unit's AdamW without any host read (with
+        capturable=True units the step count and skip decision stay on the device, so
+        the reductions and this can be captured in one CUDA graph); read the result with
+        finish_step()."""
         head = self.units[0]
         st = torch_stream(stream, head.device)
+        self._launch(st)
+
+    def finish_step(self, stream=None) -> zs.NormResult:
+        """Read the step's result once for every unit (a device-to-host copy)."""
+        head = self.units[0]
+        st = torch_stream(stream, head.device)
+        result = head.opt.finish_step(st)
+        for u in self.units[1:]:
+            u.opt.finish_step(st, result=result)
+        return result
+
+    def _launch(self, st) -> None:
+        head = self.units[0]
         for u in self.units:  # a unit whose last reduction did not fuse the norm: its partials now
             if not u.opt._norm_ready and u.opt.n > 0:
                 zs.zero_grad_sqnorm(u.opt.grad, 0.0, math.inf, u.opt.ws, self._local, st)
@@ -268,10 +282,15 @@ class ZeroUnits:
             u.opt.launch_step(stream=st, norm_result=head.opt.norm_buf)
         for u in self.units:
             u.opt._norm_ready = False
-        # every unit used the same result: one device-to-host read serves them all
-        result = head.opt.finish_step(st)
-        for u in self.units[1:]:
-            u.opt.finish_step(st, result=result)
+
+    def step(self, stream=None) -> zs.NormResult:
+        """One step of every unit with the model's global norm; the units' parameters are
+        all-gathered afterwards (nothing changes, and nothing is gathered, when the norm
+        is not finite)."""
+        head = self.units[0]
+        st = torch_stream(stream, head.device)
+        self._launch(st)
+        result = self.finish_step(st)  # every unit used the same result: one device-to-host read
         if result.finite:
             for u in self.units:
                 u.all_gather_params(st)

@@ -372,3 +372,45 @@ def test_units_share_one_global_clip():
                 assert np.array_equal(raw(u.flat_param)[:st.lowp.size], st.lowp)
             else:
                 assert_close_f32(raw(u.opt.master), st.p)
+
+
+def test_units_captured_in_one_graph():
+    """The five-unit step captured once (every unit's reduction with the fused norm, the one
+    finalize, the combine, the device step count and every unit's AdamW) and replayed over
+    new grads -- a NaN in the last unit at step 2 skips every unit -- bit for bit against
+    the oracle after every replay."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import ZeroUnits
+    import workloads as W
+    wl = W.small_llama(layers=3, hidden=256, mlp=688, vocab=1000, max_norm=0.05)
+    units = _llama_units(wl.numels)
+    offs = np.concatenate([[0], np.cumsum([sum(u) for u in units])]).astype(np.int64)
+    masters = [W.master_init(wl, int(offs[i]), int(offs[i + 1])) for i in range(len(units))]
+    zu = ZeroUnits(units, device=DEV, lr=wl.lr, betas=wl.betas, eps=wl.eps, weight_decay=wl.weight_decay,
+                   max_norm=wl.max_norm, masters=[m.to(DEV) for m in masters], capturable=True)
+    states = [oracle.new_state(raw(m)) for m in masters]
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        zu.reduce_scatter_grads()
+        zu.launch_step()
+    for t in range(1, 5):
+        grads = []
+        for i, u in enumerate(zu.units):
+            g = W.flat_grads(wl, t, 0, int(offs[i]), int(offs[i + 1]), device=DEV)
+            if t == 2 and i == len(units) - 1:
+                g[7] = float("nan")
+            u.flat_grad[:g.numel()] = g
+            grads.append(oracle.to_f32(raw(g), "bf16"))
+        graph.replay()
+        res = zu.finish_step()
+        cr = oracle.clip(oracle.sqnorm(np.concatenate(grads)), 0.0, wl.max_norm)
+        assert res.finite == cr.finite == (t != 2)
+        for u, st, g in zip(zu.units, states, grads):
+            if cr.finite:
+                st.t += 1
+                sc = oracle.adamw_scalars(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay, st.t)
+                oracle.adamw(st.p, st.m, st.v, g, sc, cr.coef, st.lowp)
+            assert u.opt.t == st.t == (t if t < 2 else t - 1)
+            for got, ref in ((u.opt.master, st.p), (u.opt.exp_avg, st.m), (u.opt.exp_avg_sq, st.v)):
+                assert bits_equal_f32(raw(got), ref), t
+            assert np.array_equal(raw(u.flat_param)[:st.lowp.size], st.lowp)
