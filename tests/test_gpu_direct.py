@@ -69,11 +69,19 @@ def test_adamw_tensors_equals_flatten_then_adamw(case, dtype):
             assert np.array_equal(raw(LA.t), raw(LB.t))
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_norm_only_flatten_equals_fused_flatten(dtype):
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("shape", ["ragged", "llama"])
+def test_norm_only_flatten_equals_fused_flatten(dtype, shape):
+    """The norm-only pass's partials equal the writing pass's: ragged tensors (tiles across
+    tensor boundaries, element by element) and Llama-shaped ones (whole 32768-element tiles
+    inside one tensor, the vector path), every grad dtype, a misaligned start or not."""
     from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
-    numels = list(W.ragged_numels(300, seed=17, max_log2=14))
-    host, dev = _table_case(numels, dtype, null=(5,), seed=4, elem_offsets=[0, 2, 7])
+    if shape == "ragged":
+        numels = list(W.ragged_numels(300, seed=17, max_log2=14))
+        host, dev = _table_case(numels, dtype, null=(5,), seed=4, elem_offsets=[0, 2, 7])
+    else:
+        numels = list(W.llama_numels(2, 256, 688, 1000))
+        host, dev = _table_case(numels, dtype, null=(5,), seed=4, elem_offsets=[0, 0, 3])
     table, total = zs.zero_tensor_table(dev, numels)
     d_table = zs.device_table(table, len(numels), DEV)
     for world, rank in ((1, 0), (3, 2)):
