@@ -125,3 +125,43 @@ def test_graph_captured_loss_scaled_steps_with_device_scale():
             assert bits_equal_f32(raw(got), ref), t
         assert np.array_equal(raw(opt.lowp), st.lowp)
     assert ref_scale == 2.0 ** 16 * 2 * 0.5 * 2 * 2
+
+
+def test_device_scale_matches_host_scale_in_every_grad_pass():
+    """A scale read from device memory (d_scale) gives the bits of the same scale passed from
+    the host, in the flatten (writing and norm-only), the accumulation and the reduction,
+    with their fused norm partials and the non-finite flag."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    from test_gpu_kernels import _table_case
+    numels = list(W.llama_numels(1, 256, 688, 1000)) + list(W.ragged_numels(50, seed=2, max_log2=12))
+    host, dev = _table_case(numels, "f16", seed=5, elem_offsets=[0, 3])
+    table, total = zs.zero_tensor_table(dev, numels)
+    d_table = zs.device_table(table, len(numels), DEV)
+    nb = zs.zero_grad_sqnorm_workspace_bytes(total)
+    for scale in (2.0 ** -16 / 4, 0.3):
+        dsc = torch.tensor([scale], dtype=torch.float32, device=DEV)
+        outs = []
+        for d_scale in (None, dsc):
+            hs = scale if d_scale is None else 7.0  # the host value is ignored when d_scale is given
+            flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+            dst = torch.empty(total, device=DEV)
+            ws1 = torch.zeros(nb, dtype=torch.uint8, device=DEV)
+            zs.zero_flatten_cast(d_table, len(numels), total, torch.float16, 0, total, hs, False, dst, flag, ws1,
+                                 d_scale=d_scale)
+            ws2 = torch.zeros(nb, dtype=torch.uint8, device=DEV)
+            zs.zero_flatten_cast(d_table, len(numels), total, torch.float16, 0, total, hs, False, None, flag, ws2,
+                                 d_scale=d_scale)
+            src = torch.cat([x.view(-1) for x in dev])
+            acc = torch.full((total,), 0.5, device=DEV)
+            ws3 = torch.zeros(nb, dtype=torch.uint8, device=DEV)
+            zs.zero_accum(acc, src, hs, True, flag, ws3, d_scale=d_scale)
+            red = torch.zeros(total, device=DEV)
+            ws4 = torch.zeros(nb, dtype=torch.uint8, device=DEV)
+            zs.zero_reduce_chunks(red, torch.stack([src, src.flip(0)]), total, hs, False, flag, ws4, d_scale=d_scale)
+            torch.cuda.synchronize()
+            outs.append(([t.cpu().view(torch.uint8).numpy() for t in (dst, ws1, ws2, acc, ws3, red, ws4)],
+                         flag.item()))
+        (host_bufs, host_flag), (dev_bufs, dev_flag) = outs
+        assert host_flag == dev_flag
+        for a, b in zip(host_bufs, dev_bufs):
+            assert np.array_equal(a, b), scale
