@@ -745,22 +745,31 @@ def run_units(args):
         u.flat_grad[:offs[i + 1] - offs[i]] = W.flat_grads(wl, 1, 0, offs[i], offs[i + 1], device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def one_step():
+    def one_step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
         zu.reduce_scatter_grads()
+        if ev is not None:
+            ev[1].record(stream)
         if not zu.step().finite:
             raise RuntimeError("non-finite grad norm in the benchmark")
+        if ev is not None:
+            ev[2].record(stream)
 
     for _ in range(args.warmup):
         one_step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index) as clk:
         a.record(stream)
-        for _ in range(args.steps):
-            one_step()
+        for k in range(args.steps):
+            one_step(evs[k])
         b.record(stream)
         torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / args.steps
+    t_reduce = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs)
+    t_step = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs)
     line = {
         "metric": METRIC, "value": wl.total / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -769,6 +778,9 @@ def run_units(args):
                    "units": len(units), "grad_dtype": "bf16", "lowp_dtype": "bf16", "max_norm": wl.max_norm,
                    "l2": "inputs larger than L2; no flush"},
         "bytes_per_param_step": 6 + 30,
+        "phases_ms": {"reductions": t_reduce, "norm_adamw_read": t_step},
+        "phases_gbs": {"reductions": 6 * wl.total / (t_reduce / 1e3) / 1e9,
+                       "adamw": 30 * wl.total / (t_step / 1e3) / 1e9},
         "gpu_launches": (2 * len(units) + 2) * args.steps,  # per unit reduce + AdamW; one finalize, one combine
         "clocks": clk.summary(),
     }
