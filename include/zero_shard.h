@@ -9,7 +9,13 @@
  *   zero_grad_sqnorm   global L2 grad norm and the clip coefficient
  *   zero_adamw_step    fused bias-corrected AdamW on fp32 master / exp_avg /
  *                      exp_avg_sq with a bf16 (or f16) parameter write-back
- * plus the host-only helpers zero_shard_range and zero_tensor_table.
+ * plus the host-only helpers zero_shard_range and zero_tensor_table.  Around
+ * them: zero_reduce_chunks (the local reduction of a ZeRO-2/3 reduce-scatter),
+ * zero_grad_sqnorm_finalize / _combine (the norm from fused partials and from
+ * the ranks' sums), the loss-scale updates (host and device), the AdamW
+ * variants that read the grads through the tensor table or take their
+ * scalars from a device step state (graph-capturable steps), and
+ * zero_grad_sqnorm_noalloc.
  *
  * Sources: the ZeRO page (ai6s.net, "cann-recipes-train" ZeRO-1/2/3 on
  * Ascend), the memory-ledger / FlatParameter page (ybb.press,
@@ -19,7 +25,8 @@
  * Conventions for every call:
  *  - Memory.  The library allocates nothing (device or host) and keeps no
  *    state between calls (beyond the fixed scratch array of
- *    zero_grad_sqnorm_noalloc).  The caller owns every buffer.  Pointers prefixed d_ are device addresses;
+ *    zero_grad_sqnorm_noalloc and the debug build's violation record).  The
+ *    caller owns every buffer.  Pointers prefixed d_ are device addresses;
  *    everything else is host memory.
  *  - Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *    default stream).  Device work is enqueued asynchronously on it; no call
