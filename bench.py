@@ -849,6 +849,81 @@ def graph_step_ms(args, wl, s, e, dev, micro, stream, flush=None):
     return ms, b2b
 
 
+def direct_step_ms(args, wl, opt, micro, tables, stream, flush=None) -> dict:
+    """The same step with its last micro-batch never written to the fp32 grad: the
+    earlier micro-batches' passes, then a norm pass over the last one (added on the fly
+    to their sum, or alone without accumulation) that writes only the norm partials, and
+    AdamW reading the last micro-batch through the tensor table (plus the sum).  Timed
+    like the materialized step (per-step events after an L2 flush when `flush` is given)."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    M = wl.micro_batches
+    span = opt.ghi - opt.glo
+    if wl.mode == "zero3":
+        last = (opt.device_flat_table(micro[-1]), 1, span, micro[-1].dtype, 0, span, opt.start - opt.glo)
+    else:
+        table, count, dt = tables[-1]
+        last = (table, count, opt.total, dt, opt.glo, opt.ghi, opt.start)
+    esize = W.torch_dtype(wl.grad_dtype).itemsize
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        for j in range(M - 1):
+            if wl.mode == "zero3":
+                opt.accum(micro[j], accumulate=j > 0, scale=1.0 / M, stream=stream)
+            else:
+                table, count, dt = tables[j]
+                zs.zero_flatten_cast(table, count, opt.total, dt, opt.glo, opt.ghi, 1.0 / M, j > 0, opt.grad, None,
+                                     None, stream)
+        table, count, total, dt, lo, hi, sstart = last
+        zs.zero_flatten_cast(table, count, total, dt, lo, hi, 1.0 / M, zs.NORM_OF_SUM if M > 1 else False,
+                             opt.grad if M > 1 else None, None, opt.ws, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        zs.zero_grad_sqnorm_finalize(opt.ws, span, 0.0, opt.max_norm, opt.norm_buf, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        zs.zero_adamw_step_tensors(opt.master, opt.exp_avg, opt.exp_avg_sq, table, count, total, dt, sstart, 1.0 / M,
+                                   opt.lowp, opt.lr, opt.betas[0], opt.betas[1], opt.eps, opt.weight_decay, opt.t + 1,
+                                   opt.norm_buf, stream, acc=opt.shard_grad() if M > 1 else None)
+        if ev is not None:
+            ev[3].record(stream)
+        if not opt.finish_step().finite:
+            raise RuntimeError("non-finite grad norm in the benchmark")
+
+    for _ in range(args.warmup):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for k in range(args.steps):
+        if flush is not None:
+            flush()
+        step(evs[k])
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = (a.elapsed_time(b) / args.steps if flush is None
+          else statistics.mean(ev[0].elapsed_time(ev[3]) for ev in evs))
+    t_grad = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs)
+    t_k4 = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in evs)
+    n = opt.n
+    acc = 4 if M > 1 else 0
+    # earlier passes: source read, fp32 sum written (first) or read and written (later); the norm pass
+    # reads the last source and the sum; AdamW reads p, m, v, the grad (and the sum), writes p, m, v, lowp
+    grad_bytes = (M - 1) * span * esize + 4 * span * max(0, 1 + 2 * (M - 2)) + span * (esize + acc)
+    k4_bytes = n * (12 + esize + acc + 12 + 2)
+    return {"ms_per_step": ms, "value": n / (ms / 1e3), "unit": UNIT,
+            "kernels_ms": {"grad_passes_and_norm_pass": t_grad, "adamw_from_table": t_k4},
+            "kernels_gbs": {"grad_passes_and_norm_pass": grad_bytes / (t_grad / 1e3) / 1e9,
+                            "adamw_from_table": k4_bytes / (t_k4 / 1e3) / 1e9},
+            "adamw_bytes_per_param": 12 + esize + acc + 12 + 2,
+            "what": "the last micro-batch is never written to the fp32 grad: a norm pass "
+                    + ("adds it to the earlier micro-batches' sum on the fly" if M > 1 else "reads it")
+                    + " and writes only the norm partials, and AdamW reads it through the tensor table"
+                    + (" and adds it to the sum" if M > 1 else "") + "; bit-identical to the materialized step"}
+
+
 def run_config(args):
     """One configuration's whole step on one GPU (its micro-batches, fused norm on the
     last one, AdamW), inputs resident; prints one JSON line with the per-kernel split."""
@@ -930,6 +1005,7 @@ def run_config(args):
         eager_b2b = a.elapsed_time(b) / args.steps
     t_grad = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs)
     t_k4 = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in evs)
+    direct = direct_step_ms(args, wl, opt, micro, tables, stream, flush)
     graph_ms = graph_step_ms(args, wl, s, e, dev, micro, stream, flush) if n <= (1 << 31) else None
     peaks, _ = measured_peaks()
     grad_elems = opt.grad.numel()
@@ -957,6 +1033,7 @@ def run_config(args):
                          "what": "the same step captured once in a CUDA graph (step count and skip decision on the "
                                  "device), no host work or device-to-host read per step; ms_per_step timed like the "
                                  "eager step, back_to_back_ms_per_step = replays one after another"}
+    line["direct"] = direct
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_config_rates(wl)
     print(json.dumps(line))

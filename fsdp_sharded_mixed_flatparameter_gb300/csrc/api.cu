@@ -107,10 +107,12 @@ zero_status zero_flatten_cast(const zero_tensor* d_table, int32_t n_tensors, int
     return fail(ZERO_EINVAL, "zero_flatten_cast: shard [%lld, %lld) outside [0, %lld]", (long long)shard_start,
                 (long long)shard_end, (long long)total);
   if (!zs::valid_dtype(src_dtype)) return fail(ZERO_EINVAL, "zero_flatten_cast: bad src_dtype %d", (int)src_dtype);
-  if (accumulate != 0 && accumulate != 1) return fail(ZERO_EINVAL, "zero_flatten_cast: accumulate must be 0 or 1");
+  if (accumulate < 0 || accumulate > 2) return fail(ZERO_EINVAL, "zero_flatten_cast: accumulate must be 0, 1 or 2");
   if (!std::isfinite(scale)) return fail(ZERO_EINVAL, "zero_flatten_cast: non-finite scale");
   if (shard_end > shard_start && d_dst == nullptr && (d_norm_ws == nullptr || accumulate != 0))
     return fail(ZERO_EINVAL, "zero_flatten_cast: NULL d_dst needs a norm workspace and accumulate == 0");
+  if (accumulate == 2 && d_norm_ws == nullptr)
+    return fail(ZERO_EINVAL, "zero_flatten_cast: accumulate == 2 (norm of the sum only) needs a norm workspace");
   const zero_status w = check_norm_ws("zero_flatten_cast", d_norm_ws, norm_ws_bytes, shard_end - shard_start);
   if (w != ZERO_OK) return w;
   if (shard_end == shard_start) return ZERO_OK;
@@ -289,7 +291,7 @@ zero_status zero_adamw_step(float* d_master, float* d_exp_avg, float* d_exp_avg_
 zero_status zero_adamw_step_tensors(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
                                     const zero_tensor* d_table, int32_t n_tensors, int64_t total,
                                     zero_dtype grad_dtype, int64_t shard_start, float grad_scale,
-                                    void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
+                                    const float* d_acc, void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
                                     const zero_adamw_hparams* hp, int64_t step, const zero_norm_result* d_clip,
                                     void* stream) {
   const char* who = "zero_adamw_step_tensors";
@@ -309,17 +311,19 @@ zero_status zero_adamw_step_tensors(float* d_master, float* d_exp_avg, float* d_
   if (d_param_lowp != nullptr && lowp_dtype != ZERO_BF16 && lowp_dtype != ZERO_F16)
     return fail(ZERO_EINVAL, "%s: lowp_dtype must be BF16 or F16", who);
   if (n == 0) return ZERO_OK;
-  return zs::launch_adamw_table(d_master, d_exp_avg, d_exp_avg_sq, d_table, n_tensors, grad_dtype, shard_start,
-                                grad_scale, d_param_lowp, lowp_dtype, n, s, nullptr, d_clip, zs::as_stream(stream));
+  return zs::launch_adamw_table(d_master, d_exp_avg, d_exp_avg_sq, d_acc, d_table, n_tensors, grad_dtype,
+                                shard_start, grad_scale, d_param_lowp, lowp_dtype, n, s, nullptr, d_clip,
+                                zs::as_stream(stream));
 }
 
 // ------------------------------------------------------------- debug builds
 zero_status zero_debug_errors(uint64_t* out, int32_t reset) {
   if (out == nullptr) return fail(ZERO_EINVAL, "zero_debug_errors: NULL out");
 #ifdef ZERO_DEBUG
-  zero_status (*const readers[])(unsigned long long*, bool) = {zs::debug_read_adamw, zs::debug_read_adamw_table,
-                                                                 zs::debug_read_adamw_device, zs::debug_read_flatten,
-                                                                 zs::debug_read_sqnorm};
+  zero_status (*const readers[])(unsigned long long*, bool) = {
+      zs::debug_read_adamw,          zs::debug_read_adamw_table,        zs::debug_read_adamw_table_acc,
+      zs::debug_read_adamw_table_p4, zs::debug_read_adamw_table_p4_acc, zs::debug_read_adamw_device,
+      zs::debug_read_flatten,        zs::debug_read_sqnorm};
   uint64_t total = 0, first[3] = {0, 0, 0};
   for (auto rd : readers) {
     unsigned long long r[4];
@@ -390,7 +394,7 @@ zero_status zero_adamw_step_device(float* d_master, float* d_exp_avg, float* d_e
 zero_status zero_adamw_step_tensors_device(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
                                            const zero_tensor* d_table, int32_t n_tensors, int64_t total,
                                            zero_dtype grad_dtype, int64_t shard_start, float grad_scale,
-                                           void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
+                                           const float* d_acc, void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
                                            const zero_adamw_device_state* d_state, const zero_norm_result* d_clip,
                                            void* stream) {
   const char* who = "zero_adamw_step_tensors_device";
@@ -409,9 +413,9 @@ zero_status zero_adamw_step_tensors_device(float* d_master, float* d_exp_avg, fl
   if (d_param_lowp != nullptr && lowp_dtype != ZERO_BF16 && lowp_dtype != ZERO_F16)
     return fail(ZERO_EINVAL, "%s: lowp_dtype must be BF16 or F16", who);
   if (n == 0) return ZERO_OK;
-  return zs::launch_adamw_table(d_master, d_exp_avg, d_exp_avg_sq, d_table, n_tensors, grad_dtype, shard_start,
-                                grad_scale, d_param_lowp, lowp_dtype, n, zs::AdamScalars{}, d_state, d_clip,
-                                zs::as_stream(stream));
+  return zs::launch_adamw_table(d_master, d_exp_avg, d_exp_avg_sq, d_acc, d_table, n_tensors, grad_dtype,
+                                shard_start, grad_scale, d_param_lowp, lowp_dtype, n, zs::AdamScalars{}, d_state,
+                                d_clip, zs::as_stream(stream));
 }
 
 }  // extern "C"

@@ -33,8 +33,15 @@
 // (reduce.cuh), so its partial equals bit for bit what the separate norm
 // kernel would compute from the written buffer -- without reading it again.
 //
-// Norm only (K1n, normonly_kernel below): the direct AdamW path needs the
-// norm of the grads but not the flat copy; that pass has its own kernel.
+// Norm of the sum only (STORE = false, with ACC and NORM): the last
+// micro-batch of a step whose AdamW adds it to the accumulator itself
+// (zero_adamw_step_tensors with d_acc) needs the norm of acc + scale * x but
+// not its flat copy: the same pass, reading the accumulator and writing only
+// the partials (6 instead of 10 bytes per element for 16-bit grads).
+//
+// Norm only (K1n, normonly_kernel below): the direct AdamW path without
+// accumulation needs the norm of the grads but not the flat copy; that pass
+// has its own kernel.
 #include <string.h>
 
 #include "common.cuh"
@@ -44,59 +51,7 @@
 
 namespace zs {
 
-// Words m .. m+4 of the 8 words a:b (m block-uniform, 0..3), shifted right by
-// sh = 0 or 16 bits across word boundaries: the 8 16-bit values that start
-// 2*m + sh/16 values into a:b.
-__device__ __forceinline__ uint4 realign16(uint4 a, uint4 b, int m, unsigned sh) {
-  uint32_t q0, q1, q2, q3, q4;
-  switch (m) {
-    case 0: q0 = a.x; q1 = a.y; q2 = a.z; q3 = a.w; q4 = b.x; break;
-    case 1: q0 = a.y; q1 = a.z; q2 = a.w; q3 = b.x; q4 = b.y; break;
-    case 2: q0 = a.z; q1 = a.w; q2 = b.x; q3 = b.y; q4 = b.z; break;
-    default: q0 = a.w; q1 = b.x; q2 = b.y; q3 = b.z; q4 = b.w; break;
-  }
-  return make_uint4(__funnelshift_r(q0, q1, sh), __funnelshift_r(q1, q2, sh), __funnelshift_r(q2, q3, sh),
-                    __funnelshift_r(q3, q4, sh));
-}
-
-// The direct tile's four groups of 8 per thread (groups t + 256 r) from a
-// 16-bit source `src` that is element- but not 16-byte aligned: every thread
-// loads the aligned 16-byte vector under its group, takes the next vector
-// from the neighbouring lane (lane 31 loads it: it is the next warp's), and
-// cuts its 8 values out of the pair in registers -- no shared-memory staging.
-// The vectors read reach up to 7 values before src and after the tile's end;
-// the caller guarantees both lie inside the tensor.
-template <int DT>
-__device__ __forceinline__ void load8_shifted(const char* src, float (&x)[4][8]) {
-  const uintptr_t mis = reinterpret_cast<uintptr_t>(src) % 16;  // 2, 4, ..., 14
-  const char* abase = src - mis;
-  const int m = static_cast<int>(mis >> 2);
-  const unsigned sh = static_cast<unsigned>(mis & 2u) * 8u;
-  const int lane = threadIdx.x & 31;
-  uint4 w[4], nx[4];
-#pragma unroll
-  for (int r = 0; r < 4; ++r) w[r] = ld16_ro(abase + 16 * (threadIdx.x + r * kFlThreads));
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    nx[r] = make_uint4(0u, 0u, 0u, 0u);
-    if (lane == 31) nx[r] = ld16_ro(abase + 16 * (threadIdx.x + r * kFlThreads + 1));
-  }
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const uint4 d = make_uint4(__shfl_down_sync(0xffffffffu, w[r].x, 1), __shfl_down_sync(0xffffffffu, w[r].y, 1),
-                               __shfl_down_sync(0xffffffffu, w[r].z, 1), __shfl_down_sync(0xffffffffu, w[r].w, 1));
-    if (lane != 31) nx[r] = d;
-    const uint4 o = realign16(w[r], nx[r], m, sh);
-    const uint32_t ws[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[r][2 * j] = half_bits_to_f32<DT>(ws[j] & 0xffffu);
-      x[r][2 * j + 1] = half_bits_to_f32<DT>(ws[j] >> 16);
-    }
-  }
-}
-
-template <int DT, bool ACC, bool NORM>
+template <int DT, bool ACC, bool NORM, bool STORE>
 __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* __restrict__ table, int n_tensors,
                                                              int64_t shard_start, int64_t len, int64_t ntiles,
                                                              float* __restrict__ dst, bool dst_vec, float scale,
@@ -110,6 +65,7 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
   constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
   constexpr int kPerBlock = NORM ? static_cast<int>(kSqTile / kFlTile) : 1;  // tiles per block
   static_assert(!NORM || kFlThreads == kSqThreads, "norm tile contract");
+  static_assert(STORE || (ACC && NORM), "a pass that stores nothing is the norm of the accumulated sum");
   const int64_t nblocks_work = (ntiles + kPerBlock - 1) / kPerBlock;
   bool bad = false;
 
@@ -152,12 +108,17 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
 #pragma unroll
           for (int r = 0; r < 4; ++r) load8_src<DT>(tsrc + es * 8 * (threadIdx.x + r * kFlThreads), x[r]);
         } else {
-          load8_shifted<DT>(tsrc, x);
+          load8_shifted<DT, 4>(tsrc, x);
         }
         float a[4][8];
         if (ACC) {
 #pragma unroll
-          for (int r = 0; r < 4; ++r) ld8_rw(dst + base + 8 * (threadIdx.x + r * kFlThreads), a[r]);
+          for (int r = 0; r < 4; ++r) {
+            if (STORE)
+              ld8_rw(dst + base + 8 * (threadIdx.x + r * kFlThreads), a[r]);
+            else
+              ld8_ro(dst + base + 8 * (threadIdx.x + r * kFlThreads), a[r]);  // read-only in this pass
+          }
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -168,7 +129,7 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
             x[r][i] = ACC ? __fadd_rn(a[r][i], y) : y;
           }
           if (NORM) nacc.add8(x[r]);
-          st8(dst + base + 8 * (threadIdx.x + r * kFlThreads), x[r]);
+          if (STORE) st8(dst + base + 8 * (threadIdx.x + r * kFlThreads), x[r]);
         }
         continue;
       }
@@ -186,18 +147,21 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
           for (int i = 0; i < 8; ++i) y[i] = stage[stage_idx(8 * u + i)];
           if (ACC) {
             float a[8];
-            ld8_rw(dst + d, a);
+            if (STORE)
+              ld8_rw(dst + d, a);
+            else
+              ld8_ro(dst + d, a);
 #pragma unroll
             for (int i = 0; i < 8; ++i) y[i] = __fadd_rn(a[i], y[i]);
           }
           if (NORM) nacc.add8(y);
-          st8(dst + d, y);
+          if (STORE) st8(dst + d, y);
         } else {
           for (int i = 0; i < 8 && 8 * u + i < tlen; ++i) {
             const float si = stage[stage_idx(8 * u + i)];
             const float yi = ACC ? __fadd_rn(dst[d + i], si) : si;
             if (NORM) nacc.add1(i, yi);
-            dst[d + i] = yi;
+            if (STORE) dst[d + i] = yi;
           }
         }
       }
@@ -227,8 +191,11 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
 //    loads in flight measured the same as eight and sixteen were slower at
 //    152 registers);
 //  * any other tile (tensor boundaries, a tensor without grad, misaligned
-//    sources, the ragged end) goes element by element: every thread walks
-//    the table forward over its own elements in the contract's order;
+//    sources, the ragged end) is staged in shared memory part by part with
+//    source-aligned vector loads, as the flatten kernel stages its tiles.
+//    (Walking the table element by element instead cost about 50 pure tiles'
+//    time per such tile: 0.88 ms for the 376M-element ragged shard of 20,000
+//    tensors, against 0.26 ms staged);
 //  * for 16-bit grads with a power-of-two scale (EXACT = 1; 2 when the scale
 //    is 1 and the multiply goes away) every value fl(scale * w) has a square
 //    with no rounding residual, so NormAcc::add2_exact gives the general
@@ -239,13 +206,16 @@ __global__ void __launch_bounds__(kFlThreads) flatten_kernel(const zero_tensor* 
 //    no flag).
 // The partials equal bit for bit those of the separate norm kernel over the
 // flattened values, and those of the writing flatten pass with the fused norm.
+// Registers: the exact-square variants are held to 64 (4 blocks per SM, no
+// spills); the general one is left to the compiler's choice (46-54, no
+// spills -- held to 64 it spilled).
 template <int DT, int EXACT>
-__global__ void __launch_bounds__(kSqThreads) normonly_kernel(const zero_tensor* __restrict__ table, int n_tensors,
-                                                              int64_t shard_start, int64_t len, int64_t ntiles,
-                                                              float scale, const float* __restrict__ dscale,
-                                                              int32_t* __restrict__ flag,
-                                                              double* __restrict__ partials) {
+__global__ void __launch_bounds__(kSqThreads, EXACT ? 4 : 0)
+    normonly_kernel(const zero_tensor* __restrict__ table, int n_tensors, int64_t shard_start, int64_t len,
+                    int64_t ntiles, float scale, const float* __restrict__ dscale, int32_t* __restrict__ flag,
+                    double* __restrict__ partials) {
   __shared__ float2 red[kSqThreads / 32];
+  __shared__ float stage[kFlStage];  // tiles with tensor boundaries (37 KB: still 4 blocks per SM)
   constexpr int es = SrcTraits<DT>::esize;
   constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
   static_assert(!EXACT || DT != ZERO_F32, "exact squares: 16-bit grads only");
@@ -317,22 +287,33 @@ __global__ void __launch_bounds__(kSqThreads) normonly_kernel(const zero_tensor*
         }
       }
     } else {
-      // element by element; each thread walks the table forward over its own
-      // elements, which ascend in the contract's (r, i) order
+      // staged in four 8192-element parts: the block reads each source segment of
+      // the part with loads aligned to that source (stage_range), then every thread
+      // adds its groups of the part -- groups 4 * part + r of the contract, r = 0..3,
+      // so the parts in order give the contract's order
       int j = ti;
-      for (int r = 0; r < kSqVecPerThread; ++r) {
-        const int64_t g = base + (static_cast<int64_t>(r) * kSqThreads + threadIdx.x) * 8;
-        for (int i = 0; i < 8 && g + i < len; ++i) {
-          const int64_t kf = shard_start + g + i;
-          while (j + 1 < n_tensors && __ldg(&table[j + 1].flat_offset) <= kf) ++j;
-          const void* p = table[j].ptr;
-          const int64_t off = __ldg(&table[j].flat_offset), num = __ldg(&table[j].numel);
-          float x = 0.0f;
-          if (p != nullptr && ZS_CHECK(kf >= off && kf - off < num, 51, kf)) x = load_elem<DT>(p, kf - off);
-          const float y = __fmul_rn(scale, x);
-          bad |= !finite_f(y);
-          nacc.add1(i, y);
+#pragma unroll 1
+      for (int part = 0; part < static_cast<int>(kSqTile / kFlTile); ++part) {
+        const int64_t plo = base + static_cast<int64_t>(part) * kFlTile;
+        if (plo >= len) break;  // block-uniform: the ragged end
+        const int plen = static_cast<int>((len - plo < kFlTile) ? (len - plo) : kFlTile);
+        const int64_t klo = shard_start + plo;
+        while (j + 1 < n_tensors && __ldg(&table[j + 1].flat_offset) <= klo) ++j;
+        stage_range<DT>(table, n_tensors, j, klo, klo + plen, scale, stage, bad);
+        __syncthreads();
+#pragma unroll 1
+        for (int r = 0; r < static_cast<int>(kFlTile / (8 * kSqThreads)); ++r) {
+          const int g = 8 * (r * kSqThreads + static_cast<int>(threadIdx.x));
+          if (g + 8 <= plen) {
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = stage[stage_idx(g + i)];
+            nacc.add8(y);
+          } else {
+            for (int i = 0; i < 8 && g + i < plen; ++i) nacc.add1(i, stage[stage_idx(g + i)]);
+          }
         }
+        __syncthreads();  // the stage is refilled by the next part
       }
     }
     const double bs = block_sum_norm<kSqThreads>(nacc, red);
@@ -350,7 +331,7 @@ static bool pow2_scale(float scale) {
   return (b & 0x7fffffu) == 0u && ex != 0u && ex != 0xffu;
 }
 
-template <int DT, bool ACC, bool NORM>
+template <int DT, bool ACC, bool NORM, bool STORE = true>
 static zero_status launch_flatten_t(const zero_tensor* table, int32_t n_tensors, int64_t s, int64_t e, float scale,
                                     const float* dscale, float* dst, int32_t* flag, double* partials,
                                     cudaStream_t st) {
@@ -359,8 +340,8 @@ static zero_status launch_flatten_t(const zero_tensor* table, int32_t n_tensors,
   const int64_t per = NORM ? kSqTile / kFlTile : 1;
   const unsigned grid = one_pass_blocks(ntiles, per);
   const bool dst_vec = aligned(dst, 32);
-  flatten_kernel<DT, ACC, NORM><<<grid, kFlThreads, 0, st>>>(table, n_tensors, s, len, ntiles, dst, dst_vec, scale,
-                                                             dscale, flag, partials);
+  flatten_kernel<DT, ACC, NORM, STORE><<<grid, kFlThreads, 0, st>>>(table, n_tensors, s, len, ntiles, dst, dst_vec,
+                                                                    scale, dscale, flag, partials);
   return check_launch("flatten_kernel");
 }
 
@@ -389,8 +370,12 @@ static zero_status launch_normonly(const zero_tensor* table, int32_t n_tensors, 
 
 template <int DT, bool ACC>
 static zero_status launch_flatten_n(const zero_tensor* table, int32_t n_tensors, int64_t s, int64_t e, float scale,
-                                    const float* dscale, float* dst, int32_t* flag, double* partials,
+                                    const float* dscale, bool store, float* dst, int32_t* flag, double* partials,
                                     cudaStream_t st) {
+  if (!store) {  // the norm of dst + the values, dst only read (ACC, dst and partials checked by the caller)
+    if (!ACC || dst == nullptr || partials == nullptr) return ZERO_EINVAL;
+    return launch_flatten_t<DT, true, true, false>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
+  }
   if (dst == nullptr) {  // norm partials only: the grad is not written (ACC is rejected by the caller)
     if (ACC) return ZERO_EINVAL;
     return launch_normonly<DT>(table, n_tensors, s, e, scale, dscale, flag, partials, st);
@@ -400,19 +385,25 @@ static zero_status launch_flatten_n(const zero_tensor* table, int32_t n_tensors,
   return launch_flatten_t<DT, ACC, false>(table, n_tensors, s, e, scale, dscale, dst, flag, nullptr, st);
 }
 
+template <int DT>
+static zero_status launch_flatten_dt(const zero_tensor* table, int32_t n_tensors, int64_t s, int64_t e, float scale,
+                                     const float* dscale, int accumulate, float* dst, int32_t* flag,
+                                     double* partials, cudaStream_t st) {
+  const bool store = accumulate != 2;  // 2: the norm of the accumulated sum, nothing stored
+  if (accumulate != 0)
+    return launch_flatten_n<DT, true>(table, n_tensors, s, e, scale, dscale, store, dst, flag, partials, st);
+  return launch_flatten_n<DT, false>(table, n_tensors, s, e, scale, dscale, store, dst, flag, partials, st);
+}
+
 zero_status launch_flatten(const zero_tensor* table, int32_t n_tensors, int src_dtype, int64_t s, int64_t e,
                            float scale, const float* dscale, int accumulate, float* dst, int32_t* flag,
                            double* partials, cudaStream_t st) {
   if (e <= s) return ZERO_OK;
-  switch (src_dtype * 2 + (accumulate ? 1 : 0)) {
-    case ZERO_F32 * 2: return launch_flatten_n<ZERO_F32, false>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
-    case ZERO_F32 * 2 + 1: return launch_flatten_n<ZERO_F32, true>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
-    case ZERO_BF16 * 2: return launch_flatten_n<ZERO_BF16, false>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
-    case ZERO_BF16 * 2 + 1:
-      return launch_flatten_n<ZERO_BF16, true>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
-    case ZERO_F16 * 2: return launch_flatten_n<ZERO_F16, false>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
-    default: return launch_flatten_n<ZERO_F16, true>(table, n_tensors, s, e, scale, dscale, dst, flag, partials, st);
-  }
+  if (src_dtype == ZERO_F32)
+    return launch_flatten_dt<ZERO_F32>(table, n_tensors, s, e, scale, dscale, accumulate, dst, flag, partials, st);
+  if (src_dtype == ZERO_BF16)
+    return launch_flatten_dt<ZERO_BF16>(table, n_tensors, s, e, scale, dscale, accumulate, dst, flag, partials, st);
+  return launch_flatten_dt<ZERO_F16>(table, n_tensors, s, e, scale, dscale, accumulate, dst, flag, partials, st);
 }
 
 // ------------------------------------------------------------------- K2
@@ -590,8 +581,8 @@ __global__ void __launch_bounds__(kSqThreads) reduce_chunks_kernel(float* __rest
                                                                    int32_t* __restrict__ flag,
                                                                    double* __restrict__ partials) {
   __shared__ float2 red[kSqThreads / 32];
-  constexpr int es = SrcTraits<DT>::esize;
-  constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
+  [[maybe_unused]] constexpr int es = SrcTraits<DT>::esize;  // (the debug build's alignment checks)
+  [[maybe_unused]] constexpr int vb = (DT == ZERO_F32) ? 32 : 16;
   if (dscale != nullptr) scale = *dscale;
   bool bad = false;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {

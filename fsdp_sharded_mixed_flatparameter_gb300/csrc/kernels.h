@@ -31,16 +31,30 @@ zero_status launch_adamw(float* p, float* m, float* v, const float* g, void* low
                          cudaStream_t st);
 
 // AdamW with the grad read through the tensor table (grad_scale * x at flat
-// index shard_start + k) instead of a materialized fp32 grad.
-zero_status launch_adamw_table(float* p, float* m, float* v, const zero_tensor* table, int n_tensors, int grad_dtype,
-                               int64_t shard_start, float gscale, void* lowp, int lowp_dtype, int64_t n,
-                               const AdamScalars& s, const zero_adamw_device_state* ds,
+// index shard_start + k) instead of a materialized fp32 grad; `acc`
+// (nullable): the earlier micro-batches' fp32 sum, added first.
+zero_status launch_adamw_table(float* p, float* m, float* v, const float* acc, const zero_tensor* table,
+                               int n_tensors, int grad_dtype, int64_t shard_start, float gscale, void* lowp,
+                               int lowp_dtype, int64_t n, const AdamScalars& s, const zero_adamw_device_state* ds,
                                const zero_norm_result* clip, cudaStream_t st);
+// Its other instances, each in a translation unit of its own (compiled in
+// parallel): acc != NULL; one table search per four parts (long tables); both.
+using AdamwTableInstance = zero_status(float* p, float* m, float* v, const float* acc, const zero_tensor* table,
+                                       int n_tensors, int grad_dtype, int64_t shard_start, float gscale, void* lowp,
+                                       int lowp_dtype, int64_t n, const AdamScalars& s,
+                                       const zero_adamw_device_state* ds, const zero_norm_result* clip,
+                                       cudaStream_t st);
+AdamwTableInstance launch_adamw_table_acc;
+AdamwTableInstance launch_adamw_table_p4;
+AdamwTableInstance launch_adamw_table_p4_acc;
 
 // Debug builds (ZERO_DEBUG): each translation unit's violation record
 // {count, first site, first index, first block}; reset clears it.
 zero_status debug_read_adamw(unsigned long long* out, bool reset);
 zero_status debug_read_adamw_table(unsigned long long* out, bool reset);
+zero_status debug_read_adamw_table_acc(unsigned long long* out, bool reset);
+zero_status debug_read_adamw_table_p4(unsigned long long* out, bool reset);
+zero_status debug_read_adamw_table_p4_acc(unsigned long long* out, bool reset);
 zero_status debug_read_adamw_device(unsigned long long* out, bool reset);
 zero_status debug_read_flatten(unsigned long long* out, bool reset);
 zero_status debug_read_sqnorm(unsigned long long* out, bool reset);
@@ -57,6 +71,8 @@ zero_status launch_adamw_prepare(const zero_adamw_hparams* hp, const zero_norm_r
 
 // `partials` (nullable): also write the norm tiles' partial sums of squares
 // of the values written (one binary64 per 32768 elements of dst / acc).
+// launch_flatten's accumulate == 2: the values fl(dst + fl(scale * x)) are
+// formed and their partials written, but dst is only read (partials required).
 // `dscale` (nullable): read the scale from device memory when the kernel runs.
 zero_status launch_flatten(const zero_tensor* table, int32_t n_tensors, int src_dtype, int64_t shard_start,
                            int64_t shard_end, float scale, const float* dscale, int accumulate, float* dst,

@@ -1,8 +1,9 @@
 // table.cuh -- reading grads through the FlatParameter tensor table:
 // locating the tensor that holds a flat index, 8-element vector loads of a
-// grad source, and staging a range of the flat buffer into shared memory
-// with loads aligned to each SOURCE tensor.  Shared by the flatten kernel and
-// the AdamW kernel that reads grads straight from the table.  Internal.
+// grad source (aligned, or realigned in registers), and staging a range of
+// the flat buffer into shared memory with loads aligned to each SOURCE
+// tensor.  Shared by the flatten kernel and the AdamW kernel that reads
+// grads straight from the table.  Internal.
 #pragma once
 
 #include "common.cuh"
@@ -66,6 +67,59 @@ __device__ __forceinline__ void load8_src(const void* p, float (&x)[8]) {
     for (int j = 0; j < 4; ++j) {
       x[2 * j] = half_bits_to_f32<DT>(ws[j] & 0xffffu);
       x[2 * j + 1] = half_bits_to_f32<DT>(ws[j] >> 16);
+    }
+  }
+}
+
+// Words m .. m+4 of the 8 words a:b (m block-uniform, 0..3), shifted right by
+// sh = 0 or 16 bits across word boundaries: the 8 16-bit values that start
+// 2*m + sh/16 values into a:b.
+__device__ __forceinline__ uint4 realign16(uint4 a, uint4 b, int m, unsigned sh) {
+  uint32_t q0, q1, q2, q3, q4;
+  switch (m) {
+    case 0: q0 = a.x; q1 = a.y; q2 = a.z; q3 = a.w; q4 = b.x; break;
+    case 1: q0 = a.y; q1 = a.z; q2 = a.w; q3 = b.x; q4 = b.y; break;
+    case 2: q0 = a.z; q1 = a.w; q2 = b.x; q3 = b.y; q4 = b.z; break;
+    default: q0 = a.w; q1 = b.x; q2 = b.y; q3 = b.z; q4 = b.w; break;
+  }
+  return make_uint4(__funnelshift_r(q0, q1, sh), __funnelshift_r(q1, q2, sh), __funnelshift_r(q2, q3, sh),
+                    __funnelshift_r(q3, q4, sh));
+}
+
+// R groups of 8 per thread (groups t + 256 r of a block of 256 threads) from
+// a 16-bit source `src` that is element- but not 16-byte aligned: every
+// thread loads the aligned 16-byte vector under its group, takes the next
+// vector from the neighbouring lane (lane 31 loads it: it is the next
+// warp's), and cuts its 8 values out of the pair in registers -- no
+// shared-memory staging.  The vectors read reach up to 7 values before src
+// and after the last group's end; the caller guarantees both lie inside the
+// tensor.  Every lane of each warp must call it (warp shuffles).
+template <int DT, int R>
+__device__ __forceinline__ void load8_shifted(const char* src, float (&x)[R][8]) {
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(src) % 16;  // 2, 4, ..., 14
+  const char* abase = src - mis;
+  const int m = static_cast<int>(mis >> 2);
+  const unsigned sh = static_cast<unsigned>(mis & 2u) * 8u;
+  const int lane = threadIdx.x & 31;
+  uint4 w[R], nx[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) w[r] = ld16_ro(abase + 16 * (threadIdx.x + r * kFlThreads));
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    nx[r] = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 31) nx[r] = ld16_ro(abase + 16 * (threadIdx.x + r * kFlThreads + 1));
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const uint4 d = make_uint4(__shfl_down_sync(0xffffffffu, w[r].x, 1), __shfl_down_sync(0xffffffffu, w[r].y, 1),
+                               __shfl_down_sync(0xffffffffu, w[r].z, 1), __shfl_down_sync(0xffffffffu, w[r].w, 1));
+    if (lane != 31) nx[r] = d;
+    const uint4 o = realign16(w[r], nx[r], m, sh);
+    const uint32_t ws[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[r][2 * j] = half_bits_to_f32<DT>(ws[j] & 0xffffu);
+      x[r][2 * j + 1] = half_bits_to_f32<DT>(ws[j] >> 16);
     }
   }
 }

@@ -86,6 +86,7 @@ class FlatShardAdamW:
         self._local_buf: Optional[torch.Tensor] = None
         self._registered = None
         self._tables: Dict[tuple, Tuple[torch.Tensor, int]] = {}
+        self._flat_tables: Dict[tuple, torch.Tensor] = {}
 
     # ------------------------------------------------------- step counter
     @property
@@ -327,22 +328,81 @@ class FlatShardAdamW:
         return self.finish_step(stream)
 
     def step_tensors(self, grads: Optional[Sequence[Optional[torch.Tensor]]] = None, *, scale: float = 1.0,
-                     stream=None, process_group=None) -> zs.NormResult:
-        """One step straight from per-tensor grads, for a step without micro-batch
-        accumulation: a norm pass reads the grads through the FlatParameter table
-        without writing them, then AdamW reads them again through the table.  No
-        fp32 flat grad is written (30 instead of 36 bytes per parameter); the result
-        is bit-identical to flatten(scale) + step().  The grad scale is a host value
-        here (a DeviceLossScale needs the materialized path: flatten/accum + step)."""
-        self.launch_step_tensors(grads, scale=scale, stream=stream, process_group=process_group)
+                     stream=None, process_group=None, accumulated: bool = False) -> zs.NormResult:
+        """One step straight from per-tensor grads: a norm pass reads the grads through
+        the FlatParameter table without writing them, then AdamW reads them again
+        through the table.  No fp32 flat grad is written (30 instead of 36 bytes per
+        parameter); the result is bit-identical to flatten(scale) + step().
+
+        accumulated: these grads are the step's LAST micro-batch, and the grad buffer
+        already holds the earlier ones (flatten()/accum() with accumulate=True after
+        the first, without fuse_norm).  The norm pass and AdamW then add them to the
+        buffer on the fly and the last micro-batch is never written (6 + 32 instead
+        of 10 + 30 bytes per parameter); bit-identical to flatten(accumulate=True,
+        scale) + step().
+
+        The grad scale is a host value here (a DeviceLossScale needs the materialized
+        path: flatten/accum + step)."""
+        self.launch_step_tensors(grads, scale=scale, stream=stream, process_group=process_group,
+                                 accumulated=accumulated)
         return self.finish_step(stream)
 
     def launch_step_tensors(self, grads: Optional[Sequence[Optional[torch.Tensor]]] = None, *, scale: float = 1.0,
-                            stream=None, process_group=None) -> None:
+                            stream=None, process_group=None, accumulated: bool = False) -> None:
         """Enqueue step_tensors() without waiting (capturable with registered grads)."""
         table, count, dt = self._resolve(grads)
-        zs.zero_flatten_cast(table, count, self.total, dt, self.glo, self.ghi, scale, False, None,
-                             self.found_nonfinite, self.ws, stream)
+        self._launch_direct(table, count, self.total, dt, self.glo, self.ghi, self.start, scale, accumulated, stream,
+                            process_group)
+
+    def step_flat(self, flat_src: torch.Tensor, *, scale: float = 1.0, stream=None, process_group=None,
+                  accumulated: bool = False) -> zs.NormResult:
+        """step_tensors() for a flat low-precision grad covering the grad range (what
+        accum() takes: ZeRO-2/3 and FSDP, where the rank receives its shard's grads
+        already flat): the last micro-batch is read by the norm pass and by AdamW and
+        never written.  Bit-identical to accum(flat_src, accumulate=accumulated,
+        scale) + step()."""
+        self.launch_step_flat(flat_src, scale=scale, stream=stream, process_group=process_group,
+                              accumulated=accumulated)
+        return self.finish_step(stream)
+
+    def launch_step_flat(self, flat_src: torch.Tensor, *, scale: float = 1.0, stream=None, process_group=None,
+                         accumulated: bool = False) -> None:
+        """Enqueue step_flat() without waiting (capturable once device_flat_table(flat_src)
+        has been called outside the capture)."""
+        table = self.device_flat_table(flat_src)
+        span = self.ghi - self.glo
+        self._launch_direct(table, 1, span, flat_src.dtype, 0, span, self.start - self.glo, scale, accumulated, stream,
+                            process_group)
+
+    def device_flat_table(self, flat_src: torch.Tensor) -> torch.Tensor:
+        """The one-entry tensor table of a flat grad over the grad range, in device memory
+        (built once per address and cached; call it before a CUDA graph capture)."""
+        span = self.ghi - self.glo
+        if flat_src.numel() != span or flat_src.dim() != 1:
+            raise ValueError(f"flat_src must be 1-D with the grad range's {span} elements")
+        key = (flat_src.data_ptr(), flat_src.numel(), flat_src.is_contiguous())
+        hit = self._flat_tables.get(key)
+        if hit is None:
+            table, total = zs.zero_tensor_table([flat_src], [span])
+            assert total == span
+            hit = zs.device_table(table, 1, self.device)
+            if len(self._flat_tables) > 64:
+                self._flat_tables.clear()
+            self._flat_tables[key] = hit
+        return hit
+
+    def _launch_direct(self, table, count: int, total: int, dt, lo: int, hi: int, shard_start: int, scale: float,
+                       accumulated: bool, stream, process_group) -> None:
+        """The direct path over a tensor table: flat indices [lo, hi) are the grad range,
+        [shard_start, shard_start + n) the shard."""
+        if accumulated and self.grad.numel() != self.ghi - self.glo:
+            raise ValueError("accumulated=True needs the grad buffer (grad_buffer=True)")
+        if accumulated:
+            zs.zero_flatten_cast(table, count, total, dt, lo, hi, scale, zs.NORM_OF_SUM, self.grad,
+                                 self.found_nonfinite, self.ws, stream)
+        else:
+            zs.zero_flatten_cast(table, count, total, dt, lo, hi, scale, False, None, self.found_nonfinite, self.ws,
+                                 stream)
         if process_group is not None and self.glo == self.start and _world(process_group) > 1:
             if self._local_buf is None:
                 self._local_buf = zs.new_norm_result(self.device)
@@ -353,15 +413,16 @@ class FlatShardAdamW:
         else:
             zs.zero_grad_sqnorm_finalize(self.ws, self.ghi - self.glo, 0.0, self.max_norm, self.norm_buf, stream)
         self._norm_ready = False
+        acc = self.shard_grad() if accumulated else None
         if self.capturable:
             zs.zero_adamw_prepare_device(self._dev_hp, self.norm_buf, self._dev_state, stream)
-            zs.zero_adamw_step_tensors_device(self.master, self.exp_avg, self.exp_avg_sq, table, count, self.total,
-                                              dt, self.start, scale, self.lowp, self._dev_state, self.norm_buf,
-                                              stream)
+            zs.zero_adamw_step_tensors_device(self.master, self.exp_avg, self.exp_avg_sq, table, count, total,
+                                              dt, shard_start, scale, self.lowp, self._dev_state, self.norm_buf,
+                                              stream, acc=acc)
         else:
-            zs.zero_adamw_step_tensors(self.master, self.exp_avg, self.exp_avg_sq, table, count, self.total, dt,
-                                       self.start, scale, self.lowp, self.lr, self.betas[0], self.betas[1],
-                                       self.eps, self.weight_decay, self._t + 1, self.norm_buf, stream)
+            zs.zero_adamw_step_tensors(self.master, self.exp_avg, self.exp_avg_sq, table, count, total, dt,
+                                       shard_start, scale, self.lowp, self.lr, self.betas[0], self.betas[1],
+                                       self.eps, self.weight_decay, self._t + 1, self.norm_buf, stream, acc=acc)
 
     # -------------------------------------------------------- checkpoint
     def state_dict(self) -> dict:

@@ -96,8 +96,8 @@ def lib() -> ctypes.CDLL:
     L.zero_grad_sqnorm_noalloc.argtypes = [vp, i64, f64, f64, vp, vp]
     L.zero_adamw_step.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, i64, ctypes.POINTER(zero_adamw_hparams), i64,
                                   vp, vp]
-    L.zero_adamw_step_tensors.argtypes = [vp, vp, vp, vp, i32, i64, ctypes.c_int, i64, f32, vp, ctypes.c_int, i64,
-                                          ctypes.POINTER(zero_adamw_hparams), i64, vp, vp]
+    L.zero_adamw_step_tensors.argtypes = [vp, vp, vp, vp, i32, i64, ctypes.c_int, i64, f32, vp, vp, ctypes.c_int,
+                                          i64, ctypes.POINTER(zero_adamw_hparams), i64, vp, vp]
     L.zero_loss_scale_update.argtypes = [ctypes.POINTER(f32), ctypes.POINTER(i32), i32, f64, f64, i32]
     L.zero_loss_scale_update_device.argtypes = [vp, i32, f64, f64, i32, vp, vp]
     L.zero_adamw_scalars.argtypes = [ctypes.POINTER(zero_adamw_hparams), i64, vp]
@@ -105,8 +105,8 @@ def lib() -> ctypes.CDLL:
     L.zero_debug_selftest.argtypes = [i64, vp]
     L.zero_adamw_prepare_device.argtypes = [vp, vp, vp, vp]
     L.zero_adamw_step_device.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, i64, vp, vp, vp]
-    L.zero_adamw_step_tensors_device.argtypes = [vp, vp, vp, vp, i32, i64, ctypes.c_int, i64, f32, vp, ctypes.c_int,
-                                                 i64, vp, vp, vp]
+    L.zero_adamw_step_tensors_device.argtypes = [vp, vp, vp, vp, i32, i64, ctypes.c_int, i64, f32, vp, vp,
+                                                 ctypes.c_int, i64, vp, vp, vp]
     L.zero_status_string.argtypes = [ctypes.c_int]
     L.zero_status_string.restype = ctypes.c_char_p
     L.zero_last_error.argtypes = []
@@ -219,17 +219,37 @@ def _dscale(d_scale: Optional[torch.Tensor]):
     return _dev(d_scale, "d_scale")
 
 
+# zero_flatten_cast's accumulate == 2: the norm of the accumulated sum only (nothing stored)
+NORM_OF_SUM = 2
+
+
+def _accum_mode(accumulate) -> int:
+    if isinstance(accumulate, bool) or accumulate in (0, 1):
+        return int(bool(accumulate))
+    if accumulate == NORM_OF_SUM:
+        return NORM_OF_SUM
+    raise ValueError("accumulate must be False, True or NORM_OF_SUM")
+
+
+def _check_acc(acc: Optional[torch.Tensor], n: int) -> None:
+    if acc is not None and (acc.numel() != n or acc.dtype != torch.float32):
+        raise ValueError("acc must be fp32 with master's size")
+
+
 def zero_flatten_cast(d_table: torch.Tensor, n_tensors: int, total: int, src_dtype: torch.dtype, shard_start: int,
-                      shard_end: int, scale: float, accumulate: bool, dst: torch.Tensor,
+                      shard_end: int, scale: float, accumulate, dst: torch.Tensor,
                       found_nonfinite: Optional[torch.Tensor] = None, norm_ws: Optional[torch.Tensor] = None,
                       stream=None, d_scale: Optional[torch.Tensor] = None) -> None:
+    """accumulate: False / True, or NORM_OF_SUM (2): the norm partials of dst + scale * x
+    into norm_ws, dst only read."""
     if dst is not None and shard_end > shard_start and dst.numel() < shard_end - shard_start:
         raise ValueError("dst is smaller than the shard")
     tab = _dev(d_table, "d_table", torch.uint8, allow_none=n_tensors == 0)
     if n_tensors > 0 and d_table.numel() < n_tensors * TENSOR_ENTRY_BYTES:
         raise ValueError("d_table holds fewer entries than n_tensors")
     _check(lib().zero_flatten_cast(tab, n_tensors, total, _DT[src_dtype], shard_start, shard_end, scale,
-                                   _dscale(d_scale), int(bool(accumulate)), _dev(dst, "dst", torch.float32, allow_none=norm_ws is not None),
+                                   _dscale(d_scale), _accum_mode(accumulate),
+                                   _dev(dst, "dst", torch.float32, allow_none=norm_ws is not None),
                                    _dev(found_nonfinite, "found_nonfinite", torch.int32, allow_none=True),
                                    _dev(norm_ws, "norm_ws", allow_none=True), _ws_bytes(norm_ws), _stream(stream)))
 
@@ -332,12 +352,14 @@ def zero_adamw_step_tensors(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg
                             d_table: torch.Tensor, n_tensors: int, total: int, grad_dtype: torch.dtype,
                             shard_start: int, grad_scale: float, param_lowp: Optional[torch.Tensor], lr: float,
                             beta1: float, beta2: float, eps: float, weight_decay: float, step: int,
-                            clip: Optional[torch.Tensor] = None, stream=None) -> None:
-    """AdamW over [shard_start, shard_start + n) with the grads read through the tensor table."""
+                            clip: Optional[torch.Tensor] = None, stream=None, acc: Optional[torch.Tensor] = None) -> None:
+    """AdamW over [shard_start, shard_start + n) with the grads read through the tensor table;
+    acc: the earlier micro-batches' fp32 sum over the same n elements, added first (or None)."""
     n = master.numel()
     for t, nm in ((exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq")):
         if t.numel() != n:
             raise ValueError(f"{nm} differs in size from master")
+    _check_acc(acc, n)
     if n_tensors > 0 and d_table.numel() < n_tensors * TENSOR_ENTRY_BYTES:
         raise ValueError("d_table holds fewer entries than n_tensors")
     lowp_dt = ZERO_BF16
@@ -352,6 +374,7 @@ def zero_adamw_step_tensors(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg
                                          _dev(exp_avg_sq, "exp_avg_sq", torch.float32),
                                          _dev(d_table, "d_table", torch.uint8, allow_none=n_tensors == 0), n_tensors,
                                          total, _DT[grad_dtype], shard_start, grad_scale,
+                                         _dev(acc, "acc", torch.float32, allow_none=True),
                                          _dev(param_lowp, "param_lowp", allow_none=True), lowp_dt, n, ctypes.byref(hp),
                                          step, _dev(clip, "clip", allow_none=True), _stream(stream)))
 
@@ -441,12 +464,14 @@ def zero_adamw_step_device(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg_
 def zero_adamw_step_tensors_device(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg_sq: torch.Tensor,
                                    d_table: torch.Tensor, n_tensors: int, total: int, grad_dtype: torch.dtype,
                                    shard_start: int, grad_scale: float, param_lowp: Optional[torch.Tensor],
-                                   state: torch.Tensor, clip: Optional[torch.Tensor] = None, stream=None) -> None:
+                                   state: torch.Tensor, clip: Optional[torch.Tensor] = None, stream=None,
+                                   acc: Optional[torch.Tensor] = None) -> None:
     """zero_adamw_step_tensors with the scalars and skip decision of the device step state."""
     n = master.numel()
     for t, nm in ((exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq")):
         if t.numel() != n:
             raise ValueError(f"{nm} differs in size from master")
+    _check_acc(acc, n)
     if n_tensors > 0 and d_table.numel() < n_tensors * TENSOR_ENTRY_BYTES:
         raise ValueError("d_table holds fewer entries than n_tensors")
     if clip is not None and clip.numel() * clip.element_size() < NORM_RESULT_BYTES:
@@ -455,7 +480,8 @@ def zero_adamw_step_tensors_device(master: torch.Tensor, exp_avg: torch.Tensor, 
     _check(lib().zero_adamw_step_tensors_device(
         _dev(master, "master", torch.float32), _dev(exp_avg, "exp_avg", torch.float32),
         _dev(exp_avg_sq, "exp_avg_sq", torch.float32), _dev(d_table, "d_table", torch.uint8, allow_none=n_tensors == 0),
-        n_tensors, total, _DT[grad_dtype], shard_start, grad_scale, lp, lowp_dt, n, _state_arg(state),
+        n_tensors, total, _DT[grad_dtype], shard_start, grad_scale, _dev(acc, "acc", torch.float32, allow_none=True),
+        lp, lowp_dt, n, _state_arg(state),
         _dev(clip, "clip", allow_none=True), _stream(stream)))
 
 

@@ -130,6 +130,11 @@ zero_status zero_tensor_table(const void* const* ptrs, const int64_t* numels, in
  * (0 when its tensor has no grad):
  *   accumulate == 0:  d_dst[k - shard_start] = fl(scale * x)
  *   accumulate == 1:  d_dst[k - shard_start] = fl(d_dst[...] + fl(scale * x))
+ *   accumulate == 2:  the values of accumulate == 1 are formed but not
+ *                     stored (d_dst is only read): the norm workspace is
+ *                     required and receives their partials.  For the last
+ *                     micro-batch of a step whose AdamW adds it to the
+ *                     accumulator itself (zero_adamw_step_tensors, d_acc).
  * d_table: device array of n_tensors entries as built by zero_tensor_table
  *   (sorted by flat_offset, contiguous, ending at `total`).
  * src_dtype: dtype of every grad in the table (F32, BF16 or F16).
@@ -153,8 +158,9 @@ zero_status zero_tensor_table(const void* const* ptrs, const int64_t* numels, in
  *   grad again.  Pass it on the last micro-batch only.
  * Errors: ZERO_EINVAL for n_tensors < 0, d_table NULL with n_tensors > 0,
  * shard bounds outside 0 <= shard_start <= shard_end <= total, d_dst NULL
- * on a non-empty shard, a bad dtype, accumulate not 0/1, a non-finite
- * scale, or a too-small / misaligned norm workspace.  The table's contents
+ * on a non-empty shard (but for the norm-only pass above), a bad dtype,
+ * accumulate not 0/1/2, accumulate == 2 without a norm workspace, a
+ * non-finite scale, or a too-small / misaligned norm workspace.  The table's contents
  * cannot be checked on the host: a table that does not match `total` or
  * points at too-small buffers is the caller's error and reads out of
  * bounds. */
@@ -397,6 +403,14 @@ zero_status zero_loss_scale_update_device(zero_loss_scale_state* d_state, int32_
  * (norm pass with d_dst = NULL, then this) and never writes the 4-byte fp32
  * grad, 30 instead of 36 bytes per parameter, and the fp32 grad buffer
  * (4 bytes/param of HBM) is not needed at all.
+ * d_acc: NULL, or the fp32 sum of the step's earlier micro-batches (n
+ *   elements, element k at flat index shard_start + k, as zero_flatten_cast
+ *   or zero_accum left it): the grad is then fl(d_acc[k] + fl(grad_scale *
+ *   x)), the value the last micro-batch's zero_flatten_cast(..., accumulate
+ *   = 1) would have stored.  With the norm pass zero_flatten_cast(...,
+ *   accumulate = 2), the last micro-batch is never written: 6 + 32 instead
+ *   of 10 + 30 bytes per parameter for 16-bit grads.  Only read; it must not
+ *   overlap the state.  Fast path: 32-byte aligned, like the state.
  * d_table / n_tensors / total / grad_dtype as for zero_flatten_cast; the
  * other arguments as for zero_adamw_step.
  * Errors: those of zero_adamw_step, plus a bad table, [shard_start,
@@ -405,7 +419,7 @@ zero_status zero_loss_scale_update_device(zero_loss_scale_state* d_state, int32_
 zero_status zero_adamw_step_tensors(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
                                     const zero_tensor* d_table, int32_t n_tensors, int64_t total,
                                     zero_dtype grad_dtype, int64_t shard_start, float grad_scale,
-                                    void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
+                                    const float* d_acc, void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
                                     const zero_adamw_hparams* hp, int64_t step,
                                     const zero_norm_result* d_clip, void* stream);
 
@@ -472,7 +486,7 @@ zero_status zero_adamw_step_device(float* d_master, float* d_exp_avg, float* d_e
 zero_status zero_adamw_step_tensors_device(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
                                            const zero_tensor* d_table, int32_t n_tensors, int64_t total,
                                            zero_dtype grad_dtype, int64_t shard_start, float grad_scale,
-                                           void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
+                                           const float* d_acc, void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
                                            const zero_adamw_device_state* d_state,
                                            const zero_norm_result* d_clip, void* stream);
 

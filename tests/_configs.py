@@ -95,12 +95,14 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
                  oracle_threads: int = ORACLE_THREADS) -> RunReport:
     """fused: the last micro-batch's flatten/accumulate also computes the grad
     norm's partials (the norm is then only finalized); otherwise the norm is a
-    separate pass over the flat grad.  direct: one micro-batch of per-tensor
-    grads, stepped with step_tensors() (no fp32 grad buffer at all).  graph: a
+    separate pass over the flat grad.  direct: the last micro-batch is never
+    written to the fp32 grad: step_tensors() (per-tensor grads) or step_flat()
+    (flat ZeRO-3 grads) read it in the norm pass and in AdamW, added to the
+    earlier micro-batches' sum when there are any (without them there is no
+    fp32 grad buffer at all).  graph: a
     capturable optimizer (step count and skip decision on the device); the
     first step's grad passes and step are captured in one CUDA graph and every
     step replays it over grads rewritten in place."""
-    assert not direct or (wl.micro_batches == 1 and wl.mode != "zero3")
     from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
 
     s, e = oracle.shard_range(wl.total, wl.world_size, wl.rank)
@@ -111,7 +113,7 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
     opt = FlatShardAdamW(wl.numels, world_size=wl.world_size, rank=wl.rank, lr=wl.lr, betas=wl.betas, eps=wl.eps,
                          weight_decay=wl.weight_decay, max_norm=wl.max_norm, lowp_dtype=lowp_dt,
                          grad_range="full" if wl.mode == "zero1" else "shard", device=DEV, master=master.clone(),
-                         grad_buffer=not direct, capturable=graph)
+                         grad_buffer=not direct or wl.micro_batches > 1, capturable=graph)
     assert (opt.start, opt.end) == (s, e)
     if sample is None or sample >= n:
         idx = None
@@ -131,13 +133,15 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
     captured = None
 
     def enqueue(micro):
-        for j in range(M):
+        for j in range(M - 1 if direct else M):
             if wl.mode == "zero3":
                 opt.accum(micro[j], accumulate=j > 0, scale=scale, fuse_norm=fused and j == M - 1)
-            elif not direct:
+            else:
                 opt.flatten(micro[j].tensors, accumulate=j > 0, scale=scale, fuse_norm=fused and j == M - 1)
-        if direct:
-            opt.launch_step_tensors(micro[0].tensors)
+        if direct and wl.mode == "zero3":
+            opt.launch_step_flat(micro[-1], scale=scale, accumulated=M > 1)
+        elif direct:
+            opt.launch_step_tensors(micro[-1].tensors, scale=scale, accumulated=M > 1)
         else:
             opt.launch_step()
 
@@ -154,9 +158,11 @@ def run_workload(wl: W.Workload, steps: int, sample: Optional[int] = None, chunk
                 micro.append(tg)
         if graph:
             if captured is None:
-                if wl.mode != "zero3":
-                    for tg in micro:
-                        opt.device_table(tg.tensors)  # device tables built before capture (no copies inside it)
+                for src in micro:  # device tables built before capture (no copies inside it)
+                    if wl.mode != "zero3":
+                        opt.device_table(src.tensors)
+                    elif direct:
+                        opt.device_flat_table(src)
                 torch.cuda.synchronize()
                 captured = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(captured):

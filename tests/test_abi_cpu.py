@@ -103,7 +103,11 @@ def test_invalid_arguments_return_einval_before_any_launch(L):
         L.zero_flatten_cast(FAKE, 2, 10, 1, 6, 5, 1.0, None, 0, FAKE, None, None, 0, None),          # start > end
         L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 11, 1.0, None, 0, FAKE, None, None, 0, None),         # end > total
         L.zero_flatten_cast(FAKE, 2, 10, 7, 0, 5, 1.0, None, 0, FAKE, None, None, 0, None),          # bad dtype
-        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, None, 2, FAKE, None, None, 0, None),          # accumulate 2
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, None, 2, FAKE, None, None, 0, None),          # 2 without norm ws
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, None, 2, None, None, FAKE, 8, None),          # 2 with NULL dst
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, None, 3, FAKE, None, FAKE, 8, None),          # accumulate 3
+        L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, None, -1, FAKE, None, FAKE, 8, None),         # accumulate -1
+        L.zero_accum(FAKE, FAKE, 1, 10, 1.0, None, 2, None, FAKE, 8, None),                          # accumulate 2
         L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, math.nan, None, 0, FAKE, None, None, 0, None),     # NaN scale
         L.zero_flatten_cast(FAKE, 2, 10, 1, 0, 5, 1.0, None, 0, None, None, None, 0, None),          # NULL dst
         L.zero_flatten_cast(FAKE, 0, 10, 1, 0, 5, 1.0, None, 0, FAKE, None, None, 0, None),          # total without tensors
@@ -136,6 +140,21 @@ def test_invalid_arguments_return_einval_before_any_launch(L):
                              zero_adamw_hparams(1e-3, .9, .999, 0.0, 0), zero_adamw_hparams(1e-3, .9, .999, 1e-8, -1),
                              zero_adamw_hparams(math.nan, .9, .999, 1e-8, 0)]):
         cases.append(L.zero_adamw_step(FAKE, FAKE, FAKE, FAKE, None, 1, 10, ctypes.byref(bad), 1, None, None))
+    # AdamW through the tensor table (d_acc is nullable and never the reason for a refusal)
+    cases += [
+        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, None, 2, 10, 1, 0, 1.0, FAKE, None, 1, 5, ctypes.byref(hp), 1,
+                                  None, None),                                                   # NULL table
+        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 6, 1.0, FAKE, None, 1, 5, ctypes.byref(hp), 1,
+                                  None, None),                                                   # past total
+        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, FAKE, 2, 10, 9, 0, 1.0, FAKE, None, 1, 5, ctypes.byref(hp), 1,
+                                  None, None),                                                   # bad grad dtype
+        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 0, math.inf, FAKE, None, 1, 5, ctypes.byref(hp),
+                                  1, None, None),                                                # inf grad_scale
+        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 0, 1.0, FAKE, None, 1, 5, ctypes.byref(hp), 0,
+                                  None, None),                                                   # step 0
+        L.zero_adamw_step_tensors(FAKE, None, FAKE, FAKE, 2, 10, 1, 0, 1.0, FAKE, None, 1, 5, ctypes.byref(hp), 1,
+                                  None, None),                                                   # NULL m
+    ]
     # graph-capturable calls (device step state)
     cases += [
         L.zero_adamw_prepare_device(None, None, FAKE, None),                                   # NULL hp
@@ -145,9 +164,12 @@ def test_invalid_arguments_return_einval_before_any_launch(L):
         L.zero_adamw_step_device(FAKE, FAKE, FAKE, None, None, 1, 10, FAKE, None, None),       # NULL grad
         L.zero_adamw_step_device(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 10, FAKE, None, None),       # F32 lowp
         L.zero_adamw_step_device(FAKE, FAKE, FAKE, FAKE, None, 1, -1, FAKE, None, None),       # n < 0
-        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, None, 2, 10, 1, 0, 1.0, None, 1, 5, FAKE, None, None),
-        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 6, 1.0, None, 1, 5, FAKE, None, None),
-        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 0, 1.0, None, 1, 5, None, None, None),
+        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, None, 2, 10, 1, 0, 1.0, None, None, 1, 5, FAKE, None,
+                                         None),                                                  # NULL table
+        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 6, 1.0, FAKE, None, 1, 5, FAKE, None,
+                                         None),                                                  # past total
+        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 0, 1.0, FAKE, None, 1, 5, None, None,
+                                         None),                                                  # NULL state
         L.zero_loss_scale_update_device(None, 1, 2.0, 0.5, 10, None, None),                     # NULL state
         L.zero_loss_scale_update_device(FAKE, 0, 2.0, 0.5, 10, None, None),                     # accum_steps 0
         L.zero_loss_scale_update_device(FAKE, 1, 1.0, 0.5, 10, None, None),                     # growth 1

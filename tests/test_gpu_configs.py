@@ -84,6 +84,33 @@ def test_ragged_direct_path_full():
     _summary(rep)
 
 
+def test_gpt2_zero1_rank3_direct_accum_full():
+    """GPT-2 ZeRO-1 with the last of the 8 micro-batches never written: the norm over the whole
+    124M buffer and AdamW both add it to the other seven's sum on the fly."""
+    rep = run_workload(W.gpt2_zero1(), steps=10, direct=True)
+    assert all(s.ref_coef < 1.0 for s in rep.steps)
+    _summary(rep)
+
+
+def test_llama13b_zero3_rank7_direct_accum_full_size_all_steps_sampled():
+    """The 13B ZeRO-3 rank at full size, all 20 steps, the last fp16 micro-batch read in place
+    by the norm pass and AdamW (step_flat)."""
+    wl = W.llama13b_zero3()
+    rep = run_workload(wl, steps=wl.steps, sample=1_000_000, direct=True)
+    assert rep.n == 1626983040 and len(rep.steps) == 20
+    assert all(s.ref_coef < 1.0 for s in rep.steps)
+    _summary(rep)
+
+
+def test_llama13b_zero3_shape_direct_accum_graph_all_steps():
+    """The same path captured once in a CUDA graph and replayed for every step, whole shard
+    compared."""
+    wl = W.llama13b_zero3().with_(numels=tuple(W.llama_numels(5, 640, 1728, 4000)), max_norm=0.1)
+    rep = run_workload(wl, steps=W.llama13b_zero3().steps, direct=True, graph=True)
+    assert all(s.ref_coef < 1.0 for s in rep.steps)
+    _summary(rep)
+
+
 def test_llama7b_shape_all_steps():
     wl = W.small_llama(layers=4, hidden=512, mlp=1376, vocab=3200)
     rep = run_workload(wl, steps=W.llama7b().steps, fused=False)

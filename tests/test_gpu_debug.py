@@ -56,7 +56,8 @@ def test_debug_selftest_is_reported():
 
 def test_kernel_suites_record_no_violation_under_the_debug_build():
     suites = ["tests/test_gpu_kernels.py", "tests/test_gpu_direct.py", "tests/test_gpu_graph.py",
-              "tests/test_gpu_amp.py", "tests/test_gpu_multirank.py", "tests/test_gpu_dataplane.py"]
+              "tests/test_gpu_amp.py", "tests/test_gpu_multirank.py", "tests/test_gpu_dataplane.py",
+              "tests/test_gpu_direct_accum.py"]
     # (the 2^32-pattern write-back check and the full-size data-plane rank run once, under the
     # release build: here they would only repeat the same kernel sites for a minute)
     p = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",

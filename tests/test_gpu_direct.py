@@ -26,6 +26,8 @@ def _lib():
 
 CASES = [
     ("ragged", lambda: list(W.ragged_numels(250, seed=13, max_log2=13)), [0, 1, 3, 8, 5], (3,)),
+    # more than 1,024 tensors: AdamW searches the table once per four 2048-element parts
+    ("ragged_long", lambda: list(W.ragged_numels(1500, seed=14, max_log2=14)), [0, 1, 3, 8, 5], (3, 700)),
     ("llama", lambda: list(W.llama_numels(1, 256, 688, 1000)), [0], ()),
 ]
 
@@ -70,17 +72,23 @@ def test_adamw_tensors_equals_flatten_then_adamw(case, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
-@pytest.mark.parametrize("shape", ["ragged", "llama"])
+@pytest.mark.parametrize("shape", ["ragged", "llama", "llama_large"])
 def test_norm_only_flatten_equals_fused_flatten(dtype, shape):
-    """The norm-only pass's partials equal the writing pass's: ragged tensors (tiles across
-    tensor boundaries, element by element) and Llama-shaped ones (whole 32768-element tiles
-    inside one tensor, the vector path), every grad dtype, a misaligned start or not."""
+    """The norm-only pass's partials equal the writing pass's, on both of its kernels: lists of
+    small tensors (ragged, and a small Llama list: the tiled kernel without stores, staged and
+    vector tiles) and of large ones (a Llama list with tensors of millions of elements: K1n,
+    whole 32768-element tiles inside one tensor on the vector path, tensor boundaries element
+    by element), every grad dtype, a misaligned start or not."""
     from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
     if shape == "ragged":
         numels = list(W.ragged_numels(300, seed=17, max_log2=14))
         host, dev = _table_case(numels, dtype, null=(5,), seed=4, elem_offsets=[0, 2, 7])
-    else:
+    elif shape == "llama":
         numels = list(W.llama_numels(2, 256, 688, 1000))
+        host, dev = _table_case(numels, dtype, null=(5,), seed=4, elem_offsets=[0, 0, 3])
+    else:
+        numels = list(W.llama_numels(1, 1024, 2752, 2000))
+        assert sum(numels) // len(numels) > 16 * 32768  # the K1n side of the kernel choice
         host, dev = _table_case(numels, dtype, null=(5,), seed=4, elem_offsets=[0, 0, 3])
     table, total = zs.zero_tensor_table(dev, numels)
     d_table = zs.device_table(table, len(numels), DEV)

@@ -492,14 +492,17 @@ def test_exact_square_norm_equals_separate_norm(dtype):
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_exact_square_norm_flags_nonfinite(dtype):
     """The exact-square path (flag decided from the sum, values re-read) raises the flag for inf and NaN grads,
-    in in-tensor and staged tiles alike, and only for them: a finite bf16 grad whose
+    in in-tensor and boundary tiles alike, and only for them: a finite bf16 grad whose
     square overflows binary32 makes the norm non-finite without raising the flag."""
     from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
     tdt = W.torch_dtype(dtype)
-    numels = list(W.llama_numels(1, 256, 688, 1000))
+    numels = list(W.llama_numels(1, 1024, 2752, 2000))  # tensors large enough for K1n's exact-square path
+    assert sum(numels) // len(numels) > 16 * 32768
     specials = [math.inf, -math.inf, math.nan] + ([2.0 ** 70] if dtype == "bf16" else [])
     for value in specials:
-        for where in ((0, 5000), (4, 40000), (1, 5000), (len(numels) - 1, numels[-1] - 1)):  # in-tensor, staged
+        # inside a tensor (vector tiles), in a norm tensor between two large ones and at the very
+        # end (tiles with tensor boundaries: element by element)
+        for where in ((0, 5000), (4, 40000), (1, 5000), (8, 100), (len(numels) - 1, numels[-1] - 1)):
             g = torch.Generator().manual_seed(3)
             host = [(torch.randn(n, generator=g) * 1e-2).to(tdt) for n in numels]
             host[where[0]][where[1]] = value
@@ -604,7 +607,9 @@ def test_cast_and_exact_square_norm_exhaustive_over_16bit_patterns(dtype):
     # all f16 values; bf16 below 2^40, the subnormals and both zeros included)
     expo = (allbits >> (7 if dtype == "bf16" else 10)) & (0xFF if dtype == "bf16" else 0x1F)
     finite = allbits[expo < (127 + 40 if dtype == "bf16" else 0x1F)]
-    reps = np.tile(finite, 4)  # several norm tiles, each element in different positions
+    # several norm tiles, each element in different positions; one tensor of more than 16 norm
+    # tiles, so that the norm-only pass takes K1n (whose exact-square path this checks)
+    reps = np.tile(finite, -(-(17 * 32768) // finite.size))
     fd = torch.from_numpy(reps.view(np.int16).copy()).view(tdt).to(DEV)
     n = fd.numel()
     table, total = zs.zero_tensor_table([fd], [n])
