@@ -287,10 +287,12 @@ __global__ void __launch_bounds__(kSqThreads, EXACT ? 4 : 0)
         }
       }
     } else {
-      // staged in four 8192-element parts: the block reads each source segment of
-      // the part with loads aligned to that source (stage_range), then every thread
-      // adds its groups of the part -- groups 4 * part + r of the contract, r = 0..3,
-      // so the parts in order give the contract's order
+      // four 8192-element parts, each thread adding its groups of the part -- groups
+      // 4 * part + r of the contract, r = 0..3, so the parts in order give the
+      // contract's order.  A part inside one tensor is read straight from it (16-byte
+      // loads, realigned in registers when the source is off the 16-byte grid);
+      // any other is staged: the block reads each source segment of the part with
+      // loads aligned to that source (stage_range) into shared memory
       int j = ti;
 #pragma unroll 1
       for (int part = 0; part < static_cast<int>(kSqTile / kFlTile); ++part) {
@@ -299,6 +301,33 @@ __global__ void __launch_bounds__(kSqThreads, EXACT ? 4 : 0)
         const int plen = static_cast<int>((len - plo < kFlTile) ? (len - plo) : kFlTile);
         const int64_t klo = shard_start + plo;
         while (j + 1 < n_tensors && __ldg(&table[j + 1].flat_offset) <= klo) ++j;
+        const void* pptr = table[j].ptr;
+        const int64_t poff = __ldg(&table[j].flat_offset), pnum = __ldg(&table[j].numel);
+        const char* psrc = pptr ? static_cast<const char*>(pptr) + es * (klo - poff) : nullptr;
+        // block-uniform
+        const bool pin = plen == kFlTile && psrc != nullptr && poff <= klo && klo + kFlTile <= poff + pnum;
+        const bool pdirect = pin && reinterpret_cast<uintptr_t>(psrc) % vb == 0;
+        const bool pshift = DT != ZERO_F32 && pin && !pdirect && klo - poff >= 8 && klo + kFlTile + 8 <= poff + pnum &&
+                            ZS_CHECK(aligned(psrc, es), 54, klo);
+        if (pdirect || pshift) {
+          float x[4][8];
+          if (pdirect) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) load8_src<DT>(psrc + es * 8 * (r * kSqThreads + threadIdx.x), x[r]);
+          } else {
+            load8_shifted<DT, 4>(psrc, x);  // every lane (warp shuffles); the reads stay inside the tensor
+          }
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              x[r][i] = __fmul_rn(scale, x[r][i]);
+              bad |= !finite_f(x[r][i]);
+            }
+            nacc.add8(x[r]);
+          }
+          continue;
+        }
         stage_range<DT>(table, n_tensors, j, klo, klo + plen, scale, stage, bad);
         __syncthreads();
 #pragma unroll 1
