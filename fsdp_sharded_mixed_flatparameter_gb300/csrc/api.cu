@@ -111,7 +111,7 @@ zero_status zero_flatten_cast(const zero_tensor* d_table, int32_t n_tensors, int
   if (!std::isfinite(scale)) return fail(ZERO_EINVAL, "zero_flatten_cast: non-finite scale");
   if (shard_end > shard_start && d_dst == nullptr && (d_norm_ws == nullptr || accumulate != 0))
     return fail(ZERO_EINVAL, "zero_flatten_cast: NULL d_dst needs a norm workspace and accumulate == 0");
-  if (accumulate == 2 && d_norm_ws == nullptr)
+  if (accumulate == 2 && shard_end > shard_start && d_norm_ws == nullptr)
     return fail(ZERO_EINVAL, "zero_flatten_cast: accumulate == 2 (norm of the sum only) needs a norm workspace");
   const zero_status w = check_norm_ws("zero_flatten_cast", d_norm_ws, norm_ws_bytes, shard_end - shard_start);
   if (w != ZERO_OK) return w;

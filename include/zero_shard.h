@@ -159,8 +159,9 @@ zero_status zero_tensor_table(const void* const* ptrs, const int64_t* numels, in
  * Errors: ZERO_EINVAL for n_tensors < 0, d_table NULL with n_tensors > 0,
  * shard bounds outside 0 <= shard_start <= shard_end <= total, d_dst NULL
  * on a non-empty shard (but for the norm-only pass above), a bad dtype,
- * accumulate not 0/1/2, accumulate == 2 without a norm workspace, a
- * non-finite scale, or a too-small / misaligned norm workspace.  The table's contents
+ * accumulate not 0/1/2, accumulate == 2 on a non-empty shard without a
+ * norm workspace, a non-finite scale, or a too-small / misaligned norm
+ * workspace.  The table's contents
  * cannot be checked on the host: a table that does not match `total` or
  * points at too-small buffers is the caller's error and reads out of
  * bounds. */

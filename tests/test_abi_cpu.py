@@ -187,6 +187,9 @@ def test_empty_calls_are_noops_without_a_gpu(L):
     from fsdp_sharded_mixed_flatparameter_gb300.zero_shard import zero_adamw_hparams
     hp = zero_adamw_hparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
     assert L.zero_flatten_cast(None, 0, 0, 1, 0, 0, 1.0, None, 0, None, None, None, 0, None) == 0
+    assert L.zero_flatten_cast(None, 0, 0, 1, 0, 0, 1.0, None, 2, None, None, None, 0, None) == 0  # norm of the sum
+    assert L.zero_adamw_step_tensors(None, None, None, None, 0, 0, 1, 0, 1.0, None, None, 1, 0, ctypes.byref(hp), 1,
+                                     None, None) == 0
     assert L.zero_accum(None, None, 1, 0, 1.0, None, 0, None, None, 0, None) == 0
     assert L.zero_adamw_step(None, None, None, None, None, 1, 0, ctypes.byref(hp), 1, None, None) == 0
 

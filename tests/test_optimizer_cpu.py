@@ -79,4 +79,27 @@ def test_no_cpu_fallback():
         opt.flatten(grads, accumulate=False)
     with pytest.raises(ValueError):
         opt.step()
+    with pytest.raises(ValueError):  # the direct path (last micro-batch read in place) likewise
+        opt.step_tensors(grads, accumulated=True)
+    with pytest.raises(ValueError):
+        opt.step_flat(torch.zeros(opt.ghi - opt.glo, dtype=torch.bfloat16), accumulated=True)
     assert opt.t == 0 and math.isfinite(opt.lr)
+
+
+def test_direct_path_argument_checks():
+    """step_flat wants a 1-D grad over the grad range; the accumulated direct path wants the
+    grad buffer; the binding's accumulate argument takes False / True / NORM_OF_SUM only."""
+    from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
+    from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
+    opt, numels = _opt()
+    with pytest.raises(ValueError):
+        opt.device_flat_table(torch.zeros(opt.ghi - opt.glo + 1, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        opt.device_flat_table(torch.zeros(1, opt.ghi - opt.glo, dtype=torch.bfloat16))
+    nobuf = FlatShardAdamW(numels, device="cpu", grad_buffer=False)
+    with pytest.raises(ValueError, match="grad buffer"):
+        nobuf._launch_direct(None, 0, nobuf.total, torch.bfloat16, 0, nobuf.total, 0, 1.0, True, None, None)
+    assert [zs._accum_mode(a) for a in (False, True, 0, 1, zs.NORM_OF_SUM)] == [0, 1, 0, 1, 2]
+    for bad in (3, -1, 2.5):
+        with pytest.raises(ValueError):
+            zs._accum_mode(bad)
