@@ -215,7 +215,9 @@ def test_resume_and_determinism_bit_identical():
 
 def test_empty_and_single_element_shards():
     """More ranks than elements: empty shards step as no-ops (t still advances: the
-    norm of nothing is 0), one-element shards update like the oracle."""
+    norm of nothing is 0), one-element shards update like the oracle -- through the
+    materialized step, the direct path, and the direct path with accumulation over
+    per-tensor and flat grads (two halves: the same grad exactly)."""
     from fsdp_sharded_mixed_flatparameter_gb300 import FlatShardAdamW
     import oracle
     dev = torch.device("cuda:0")
@@ -223,22 +225,31 @@ def test_empty_and_single_element_shards():
     g = [torch.tensor([1e-3, -2e-3, 3e-3], dtype=torch.bfloat16), torch.tensor([4e-3, 0.0], dtype=torch.bfloat16)]
     full = np.zeros(5, np.float32)
     oracle.flatten([x.view(torch.int16).numpy().view(np.uint16) for x in g], numels, "bf16", 0, 5, 1.0, full, False)
+    modes = ("materialized", "direct", "direct_accumulated", "flat_accumulated")
     for rank in range(8):
         s, e = oracle.shard_range(5, 8, rank)
         p0 = torch.linspace(-1, 1, 5)[s:e].contiguous()
         opt = FlatShardAdamW(numels, world_size=8, rank=rank, lr=1e-2, max_norm=1.0, device=dev, master=p0.to(dev))
-        for direct in (False, True):
-            if direct:
-                r = opt.step_tensors([x.to(dev) for x in g])
+        dg = [x.to(dev) for x in g]
+        flat = torch.cat(g)[s:e].contiguous().to(dev)
+        for mode in modes:
+            if mode == "direct":
+                r = opt.step_tensors(dg)
+            elif mode == "direct_accumulated":
+                opt.flatten(dg, accumulate=False, scale=0.5)
+                r = opt.step_tensors(dg, scale=0.5, accumulated=True)
+            elif mode == "flat_accumulated":
+                opt.accum(flat, accumulate=False, scale=0.5)
+                r = opt.step_flat(flat, scale=0.5, accumulated=True)
             else:
-                opt.flatten([x.to(dev) for x in g], accumulate=False, fuse_norm=True)
+                opt.flatten(dg, accumulate=False, fuse_norm=True)
                 r = opt.step()
             assert r.finite
         st = oracle.new_state(p0.numpy())
-        for _ in range(2):
+        for _ in modes:
             oracle.step_reference(st, np.ascontiguousarray(full[s:e]), lr=1e-2, betas=(0.9, 0.999), eps=1e-8, wd=0.0,
                                   max_norm=1.0)
-        assert opt.t == st.t == 2 and opt.n == e - s
+        assert opt.t == st.t == len(modes) and opt.n == e - s
         assert np.array_equal(opt.master.cpu().numpy(), st.p)
 
 
