@@ -124,6 +124,10 @@ def test_device_state_step_skips_and_matches_host_step():
     ("ragged_small", dict(steps=3)),
     ("llama13b_small", dict(steps=3)),
     ("llama_direct", dict(steps=3, direct=True)),
+    # the last of 8 micro-batches read in place (per-tensor grads, ZeRO-1 full-buffer norm)
+    ("gpt2_direct", dict(steps=3, direct=True)),
+    # a table of more than 1,024 tensors (AdamW searches it once per four parts), 2 micro-batches
+    ("ragged_long_direct", dict(steps=3, direct=True)),
 ])
 def test_graph_replayed_steps_match_oracle(name, kw):
     """Whole steps (all micro-batches' grad passes with the fused norm, finalize, prepare,
@@ -134,7 +138,10 @@ def test_graph_replayed_steps_match_oracle(name, kw):
           "ragged_small": W.small_ragged(n_tensors=800, world_size=4, rank=2),
           "llama13b_small": W.llama13b_zero3().with_(numels=tuple(W.llama_numels(2, 512, 1376, 3200))),
           "llama_direct": W.small_llama(layers=2, hidden=256, mlp=688, vocab=1000, world_size=3, rank=1,
-                                        max_norm=0.02)}[name]
+                                        max_norm=0.02),
+          "gpt2_direct": W.gpt2_zero1(),
+          "ragged_long_direct": W.small_ragged(n_tensors=1500, max_log2=13, world_size=4, rank=2,
+                                               micro_batches=2)}[name]
     rep = run_workload(wl, graph=True, **kw)
     assert len(rep.steps) == kw["steps"]
 
