@@ -9,19 +9,17 @@ namespace zs {
 ZS_DEBUG_UNIT(adamw_table)
 
 zero_status launch_adamw_table(float* p, float* m, float* v, const float* acc, const zero_tensor* table,
-                               int n_tensors, int grad_dtype, int64_t shard_start, float gscale, void* lowp,
-                               int lowp_dtype, int64_t n, const AdamScalars& s, const zero_adamw_device_state* ds,
-                               const zero_norm_result* clip, cudaStream_t st) {
+                               int n_tensors, int grad_dtype, int64_t shard_start, float gscale, const float* dscale,
+                               void* lowp, int lowp_dtype, int64_t n, const AdamScalars& s,
+                               const zero_adamw_device_state* ds, const zero_norm_result* clip, cudaStream_t st) {
   const bool four = table_four_parts(n_tensors);
-  if (acc != nullptr)
-    return (four ? launch_adamw_table_p4_acc : launch_adamw_table_acc)(p, m, v, acc, table, n_tensors, grad_dtype,
-                                                                       shard_start, gscale, lowp, lowp_dtype, n, s,
-                                                                       ds, clip, st);
-  if (four)
-    return launch_adamw_table_p4(p, m, v, nullptr, table, n_tensors, grad_dtype, shard_start, gscale, lowp, lowp_dtype,
-                                 n, s, ds, clip, st);
-  return launch_table_instance<false, 1>(p, m, v, nullptr, table, n_tensors, grad_dtype, shard_start, gscale, lowp,
-                                         lowp_dtype, n, s, ds, clip, st);
+  AdamwTableInstance* const other = (acc != nullptr) ? (four ? launch_adamw_table_p4_acc : launch_adamw_table_acc)
+                                    : (four ? launch_adamw_table_p4 : nullptr);
+  if (other != nullptr)
+    return other(p, m, v, acc, table, n_tensors, grad_dtype, shard_start, gscale, dscale, lowp, lowp_dtype, n, s, ds,
+                 clip, st);
+  return launch_table_instance<false, 1>(p, m, v, nullptr, table, n_tensors, grad_dtype, shard_start, gscale, dscale,
+                                         lowp, lowp_dtype, n, s, ds, clip, st);
 }
 
 }  // namespace zs

@@ -86,12 +86,13 @@ template <int DT, int LOWP, int LW, bool DEVS, bool ACC, int PARTS>
 __global__ void __launch_bounds__(256, (DT == ZERO_F32 && ACC) ? 2 : (DT == ZERO_F32 || ACC) ? 3 : 4)
     adamw_table_kernel(float* __restrict__ p, float* __restrict__ m, float* __restrict__ v,
                        const float* __restrict__ acc, const zero_tensor* __restrict__ table, int n_tensors,
-                       int64_t shard_start, int64_t n, float gscale, void* __restrict__ lowp, bool state_vec,
-                       AdamScalars hs, const zero_adamw_device_state* __restrict__ ds,
-                       const zero_norm_result* __restrict__ clip) {
+                       int64_t shard_start, int64_t n, float gscale, const float* __restrict__ dscale,
+                       void* __restrict__ lowp, bool state_vec, AdamScalars hs,
+                       const zero_adamw_device_state* __restrict__ ds, const zero_norm_result* __restrict__ clip) {
   __shared__ float stage[kAtBlock + kAtBlock / 8];
   AdamScalars s;
   if (!step_scalars<DEVS>(hs, ds, s)) return;  // the prepared step is skipped
+  if (dscale != nullptr) gscale = *dscale;  // a scale kept on the device (graph-captured mixed precision)
   float coef = 1.0f;
   if (clip != nullptr) {
     if (!clip->finite) return;  // non-finite grad norm: the step is skipped
@@ -194,71 +195,64 @@ __global__ void __launch_bounds__(256, (DT == ZERO_F32 && ACC) ? 2 : (DT == ZERO
   }
 }
 
+// The launch arguments shared by every level below.
+struct TableArgs {
+  float *p, *m, *v;
+  const float* acc;
+  const zero_tensor* table;
+  int n_tensors;
+  int64_t shard_start, n;
+  float gscale;
+  const float* dscale;
+  void* lowp;
+  const AdamScalars* s;
+  const zero_adamw_device_state* ds;
+  const zero_norm_result* clip;
+  cudaStream_t st;
+};
+
 template <int DT, int LOWP, int LW, bool ACC, int PARTS>
-static zero_status launch_table_t(float* p, float* m, float* v, const float* acc, const zero_tensor* table,
-                                  int n_tensors, int64_t shard_start, int64_t n, float gscale, void* lowp,
-                                  bool state_vec, const AdamScalars& s, const zero_adamw_device_state* ds,
-                                  const zero_norm_result* clip, cudaStream_t st) {
-  const unsigned grid = one_pass_blocks(n, static_cast<int64_t>(kAtBlock) * PARTS);
-  if (ds != nullptr)
-    adamw_table_kernel<DT, LOWP, LW, true, ACC, PARTS><<<grid, 256, 0, st>>>(
-        p, m, v, acc, table, n_tensors, shard_start, n, gscale, lowp, state_vec, s, ds, clip);
+static zero_status launch_table_t(const TableArgs& a, bool state_vec) {
+  const unsigned grid = one_pass_blocks(a.n, static_cast<int64_t>(kAtBlock) * PARTS);
+  if (a.ds != nullptr)
+    adamw_table_kernel<DT, LOWP, LW, true, ACC, PARTS><<<grid, 256, 0, a.st>>>(
+        a.p, a.m, a.v, a.acc, a.table, a.n_tensors, a.shard_start, a.n, a.gscale, a.dscale, a.lowp, state_vec, *a.s,
+        a.ds, a.clip);
   else
-    adamw_table_kernel<DT, LOWP, LW, false, ACC, PARTS><<<grid, 256, 0, st>>>(
-        p, m, v, acc, table, n_tensors, shard_start, n, gscale, lowp, state_vec, s, nullptr, clip);
+    adamw_table_kernel<DT, LOWP, LW, false, ACC, PARTS><<<grid, 256, 0, a.st>>>(
+        a.p, a.m, a.v, a.acc, a.table, a.n_tensors, a.shard_start, a.n, a.gscale, a.dscale, a.lowp, state_vec, *a.s,
+        nullptr, a.clip);
   return check_launch("adamw_table_kernel");
 }
 
 template <int DT, int LOWP, bool ACC, int PARTS>
-static zero_status launch_table_lw(float* p, float* m, float* v, const float* acc, const zero_tensor* table,
-                                   int n_tensors, int64_t shard_start, int64_t n, float gscale, void* lowp,
-                                   const AdamScalars& s, const zero_adamw_device_state* ds,
-                                   const zero_norm_result* clip, cudaStream_t st) {
-  const bool sv = aligned(p, 32) && aligned(m, 32) && aligned(v, 32) && (!ACC || aligned(acc, 32));
-  const uintptr_t la = reinterpret_cast<uintptr_t>(lowp) % 16;
-  if (LOWP == 0 || la == 0)
-    return launch_table_t<DT, LOWP, 16, ACC, PARTS>(p, m, v, acc, table, n_tensors, shard_start, n, gscale, lowp, sv,
-                                                    s, ds, clip, st);
-  if (la % 8 == 0)
-    return launch_table_t<DT, LOWP, 8, ACC, PARTS>(p, m, v, acc, table, n_tensors, shard_start, n, gscale, lowp, sv,
-                                                   s, ds, clip, st);
-  if (la % 4 == 0)
-    return launch_table_t<DT, LOWP, 4, ACC, PARTS>(p, m, v, acc, table, n_tensors, shard_start, n, gscale, lowp, sv,
-                                                   s, ds, clip, st);
-  return launch_table_t<DT, LOWP, 2, ACC, PARTS>(p, m, v, acc, table, n_tensors, shard_start, n, gscale, lowp, sv, s,
-                                                 ds, clip, st);
+static zero_status launch_table_lw(const TableArgs& a) {
+  const bool sv = aligned(a.p, 32) && aligned(a.m, 32) && aligned(a.v, 32) && (!ACC || aligned(a.acc, 32));
+  const uintptr_t la = reinterpret_cast<uintptr_t>(a.lowp) % 16;
+  if (LOWP == 0 || la == 0) return launch_table_t<DT, LOWP, 16, ACC, PARTS>(a, sv);
+  if (la % 8 == 0) return launch_table_t<DT, LOWP, 8, ACC, PARTS>(a, sv);
+  if (la % 4 == 0) return launch_table_t<DT, LOWP, 4, ACC, PARTS>(a, sv);
+  return launch_table_t<DT, LOWP, 2, ACC, PARTS>(a, sv);
 }
 
 template <int DT, bool ACC, int PARTS>
-static zero_status launch_table_dt(float* p, float* m, float* v, const float* acc, const zero_tensor* table,
-                                   int n_tensors, int64_t shard_start, int64_t n, float gscale, void* lowp,
-                                   int lowp_dtype, const AdamScalars& s, const zero_adamw_device_state* ds,
-                                   const zero_norm_result* clip, cudaStream_t st) {
-  if (lowp == nullptr)
-    return launch_table_lw<DT, 0, ACC, PARTS>(p, m, v, acc, table, n_tensors, shard_start, n, gscale, nullptr, s, ds,
-                                              clip, st);
-  if (lowp_dtype == ZERO_BF16)
-    return launch_table_lw<DT, ZERO_BF16, ACC, PARTS>(p, m, v, acc, table, n_tensors, shard_start, n, gscale, lowp, s,
-                                                      ds, clip, st);
-  return launch_table_lw<DT, ZERO_F16, ACC, PARTS>(p, m, v, acc, table, n_tensors, shard_start, n, gscale, lowp, s,
-                                                   ds, clip, st);
+static zero_status launch_table_dt(const TableArgs& a, int lowp_dtype) {
+  if (a.lowp == nullptr) return launch_table_lw<DT, 0, ACC, PARTS>(a);
+  if (lowp_dtype == ZERO_BF16) return launch_table_lw<DT, ZERO_BF16, ACC, PARTS>(a);
+  return launch_table_lw<DT, ZERO_F16, ACC, PARTS>(a);
 }
 
 // Every grad dtype of one (ACC, PARTS) instance.
 template <bool ACC, int PARTS>
 static zero_status launch_table_instance(float* p, float* m, float* v, const float* acc, const zero_tensor* table,
-                                         int n_tensors, int grad_dtype, int64_t shard_start, float gscale, void* lowp,
-                                         int lowp_dtype, int64_t n, const AdamScalars& s,
-                                         const zero_adamw_device_state* ds, const zero_norm_result* clip,
-                                         cudaStream_t st) {
-  if (grad_dtype == ZERO_F32)
-    return launch_table_dt<ZERO_F32, ACC, PARTS>(p, m, v, acc, table, n_tensors, shard_start, n, gscale, lowp,
-                                                 lowp_dtype, s, ds, clip, st);
-  if (grad_dtype == ZERO_BF16)
-    return launch_table_dt<ZERO_BF16, ACC, PARTS>(p, m, v, acc, table, n_tensors, shard_start, n, gscale, lowp,
-                                                  lowp_dtype, s, ds, clip, st);
-  return launch_table_dt<ZERO_F16, ACC, PARTS>(p, m, v, acc, table, n_tensors, shard_start, n, gscale, lowp,
-                                               lowp_dtype, s, ds, clip, st);
+                                         int n_tensors, int grad_dtype, int64_t shard_start, float gscale,
+                                         const float* dscale, void* lowp, int lowp_dtype, int64_t n,
+                                         const AdamScalars& s, const zero_adamw_device_state* ds,
+                                         const zero_norm_result* clip, cudaStream_t st) {
+  const TableArgs a{p, m, v, acc, table, n_tensors, shard_start, n, gscale, dscale, lowp, &s, ds, clip, st};
+  if (grad_dtype == ZERO_F32) return launch_table_dt<ZERO_F32, ACC, PARTS>(a, lowp_dtype);
+  if (grad_dtype == ZERO_BF16) return launch_table_dt<ZERO_BF16, ACC, PARTS>(a, lowp_dtype);
+  return launch_table_dt<ZERO_F16, ACC, PARTS>(a, lowp_dtype);
 }
 
 }  // namespace zs

@@ -9,11 +9,11 @@ namespace zs {
 ZS_DEBUG_UNIT(adamw_table_p4)
 
 zero_status launch_adamw_table_p4(float* p, float* m, float* v, const float* acc, const zero_tensor* table,
-                                  int n_tensors, int grad_dtype, int64_t shard_start, float gscale, void* lowp,
-                                  int lowp_dtype, int64_t n, const AdamScalars& s, const zero_adamw_device_state* ds,
-                                  const zero_norm_result* clip, cudaStream_t st) {
-  return launch_table_instance<false, 4>(p, m, v, acc, table, n_tensors, grad_dtype, shard_start, gscale, lowp,
-                                        lowp_dtype, n, s, ds, clip, st);
+                                  int n_tensors, int grad_dtype, int64_t shard_start, float gscale,
+                                  const float* dscale, void* lowp, int lowp_dtype, int64_t n, const AdamScalars& s,
+                                  const zero_adamw_device_state* ds, const zero_norm_result* clip, cudaStream_t st) {
+  return launch_table_instance<false, 4>(p, m, v, acc, table, n_tensors, grad_dtype, shard_start, gscale, dscale,
+                                         lowp, lowp_dtype, n, s, ds, clip, st);
 }
 
 }  // namespace zs

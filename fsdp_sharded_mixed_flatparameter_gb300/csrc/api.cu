@@ -291,9 +291,9 @@ zero_status zero_adamw_step(float* d_master, float* d_exp_avg, float* d_exp_avg_
 zero_status zero_adamw_step_tensors(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
                                     const zero_tensor* d_table, int32_t n_tensors, int64_t total,
                                     zero_dtype grad_dtype, int64_t shard_start, float grad_scale,
-                                    const float* d_acc, void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
-                                    const zero_adamw_hparams* hp, int64_t step, const zero_norm_result* d_clip,
-                                    void* stream) {
+                                    const float* d_grad_scale, const float* d_acc, void* d_param_lowp,
+                                    zero_dtype lowp_dtype, int64_t n, const zero_adamw_hparams* hp, int64_t step,
+                                    const zero_norm_result* d_clip, void* stream) {
   const char* who = "zero_adamw_step_tensors";
   if (n < 0) return fail(ZERO_EINVAL, "%s: n %lld < 0", who, (long long)n);
   zs::AdamScalars s;
@@ -312,8 +312,8 @@ zero_status zero_adamw_step_tensors(float* d_master, float* d_exp_avg, float* d_
     return fail(ZERO_EINVAL, "%s: lowp_dtype must be BF16 or F16", who);
   if (n == 0) return ZERO_OK;
   return zs::launch_adamw_table(d_master, d_exp_avg, d_exp_avg_sq, d_acc, d_table, n_tensors, grad_dtype,
-                                shard_start, grad_scale, d_param_lowp, lowp_dtype, n, s, nullptr, d_clip,
-                                zs::as_stream(stream));
+                                shard_start, grad_scale, d_grad_scale, d_param_lowp, lowp_dtype, n, s, nullptr,
+                                d_clip, zs::as_stream(stream));
 }
 
 // ------------------------------------------------------------- debug builds
@@ -394,9 +394,9 @@ zero_status zero_adamw_step_device(float* d_master, float* d_exp_avg, float* d_e
 zero_status zero_adamw_step_tensors_device(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
                                            const zero_tensor* d_table, int32_t n_tensors, int64_t total,
                                            zero_dtype grad_dtype, int64_t shard_start, float grad_scale,
-                                           const float* d_acc, void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
-                                           const zero_adamw_device_state* d_state, const zero_norm_result* d_clip,
-                                           void* stream) {
+                                           const float* d_grad_scale, const float* d_acc, void* d_param_lowp,
+                                           zero_dtype lowp_dtype, int64_t n, const zero_adamw_device_state* d_state,
+                                           const zero_norm_result* d_clip, void* stream) {
   const char* who = "zero_adamw_step_tensors_device";
   if (n < 0) return fail(ZERO_EINVAL, "%s: n %lld < 0", who, (long long)n);
   const zero_status c = check_state(who, d_state);
@@ -414,8 +414,8 @@ zero_status zero_adamw_step_tensors_device(float* d_master, float* d_exp_avg, fl
     return fail(ZERO_EINVAL, "%s: lowp_dtype must be BF16 or F16", who);
   if (n == 0) return ZERO_OK;
   return zs::launch_adamw_table(d_master, d_exp_avg, d_exp_avg_sq, d_acc, d_table, n_tensors, grad_dtype,
-                                shard_start, grad_scale, d_param_lowp, lowp_dtype, n, zs::AdamScalars{}, d_state,
-                                d_clip, zs::as_stream(stream));
+                                shard_start, grad_scale, d_grad_scale, d_param_lowp, lowp_dtype, n,
+                                zs::AdamScalars{}, d_state, d_clip, zs::as_stream(stream));
 }
 
 }  // extern "C"

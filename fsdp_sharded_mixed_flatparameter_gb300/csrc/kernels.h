@@ -33,17 +33,18 @@ zero_status launch_adamw(float* p, float* m, float* v, const float* g, void* low
 // AdamW with the grad read through the tensor table (grad_scale * x at flat
 // index shard_start + k) instead of a materialized fp32 grad; `acc`
 // (nullable): the earlier micro-batches' fp32 sum, added first.
+// `dscale` (nullable): read the grad scale from device memory when the kernel runs.
 zero_status launch_adamw_table(float* p, float* m, float* v, const float* acc, const zero_tensor* table,
-                               int n_tensors, int grad_dtype, int64_t shard_start, float gscale, void* lowp,
-                               int lowp_dtype, int64_t n, const AdamScalars& s, const zero_adamw_device_state* ds,
-                               const zero_norm_result* clip, cudaStream_t st);
+                               int n_tensors, int grad_dtype, int64_t shard_start, float gscale, const float* dscale,
+                               void* lowp, int lowp_dtype, int64_t n, const AdamScalars& s,
+                               const zero_adamw_device_state* ds, const zero_norm_result* clip, cudaStream_t st);
 // Its other instances, each in a translation unit of its own (compiled in
 // parallel): acc != NULL; one table search per four parts (long tables); both.
 using AdamwTableInstance = zero_status(float* p, float* m, float* v, const float* acc, const zero_tensor* table,
-                                       int n_tensors, int grad_dtype, int64_t shard_start, float gscale, void* lowp,
-                                       int lowp_dtype, int64_t n, const AdamScalars& s,
-                                       const zero_adamw_device_state* ds, const zero_norm_result* clip,
-                                       cudaStream_t st);
+                                       int n_tensors, int grad_dtype, int64_t shard_start, float gscale,
+                                       const float* dscale, void* lowp, int lowp_dtype, int64_t n,
+                                       const AdamScalars& s, const zero_adamw_device_state* ds,
+                                       const zero_norm_result* clip, cudaStream_t st);
 AdamwTableInstance launch_adamw_table_acc;
 AdamwTableInstance launch_adamw_table_p4;
 AdamwTableInstance launch_adamw_table_p4_acc;

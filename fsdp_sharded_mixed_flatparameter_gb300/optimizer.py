@@ -328,7 +328,8 @@ class FlatShardAdamW:
         return self.finish_step(stream)
 
     def step_tensors(self, grads: Optional[Sequence[Optional[torch.Tensor]]] = None, *, scale: float = 1.0,
-                     stream=None, process_group=None, accumulated: bool = False) -> zs.NormResult:
+                     stream=None, process_group=None, accumulated: bool = False,
+                     loss_scale=None) -> zs.NormResult:
         """One step straight from per-tensor grads: a norm pass reads the grads through
         the FlatParameter table without writing them, then AdamW reads them again
         through the table.  No fp32 flat grad is written (30 instead of 36 bytes per
@@ -341,38 +342,39 @@ class FlatShardAdamW:
         of 10 + 30 bytes per parameter); bit-identical to flatten(accumulate=True,
         scale) + step().
 
-        The grad scale is a host value here (a DeviceLossScale needs the materialized
-        path: flatten/accum + step)."""
+        loss_scale: a DeviceLossScale, as for flatten(): both passes read its unscale
+        factor on the device and the norm pass raises its overflow flag; `scale` is
+        ignored."""
         self.launch_step_tensors(grads, scale=scale, stream=stream, process_group=process_group,
-                                 accumulated=accumulated)
+                                 accumulated=accumulated, loss_scale=loss_scale)
         return self.finish_step(stream)
 
     def launch_step_tensors(self, grads: Optional[Sequence[Optional[torch.Tensor]]] = None, *, scale: float = 1.0,
-                            stream=None, process_group=None, accumulated: bool = False) -> None:
+                            stream=None, process_group=None, accumulated: bool = False, loss_scale=None) -> None:
         """Enqueue step_tensors() without waiting (capturable with registered grads)."""
         table, count, dt = self._resolve(grads)
         self._launch_direct(table, count, self.total, dt, self.glo, self.ghi, self.start, scale, accumulated, stream,
-                            process_group)
+                            process_group, loss_scale)
 
     def step_flat(self, flat_src: torch.Tensor, *, scale: float = 1.0, stream=None, process_group=None,
-                  accumulated: bool = False) -> zs.NormResult:
+                  accumulated: bool = False, loss_scale=None) -> zs.NormResult:
         """step_tensors() for a flat low-precision grad covering the grad range (what
         accum() takes: ZeRO-2/3 and FSDP, where the rank receives its shard's grads
         already flat): the last micro-batch is read by the norm pass and by AdamW and
         never written.  Bit-identical to accum(flat_src, accumulate=accumulated,
         scale) + step()."""
         self.launch_step_flat(flat_src, scale=scale, stream=stream, process_group=process_group,
-                              accumulated=accumulated)
+                              accumulated=accumulated, loss_scale=loss_scale)
         return self.finish_step(stream)
 
     def launch_step_flat(self, flat_src: torch.Tensor, *, scale: float = 1.0, stream=None, process_group=None,
-                         accumulated: bool = False) -> None:
+                         accumulated: bool = False, loss_scale=None) -> None:
         """Enqueue step_flat() without waiting (capturable once device_flat_table(flat_src)
         has been called outside the capture)."""
         table = self.device_flat_table(flat_src)
         span = self.ghi - self.glo
         self._launch_direct(table, 1, span, flat_src.dtype, 0, span, self.start - self.glo, scale, accumulated, stream,
-                            process_group)
+                            process_group, loss_scale)
 
     def device_flat_table(self, flat_src: torch.Tensor) -> torch.Tensor:
         """The one-entry tensor table of a flat grad over the grad range, in device memory
@@ -392,17 +394,17 @@ class FlatShardAdamW:
         return hit
 
     def _launch_direct(self, table, count: int, total: int, dt, lo: int, hi: int, shard_start: int, scale: float,
-                       accumulated: bool, stream, process_group) -> None:
+                       accumulated: bool, stream, process_group, loss_scale=None) -> None:
         """The direct path over a tensor table: flat indices [lo, hi) are the grad range,
         [shard_start, shard_start + n) the shard."""
         if accumulated and self.grad.numel() != self.ghi - self.glo:
             raise ValueError("accumulated=True needs the grad buffer (grad_buffer=True)")
+        sc, dsc, flag = self._scale_args(scale, loss_scale)
         if accumulated:
-            zs.zero_flatten_cast(table, count, total, dt, lo, hi, scale, zs.NORM_OF_SUM, self.grad,
-                                 self.found_nonfinite, self.ws, stream)
+            zs.zero_flatten_cast(table, count, total, dt, lo, hi, sc, zs.NORM_OF_SUM, self.grad, flag, self.ws, stream,
+                                 d_scale=dsc)
         else:
-            zs.zero_flatten_cast(table, count, total, dt, lo, hi, scale, False, None, self.found_nonfinite, self.ws,
-                                 stream)
+            zs.zero_flatten_cast(table, count, total, dt, lo, hi, sc, False, None, flag, self.ws, stream, d_scale=dsc)
         if process_group is not None and self.glo == self.start and _world(process_group) > 1:
             if self._local_buf is None:
                 self._local_buf = zs.new_norm_result(self.device)
@@ -417,12 +419,13 @@ class FlatShardAdamW:
         if self.capturable:
             zs.zero_adamw_prepare_device(self._dev_hp, self.norm_buf, self._dev_state, stream)
             zs.zero_adamw_step_tensors_device(self.master, self.exp_avg, self.exp_avg_sq, table, count, total,
-                                              dt, shard_start, scale, self.lowp, self._dev_state, self.norm_buf,
-                                              stream, acc=acc)
+                                              dt, shard_start, sc, self.lowp, self._dev_state, self.norm_buf,
+                                              stream, acc=acc, d_scale=dsc)
         else:
             zs.zero_adamw_step_tensors(self.master, self.exp_avg, self.exp_avg_sq, table, count, total, dt,
-                                       shard_start, scale, self.lowp, self.lr, self.betas[0], self.betas[1],
-                                       self.eps, self.weight_decay, self._t + 1, self.norm_buf, stream, acc=acc)
+                                       shard_start, sc, self.lowp, self.lr, self.betas[0], self.betas[1],
+                                       self.eps, self.weight_decay, self._t + 1, self.norm_buf, stream, acc=acc,
+                                       d_scale=dsc)
 
     # -------------------------------------------------------- checkpoint
     def state_dict(self) -> dict:

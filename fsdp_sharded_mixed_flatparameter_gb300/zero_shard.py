@@ -96,8 +96,8 @@ def lib() -> ctypes.CDLL:
     L.zero_grad_sqnorm_noalloc.argtypes = [vp, i64, f64, f64, vp, vp]
     L.zero_adamw_step.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, i64, ctypes.POINTER(zero_adamw_hparams), i64,
                                   vp, vp]
-    L.zero_adamw_step_tensors.argtypes = [vp, vp, vp, vp, i32, i64, ctypes.c_int, i64, f32, vp, vp, ctypes.c_int,
-                                          i64, ctypes.POINTER(zero_adamw_hparams), i64, vp, vp]
+    L.zero_adamw_step_tensors.argtypes = [vp, vp, vp, vp, i32, i64, ctypes.c_int, i64, f32, vp, vp, vp,
+                                          ctypes.c_int, i64, ctypes.POINTER(zero_adamw_hparams), i64, vp, vp]
     L.zero_loss_scale_update.argtypes = [ctypes.POINTER(f32), ctypes.POINTER(i32), i32, f64, f64, i32]
     L.zero_loss_scale_update_device.argtypes = [vp, i32, f64, f64, i32, vp, vp]
     L.zero_adamw_scalars.argtypes = [ctypes.POINTER(zero_adamw_hparams), i64, vp]
@@ -105,7 +105,7 @@ def lib() -> ctypes.CDLL:
     L.zero_debug_selftest.argtypes = [i64, vp]
     L.zero_adamw_prepare_device.argtypes = [vp, vp, vp, vp]
     L.zero_adamw_step_device.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, i64, vp, vp, vp]
-    L.zero_adamw_step_tensors_device.argtypes = [vp, vp, vp, vp, i32, i64, ctypes.c_int, i64, f32, vp, vp,
+    L.zero_adamw_step_tensors_device.argtypes = [vp, vp, vp, vp, i32, i64, ctypes.c_int, i64, f32, vp, vp, vp,
                                                  ctypes.c_int, i64, vp, vp, vp]
     L.zero_status_string.argtypes = [ctypes.c_int]
     L.zero_status_string.restype = ctypes.c_char_p
@@ -352,9 +352,11 @@ def zero_adamw_step_tensors(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg
                             d_table: torch.Tensor, n_tensors: int, total: int, grad_dtype: torch.dtype,
                             shard_start: int, grad_scale: float, param_lowp: Optional[torch.Tensor], lr: float,
                             beta1: float, beta2: float, eps: float, weight_decay: float, step: int,
-                            clip: Optional[torch.Tensor] = None, stream=None, acc: Optional[torch.Tensor] = None) -> None:
+                            clip: Optional[torch.Tensor] = None, stream=None, acc: Optional[torch.Tensor] = None,
+                            d_scale: Optional[torch.Tensor] = None) -> None:
     """AdamW over [shard_start, shard_start + n) with the grads read through the tensor table;
-    acc: the earlier micro-batches' fp32 sum over the same n elements, added first (or None)."""
+    acc: the earlier micro-batches' fp32 sum over the same n elements, added first (or None);
+    d_scale: a device float used in place of grad_scale (or None)."""
     n = master.numel()
     for t, nm in ((exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq")):
         if t.numel() != n:
@@ -373,7 +375,7 @@ def zero_adamw_step_tensors(master: torch.Tensor, exp_avg: torch.Tensor, exp_avg
     _check(lib().zero_adamw_step_tensors(_dev(master, "master", torch.float32), _dev(exp_avg, "exp_avg", torch.float32),
                                          _dev(exp_avg_sq, "exp_avg_sq", torch.float32),
                                          _dev(d_table, "d_table", torch.uint8, allow_none=n_tensors == 0), n_tensors,
-                                         total, _DT[grad_dtype], shard_start, grad_scale,
+                                         total, _DT[grad_dtype], shard_start, grad_scale, _dscale(d_scale),
                                          _dev(acc, "acc", torch.float32, allow_none=True),
                                          _dev(param_lowp, "param_lowp", allow_none=True), lowp_dt, n, ctypes.byref(hp),
                                          step, _dev(clip, "clip", allow_none=True), _stream(stream)))
@@ -465,7 +467,7 @@ def zero_adamw_step_tensors_device(master: torch.Tensor, exp_avg: torch.Tensor, 
                                    d_table: torch.Tensor, n_tensors: int, total: int, grad_dtype: torch.dtype,
                                    shard_start: int, grad_scale: float, param_lowp: Optional[torch.Tensor],
                                    state: torch.Tensor, clip: Optional[torch.Tensor] = None, stream=None,
-                                   acc: Optional[torch.Tensor] = None) -> None:
+                                   acc: Optional[torch.Tensor] = None, d_scale: Optional[torch.Tensor] = None) -> None:
     """zero_adamw_step_tensors with the scalars and skip decision of the device step state."""
     n = master.numel()
     for t, nm in ((exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq")):
@@ -480,8 +482,8 @@ def zero_adamw_step_tensors_device(master: torch.Tensor, exp_avg: torch.Tensor, 
     _check(lib().zero_adamw_step_tensors_device(
         _dev(master, "master", torch.float32), _dev(exp_avg, "exp_avg", torch.float32),
         _dev(exp_avg_sq, "exp_avg_sq", torch.float32), _dev(d_table, "d_table", torch.uint8, allow_none=n_tensors == 0),
-        n_tensors, total, _DT[grad_dtype], shard_start, grad_scale, _dev(acc, "acc", torch.float32, allow_none=True),
-        lp, lowp_dt, n, _state_arg(state),
+        n_tensors, total, _DT[grad_dtype], shard_start, grad_scale, _dscale(d_scale),
+        _dev(acc, "acc", torch.float32, allow_none=True), lp, lowp_dt, n, _state_arg(state),
         _dev(clip, "clip", allow_none=True), _stream(stream)))
 
 

@@ -404,6 +404,9 @@ zero_status zero_loss_scale_update_device(zero_loss_scale_state* d_state, int32_
  * (norm pass with d_dst = NULL, then this) and never writes the 4-byte fp32
  * grad, 30 instead of 36 bytes per parameter, and the fp32 grad buffer
  * (4 bytes/param of HBM) is not needed at all.
+ * d_grad_scale: NULL, or a device float read when the kernel runs and used
+ *   in place of grad_scale (the unscale factor of a loss scale kept on the
+ *   device, as d_scale of zero_flatten_cast; grad_scale must still be finite).
  * d_acc: NULL, or the fp32 sum of the step's earlier micro-batches (n
  *   elements, element k at flat index shard_start + k, as zero_flatten_cast
  *   or zero_accum left it): the grad is then fl(d_acc[k] + fl(grad_scale *
@@ -420,7 +423,8 @@ zero_status zero_loss_scale_update_device(zero_loss_scale_state* d_state, int32_
 zero_status zero_adamw_step_tensors(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
                                     const zero_tensor* d_table, int32_t n_tensors, int64_t total,
                                     zero_dtype grad_dtype, int64_t shard_start, float grad_scale,
-                                    const float* d_acc, void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
+                                    const float* d_grad_scale, const float* d_acc, void* d_param_lowp,
+                                    zero_dtype lowp_dtype, int64_t n,
                                     const zero_adamw_hparams* hp, int64_t step,
                                     const zero_norm_result* d_clip, void* stream);
 
@@ -487,7 +491,8 @@ zero_status zero_adamw_step_device(float* d_master, float* d_exp_avg, float* d_e
 zero_status zero_adamw_step_tensors_device(float* d_master, float* d_exp_avg, float* d_exp_avg_sq,
                                            const zero_tensor* d_table, int32_t n_tensors, int64_t total,
                                            zero_dtype grad_dtype, int64_t shard_start, float grad_scale,
-                                           const float* d_acc, void* d_param_lowp, zero_dtype lowp_dtype, int64_t n,
+                                           const float* d_grad_scale, const float* d_acc, void* d_param_lowp,
+                                           zero_dtype lowp_dtype, int64_t n,
                                            const zero_adamw_device_state* d_state,
                                            const zero_norm_result* d_clip, void* stream);
 

@@ -142,17 +142,17 @@ def test_invalid_arguments_return_einval_before_any_launch(L):
         cases.append(L.zero_adamw_step(FAKE, FAKE, FAKE, FAKE, None, 1, 10, ctypes.byref(bad), 1, None, None))
     # AdamW through the tensor table (d_acc is nullable and never the reason for a refusal)
     cases += [
-        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, None, 2, 10, 1, 0, 1.0, FAKE, None, 1, 5, ctypes.byref(hp), 1,
+        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, None, 2, 10, 1, 0, 1.0, None, FAKE, None, 1, 5, ctypes.byref(hp), 1,
                                   None, None),                                                   # NULL table
-        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 6, 1.0, FAKE, None, 1, 5, ctypes.byref(hp), 1,
+        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 6, 1.0, None, FAKE, None, 1, 5, ctypes.byref(hp), 1,
                                   None, None),                                                   # past total
-        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, FAKE, 2, 10, 9, 0, 1.0, FAKE, None, 1, 5, ctypes.byref(hp), 1,
+        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, FAKE, 2, 10, 9, 0, 1.0, None, FAKE, None, 1, 5, ctypes.byref(hp), 1,
                                   None, None),                                                   # bad grad dtype
-        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 0, math.inf, FAKE, None, 1, 5, ctypes.byref(hp),
-                                  1, None, None),                                                # inf grad_scale
-        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 0, 1.0, FAKE, None, 1, 5, ctypes.byref(hp), 0,
+        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 0, math.inf, None, FAKE, None, 1, 5,
+                                  ctypes.byref(hp), 1, None, None),                              # inf grad_scale
+        L.zero_adamw_step_tensors(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 0, 1.0, None, FAKE, None, 1, 5, ctypes.byref(hp), 0,
                                   None, None),                                                   # step 0
-        L.zero_adamw_step_tensors(FAKE, None, FAKE, FAKE, 2, 10, 1, 0, 1.0, FAKE, None, 1, 5, ctypes.byref(hp), 1,
+        L.zero_adamw_step_tensors(FAKE, None, FAKE, FAKE, 2, 10, 1, 0, 1.0, None, FAKE, None, 1, 5, ctypes.byref(hp), 1,
                                   None, None),                                                   # NULL m
     ]
     # graph-capturable calls (device step state)
@@ -164,11 +164,11 @@ def test_invalid_arguments_return_einval_before_any_launch(L):
         L.zero_adamw_step_device(FAKE, FAKE, FAKE, None, None, 1, 10, FAKE, None, None),       # NULL grad
         L.zero_adamw_step_device(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 10, FAKE, None, None),       # F32 lowp
         L.zero_adamw_step_device(FAKE, FAKE, FAKE, FAKE, None, 1, -1, FAKE, None, None),       # n < 0
-        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, None, 2, 10, 1, 0, 1.0, None, None, 1, 5, FAKE, None,
+        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, None, 2, 10, 1, 0, 1.0, None, None, None, 1, 5, FAKE, None,
                                          None),                                                  # NULL table
-        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 6, 1.0, FAKE, None, 1, 5, FAKE, None,
+        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 6, 1.0, None, FAKE, None, 1, 5, FAKE, None,
                                          None),                                                  # past total
-        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 0, 1.0, FAKE, None, 1, 5, None, None,
+        L.zero_adamw_step_tensors_device(FAKE, FAKE, FAKE, FAKE, 2, 10, 1, 0, 1.0, None, FAKE, None, 1, 5, None, None,
                                          None),                                                  # NULL state
         L.zero_loss_scale_update_device(None, 1, 2.0, 0.5, 10, None, None),                     # NULL state
         L.zero_loss_scale_update_device(FAKE, 0, 2.0, 0.5, 10, None, None),                     # accum_steps 0
@@ -188,8 +188,8 @@ def test_empty_calls_are_noops_without_a_gpu(L):
     hp = zero_adamw_hparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
     assert L.zero_flatten_cast(None, 0, 0, 1, 0, 0, 1.0, None, 0, None, None, None, 0, None) == 0
     assert L.zero_flatten_cast(None, 0, 0, 1, 0, 0, 1.0, None, 2, None, None, None, 0, None) == 0  # norm of the sum
-    assert L.zero_adamw_step_tensors(None, None, None, None, 0, 0, 1, 0, 1.0, None, None, 1, 0, ctypes.byref(hp), 1,
-                                     None, None) == 0
+    assert L.zero_adamw_step_tensors(None, None, None, None, 0, 0, 1, 0, 1.0, None, None, None, 1, 0,
+                                     ctypes.byref(hp), 1, None, None) == 0
     assert L.zero_accum(None, None, 1, 0, 1.0, None, 0, None, None, 0, None) == 0
     assert L.zero_adamw_step(None, None, None, None, None, 1, 0, ctypes.byref(hp), 1, None, None) == 0
 

@@ -71,13 +71,18 @@ def test_loss_scaled_fp16_accumulation_with_overflow_skip():
     assert scaler.scale == 2.0 ** 16 * 2 * 0.5 * 2 * 2
 
 
-def test_graph_captured_loss_scaled_steps_with_device_scale():
+@pytest.mark.parametrize("direct,inf_micro", [(False, 2), (True, 2), (True, 3)],
+                         ids=["materialized", "direct", "direct-overflow-in-last"])
+def test_graph_captured_loss_scaled_steps_with_device_scale(direct, inf_micro):
     """The same loss-scaled fp16 accumulation, captured once in a CUDA graph with the loss
     scale on the device (DeviceLossScale): the accumulate passes read the unscale factor
     from device memory, the overflow flag and the non-finite norm drive the device-side
     update, the step count and skip decision stay on the device.  Replayed for 7 steps
     (an overflow at step 3) and checked after every step against the oracle: the state bit
-    for bit, the step count, and the scale trajectory of the GradScaler policy."""
+    for bit, the step count, and the scale trajectory of the GradScaler policy.  direct:
+    the last micro-batch is read in place (step_flat, accumulated) by the norm pass and
+    AdamW, both reading the unscale factor on the device; the overflow lands in an earlier
+    micro-batch or in that last one."""
     from fsdp_sharded_mixed_flatparameter_gb300 import DeviceLossScale, FlatShardAdamW
     wl = W.llama13b_zero3().with_(numels=tuple(W.llama_numels(2, 256, 688, 1000)), max_norm=0.05)
     s, e = oracle.shard_range(wl.total, wl.world_size, wl.rank)
@@ -90,10 +95,17 @@ def test_graph_captured_loss_scaled_steps_with_device_scale():
     micro = [torch.zeros(n, dtype=torch.float16, device=DEV) for _ in range(M)]
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
+    if direct:
+        opt.device_flat_table(micro[-1])  # built before the capture
     with torch.cuda.graph(graph):
-        for j in range(M):
-            opt.accum(micro[j], accumulate=j > 0, fuse_norm=j == M - 1, loss_scale=scaler)
-        opt.launch_step()
+        if direct:
+            for j in range(M - 1):
+                opt.accum(micro[j], accumulate=j > 0, loss_scale=scaler)
+            opt.launch_step_flat(micro[-1], accumulated=True, loss_scale=scaler)
+        else:
+            for j in range(M):
+                opt.accum(micro[j], accumulate=j > 0, fuse_norm=j == M - 1, loss_scale=scaler)
+            opt.launch_step()
         scaler.launch_update(opt.norm_buf)
     st = oracle.new_state(master.numpy())
     found_hist = []
@@ -107,7 +119,7 @@ def test_graph_captured_loss_scaled_steps_with_device_scale():
         for j in range(M):
             g = W.flat_grads(wl.with_(grad_dtype="f32", grad_std=1e-5), t, j, s, e)
             x = (g * S).to(torch.float16)
-            if t == 3 and j == 2:
+            if t == 3 and j == inf_micro:
                 x[n // 3] = math.inf
             micro[j].copy_(x.to(DEV))
             ref_flag |= oracle.accum(acc, raw(x), "f16", unscale, accumulate=j > 0)
@@ -129,8 +141,9 @@ def test_graph_captured_loss_scaled_steps_with_device_scale():
 
 def test_device_scale_matches_host_scale_in_every_grad_pass():
     """A scale read from device memory (d_scale) gives the bits of the same scale passed from
-    the host, in the flatten (writing and norm-only), the accumulation and the reduction,
-    with their fused norm partials and the non-finite flag."""
+    the host, in the flatten (writing, norm-only and norm of the accumulated sum), the
+    accumulation, the reduction and AdamW through the table (with and without the sum), with
+    their fused norm partials and the non-finite flag."""
     from fsdp_sharded_mixed_flatparameter_gb300 import zero_shard as zs
     from test_gpu_kernels import _table_case
     numels = list(W.llama_numels(1, 256, 688, 1000)) + list(W.ragged_numels(50, seed=2, max_log2=12))
@@ -158,8 +171,19 @@ def test_device_scale_matches_host_scale_in_every_grad_pass():
             red = torch.zeros(total, device=DEV)
             ws4 = torch.zeros(nb, dtype=torch.uint8, device=DEV)
             zs.zero_reduce_chunks(red, torch.stack([src, src.flip(0)]), total, hs, False, flag, ws4, d_scale=d_scale)
+            # the direct path: the norm of the accumulated sum, and AdamW through the table with the sum
+            ws5 = torch.zeros(nb, dtype=torch.uint8, device=DEV)
+            zs.zero_flatten_cast(d_table, len(numels), total, torch.float16, 0, total, hs, zs.NORM_OF_SUM, acc, flag,
+                                 ws5, d_scale=d_scale)
+            state = [torch.linspace(-0.1, 0.1, total, device=DEV), torch.zeros(total, device=DEV),
+                     torch.zeros(total, device=DEV)]
+            lowp = torch.empty(total, dtype=torch.bfloat16, device=DEV)
+            for t in (1, 2):
+                zs.zero_adamw_step_tensors(*state, d_table, len(numels), total, torch.float16, 0, hs, lowp, 1e-3, 0.9,
+                                           0.95, 1e-8, 0.1, t, None, acc=acc if t == 2 else None, d_scale=d_scale)
             torch.cuda.synchronize()
-            outs.append(([t.cpu().view(torch.uint8).numpy() for t in (dst, ws1, ws2, acc, ws3, red, ws4)],
+            outs.append(([t.cpu().view(torch.uint8).numpy() for t in (dst, ws1, ws2, acc, ws3, red, ws4, ws5,
+                                                                      *state, lowp)],
                          flag.item()))
         (host_bufs, host_flag), (dev_bufs, dev_flag) = outs
         assert host_flag == dev_flag
